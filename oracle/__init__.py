@@ -1,0 +1,151 @@
+"""Reference oracle for the Kalman Linear Attention scan — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package. The product path (the CUDA library in
+``bayesian_filtering_linear_gb300``) never imports it, and this package never
+imports the product path.
+
+Contents
+--------
+* :func:`forward` — ctypes wrapper of ``kla_oracle.cpp``: the plain per-element
+  variance-form Kalman loop in fp64 (or fp32), multithreaded over heads.
+* :mod:`oracle.exact` — exact-rational information-form Möbius recursion and
+  dense Gaussian conditioning of the joint chain, used to pin the C++ loop.
+
+Source: "Technische Samenvatting: Kalman Linear Attention (KLA)"
+(gist.science/nl/paper/2602.10743), Methodologie §1 (model) and §2 (Möbius
+precision recursion, affine mean recursion).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kla_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libkla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, mutant: int = 0) -> str:
+    """Compile ``kla_oracle.cpp`` with g++ -O2 (no fast-math, no FMA
+    contraction, so x86-64 and aarch64 round identically) into ``_build/``.
+    ``mutant`` > 0 builds a copy with one planted mistake (tests only)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    lib = _LIB if mutant == 0 else os.path.join(_BUILD, f"libkla_oracle_mutant{mutant}.so")
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_SRC):
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+               "-fno-fast-math", "-ffp-contract=off", f"-DKLA_ORACLE_MUTANT={int(mutant)}",
+               _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, lib)
+    return lib
+
+
+def _declare(lib):
+    fp = ctypes.c_void_p
+    lib.kla_oracle_forward_f64.restype = ctypes.c_longlong
+    lib.kla_oracle_forward_f64.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 5 + [ctypes.c_int]
+    lib.kla_oracle_forward_f32.restype = ctypes.c_longlong
+    lib.kla_oracle_forward_f32.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 3 + [ctypes.c_int]
+    return lib
+
+
+_mutants = {}
+
+
+def _load(mutant: int = 0):
+    global _lib
+    with _lock:
+        if mutant:
+            if mutant not in _mutants:
+                _mutants[mutant] = _declare(ctypes.CDLL(build(mutant=mutant)))
+            return _mutants[mutant]
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            _lib = _declare(lib)
+    return _lib
+
+
+def _f32(x):
+    """Widen to a contiguous float32 numpy array (exact for bf16 / fp32 values)."""
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu", torch.float32).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, precision: str = "f64",
+            nthreads: int | None = None, heads=None, want_scales: bool = True,
+            _mutant: int = 0) -> dict:
+    """Run the oracle over every head (or the flat head indices in ``heads``).
+
+    Shapes: q, k, a, pbar ``[B,H,T,dk]``; v, lam_v ``[B,H,T,dv]``; lam0, eta0
+    ``[B,H,dk,dv]`` or None (λ0 = 1, η0 = 0). With ``heads`` given, the
+    selected heads are gathered into a ``[n,1,...]`` batch and the returned
+    arrays have that leading shape.
+
+    Returns a dict with ``y [B,H,T,dv]``, ``lamT``, ``etaT`` ``[B,H,dk,dv]``,
+    (fp64 only) the condition scales ``y_scale`` and ``eta_scale``, and
+    ``violations`` — the count of invariant violations (0 expected).
+    """
+    arrs = [_f32(x) for x in (q, k, v, lam_v, a, pbar)]
+    l0, e0 = _f32(lam0), _f32(eta0)
+    B, H, T, dk = arrs[0].shape
+    dv = arrs[2].shape[-1]
+    if heads is not None:
+        idx = np.asarray(list(heads), dtype=np.int64)
+
+        def sel(x):
+            return None if x is None else np.ascontiguousarray(x.reshape((B * H,) + x.shape[2:])[idx][:, None])
+        arrs = [sel(x) for x in arrs]
+        l0, e0 = sel(l0), sel(e0)
+        B, H = len(idx), 1
+    for x, last in zip(arrs, (dk, dk, dv, dv, dk, dk)):
+        if x.shape != (B, H, T, last):
+            raise ValueError(f"bad input shape {x.shape}, expected {(B, H, T, last)}")
+    for s in (l0, e0):
+        if s is not None and s.shape != (B, H, dk, dv):
+            raise ValueError(f"bad state shape {s.shape}")
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    lib = _load(_mutant)
+    dt = np.float64 if precision == "f64" else np.float32
+    y = np.empty((B, H, T, dv), dt)
+    lamT = np.empty((B, H, dk, dv), dt)
+    etaT = np.empty((B, H, dk, dv), dt)
+    out = {"y": y, "lamT": lamT, "etaT": etaT}
+    if precision == "f64":
+        ys = np.empty((B, H, T, dv), np.float64) if want_scales else None
+        es = np.empty((B, H, dk, dv), np.float64) if want_scales else None
+        nv = lib.kla_oracle_forward_f64(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0),
+                                        B, H, T, dk, dv, _ptr(y), _ptr(lamT), _ptr(etaT),
+                                        _ptr(ys), _ptr(es), int(nthreads))
+        if want_scales:
+            out["y_scale"], out["eta_scale"] = ys, es
+    elif precision == "f32":
+        nv = lib.kla_oracle_forward_f32(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0),
+                                        B, H, T, dk, dv, _ptr(y), _ptr(lamT), _ptr(etaT),
+                                        int(nthreads))
+    else:
+        raise ValueError("precision must be 'f64' or 'f32'")
+    if nv < 0:
+        raise ValueError("oracle rejected its arguments")
+    out["violations"] = int(nv)
+    return out
