@@ -1,0 +1,316 @@
+// C ABI of the KLA scan library: argument validation, the launch planner and
+// the entry points declared in include/kla.h. Host code only; the kernels are
+// in kla_forward.cu (sequence scan, chunk compose, chunk carry) and
+// kla_step.cu (decode step).
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "kla.h"
+#include "kla_launch.h"
+
+namespace {
+
+using kla::Plan;
+
+constexpr size_t kMaxSmem = 227 * 1024;
+constexpr int kChunkAlign = 32;  // chunk lengths are multiples of the largest tile
+
+bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t io_size(int io) { return io == KLA_BF16 ? 2 : 4; }
+
+// Shape checks shared by every entry point that takes (B, H, T, dk, dv).
+kla_status check_shape(int B, int H, int T, int dk, int dv) {
+  if (B < 0 || H < 0 || T < 0) return KLA_ERR_INVALID_ARG;
+  if (!valid_d(dk) || !valid_d(dv)) return KLA_ERR_UNSUPPORTED_SHAPE;
+  const long long bh = (long long)B * H;
+  if (bh > INT_MAX) return KLA_ERR_UNSUPPORTED_SHAPE;
+  // Element counts must fit comfortably in 64-bit offsets.
+  if (bh > 0 && (long long)T > (1LL << 46) / (bh * 128)) return KLA_ERR_UNSUPPORTED_SHAPE;
+  return KLA_OK;
+}
+
+kla_status check_options(const kla_options* opt) {
+  if (!opt) return KLA_OK;
+  if (opt->strategy < KLA_AUTO || opt->strategy > KLA_CHUNKED) return KLA_ERR_INVALID_ARG;
+  if (opt->chunk_len < 0 || opt->chunk_len % kChunkAlign != 0) return KLA_ERR_INVALID_ARG;
+  return KLA_OK;
+}
+
+// ---- planner -----------------------------------------------------------------
+//
+// Cost model in sub-partition (SMSP) cycles. A warp advancing one token does
+// RL·2·32 element-steps, each needing one MUFU reciprocal at 4 per SMSP-cycle.
+// Blocks of CC columns (CC/wc warps) are spread evenly over the SMs and a
+// block's warps over the 4 sub-partitions, so the busiest sub-partition
+// carries ceil(ceil(blocks/SMs) · warps/4) warps. Per-row coefficients cost
+// about 4.5 columns' worth of work per block; a sub-partition with a single
+// warp issues at ~0.7 of its rate (latency), two or more at ~0.9. Chunk
+// composition costs ~1.6× a scan step. Fixed costs: ~2 tiles of pipeline fill
+// per block, ~4000 cycles per kernel launch, and the carry kernel's traffic
+// (9 floats per element per chunk at ~6.6 TB/s, ~1.95 GHz).
+constexpr double kLaunchCycles = 4000.0;
+constexpr double kCyclesPerByte = 1.95e9 / 6.6e12;
+
+struct Candidate {
+  int cc;
+  double cost;
+};
+
+int blocks_per_sm_limit(int dk, int io, int cc, int tile, int wc) {
+  const size_t smem = kla::forward_smem_bytes(dk, io, cc, tile);
+  if (smem > kMaxSmem) return 0;
+  const int by_smem = (int)((kMaxSmem + 1024) / (smem + 1024));
+  const int by_threads = 2048 / (32 * (cc / wc));
+  return std::max(0, std::min(by_smem, by_threads));
+}
+
+double pass_cost(long long bh, int dk, int dv, int io, int cc, int tile, int wc, int num_sms, long long blocks_z,
+                 double step_cost, long long tokens) {
+  const int bps = blocks_per_sm_limit(dk, io, cc, tile, wc);
+  if (bps == 0) return INFINITY;
+  const long long blocks = bh * (dv / cc) * blocks_z;
+  const long long per_sm = (blocks + num_sms - 1) / num_sms;
+  const long long waves = (per_sm + bps - 1) / bps;
+  const long long resident = std::min<long long>(per_sm, bps);
+  const long long warps_sm = resident * (cc / wc);
+  const long long warps_smsp = (warps_sm + 3) / 4;
+  const double eff = warps_smsp >= 2 ? 0.9 : 0.7;
+  const double warp_token = 8.0 * kla::rows_per_lane_for(dk) * 2;  // cycles per warp per token
+  return kLaunchCycles + (double)waves * (double)(tokens + 2 * tile) * (double)warps_smsp * warp_token *
+                             (step_cost + 4.5 / cc) / eff;
+}
+
+kla_status make_plan(int B, int H, int T, int dk, int dv, int io, const kla_options* opt, int num_sms,
+                     Plan* out) {
+  kla_status st = check_shape(B, H, T, dk, dv);
+  if (st != KLA_OK) return st;
+  if ((st = check_options(opt)) != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  if (num_sms < 1) return KLA_ERR_INVALID_ARG;
+  const int strategy = opt ? opt->strategy : KLA_AUTO;
+  const int fixed_len = opt ? opt->chunk_len : 0;
+  const long long bh = (long long)B * H;
+  const long long elems = bh * dk * dv;
+  const int wc = kla::warp_cols(dk);
+  const int tile = kla::tile_for(dk, io);
+  const int cc_min = std::max<int>(wc, (int)(16 / io_size(io)));
+  const int cc_max = std::min(dv, 8 * wc);
+
+  auto best_cc = [&](int num_chunks, int chunk_len, double* cost_out) {
+    Candidate best{cc_min, INFINITY};
+    for (int cc = cc_max; cc >= cc_min; cc /= 2) {
+      double c = pass_cost(bh, dk, dv, io, cc, tile, wc, num_sms, num_chunks, 1.0, chunk_len);
+      if (num_chunks > 1) {
+        c += pass_cost(bh, dk, dv, io, cc, tile, wc, num_sms, num_chunks - 1, 1.6, chunk_len);
+        c += kLaunchCycles + kCyclesPerByte * 36.0 * (double)num_chunks * (double)elems;
+      }
+      if (c < best.cost) best = {cc, c};
+    }
+    *cost_out = best.cost;
+    return best.cc;
+  };
+
+  Plan p{};
+  p.rows_per_lane = kla::rows_per_lane_for(dk);
+  p.tile = tile;
+  const long long Tl = std::max(T, 1);
+  double seq_cost = 0.0;
+  const int seq_cc = best_cc(1, (int)Tl, &seq_cost);
+  p.strategy = KLA_SEQUENTIAL;
+  p.chunk_len = (int)Tl;
+  p.num_chunks = 1;
+  p.cols_per_block = seq_cc;
+
+  if (strategy == KLA_CHUNKED || strategy == KLA_AUTO) {
+    int best_len = 0, best_cc_c = 0;
+    double best_cost = INFINITY;
+    auto consider = [&](long long len) {
+      len = ((len + kChunkAlign - 1) / kChunkAlign) * kChunkAlign;
+      if (len < kChunkAlign) len = kChunkAlign;
+      const long long S = (Tl + len - 1) / len;
+      if (S < 2 || S > 65535) return;
+      double c = 0.0;
+      const int cc = best_cc((int)S, (int)len, &c);
+      if (c < best_cost) { best_cost = c; best_len = (int)len; best_cc_c = cc; }
+    };
+    if (fixed_len > 0) {
+      consider(fixed_len);
+    } else {
+      for (int S = 2; S <= 256; S = S < 8 ? S + 1 : S * 2) consider((Tl + S - 1) / S);
+    }
+    const bool take = strategy == KLA_CHUNKED ? best_len > 0 : (best_len > 0 && best_cost < seq_cost);
+    if (take) {
+      p.strategy = KLA_CHUNKED;
+      p.chunk_len = best_len;
+      p.num_chunks = (int)((Tl + best_len - 1) / best_len);
+      p.cols_per_block = best_cc_c;
+    }
+  }
+  p.ws_bytes = p.strategy == KLA_CHUNKED ? kla::chunk_workspace_bytes(elems, p.num_chunks) : 0;
+  *out = p;
+  return KLA_OK;
+}
+
+// Per-device SM count, queried once.
+std::atomic<int> g_sms[256];
+
+kla_status device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KLA_ERR_CUDA;
+  if (dev < 0 || dev >= 256) return KLA_ERR_CUDA;
+  int n = g_sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return KLA_ERR_CUDA;
+    g_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  *sms = n;
+  return KLA_OK;
+}
+
+bool overlaps_partially(const void* x, const void* y, size_t bytes) {
+  if (!x || !y || x == y) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(y);
+  return a < b + bytes && b < a + bytes;
+}
+
+void fill_info(const Plan& p, kla_plan_info* out) {
+  out->strategy = p.strategy;
+  out->chunk_len = p.chunk_len;
+  out->num_chunks = p.num_chunks;
+  out->cols_per_block = p.cols_per_block;
+  out->workspace_bytes = p.ws_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kla_status_string(kla_status s) {
+  switch (s) {
+    case KLA_OK: return "ok";
+    case KLA_ERR_INVALID_ARG: return "invalid argument";
+    case KLA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (d_k, d_v must be 16, 32, 64 or 128)";
+    case KLA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case KLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KLA_ERR_CUDA: return "CUDA error";
+    case KLA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int kla_version(void) { return 100; }
+
+kla_status kla_plan_for_sms(int B, int H, int T, int dk, int dv, kla_dtype io, const kla_options* opt,
+                            int num_sms, kla_plan_info* out) {
+  if (!out) return KLA_ERR_INVALID_ARG;
+  Plan p{};
+  const kla_status st = make_plan(B, H, T, dk, dv, io, opt, num_sms, &p);
+  if (st == KLA_OK) fill_info(p, out);
+  return st;
+}
+
+kla_status kla_plan(int B, int H, int T, int dk, int dv, kla_dtype io, const kla_options* opt,
+                    kla_plan_info* out) {
+  if (!out) return KLA_ERR_INVALID_ARG;
+  Plan p{};
+  kla_status st = make_plan(B, H, T, dk, dv, io, opt, 1, &p);  // validates first, no CUDA call
+  if (st != KLA_OK) return st;
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  if ((st = make_plan(B, H, T, dk, dv, io, opt, sms, &p)) != KLA_OK) return st;
+  fill_info(p, out);
+  return KLA_OK;
+}
+
+size_t kla_forward_workspace_size(int B, int H, int T, int dk, int dv, const kla_options* opt) {
+  Plan p{};
+  if (make_plan(B, H, T, dk, dv, KLA_F32, opt, 1, &p) != KLA_OK) return (size_t)-1;
+  int sms = 0;
+  if (device_sms(&sms) != KLA_OK) return (size_t)-1;
+  size_t ws = 0;
+  for (int io = KLA_F32; io <= KLA_BF16; ++io) {
+    if (make_plan(B, H, T, dk, dv, io, opt, sms, &p) != KLA_OK) return (size_t)-1;
+    ws = std::max(ws, p.ws_bytes);
+  }
+  return ws;
+}
+
+kla_status kla_forward(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                       const void* pbar, const float* lam0, const float* eta0, void* y, float* lamT,
+                       float* etaT, int B, int H, int T, int dk, int dv, kla_dtype io, void* workspace,
+                       size_t ws_bytes, const kla_options* opt, void* stream) {
+  // ---- validation: no CUDA call before it passes ---------------------------
+  kla_status st = check_shape(B, H, T, dk, dv);
+  if (st != KLA_OK) return st;
+  if ((st = check_options(opt)) != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  const long long tokens = bh * T;
+  if ((lam0 == nullptr) != (eta0 == nullptr)) return KLA_ERR_INVALID_ARG;
+  if ((lamT == nullptr) != (etaT == nullptr)) return KLA_ERR_INVALID_ARG;
+  if (tokens > 0 && (!q || !k || !v || !lam_v || !a || !pbar || !y)) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  const size_t state_bytes = (size_t)bh * dk * dv * sizeof(float);
+  if (overlaps_partially(lamT, lam0, state_bytes) || overlaps_partially(etaT, eta0, state_bytes) ||
+      overlaps_partially(lamT, eta0, state_bytes) || overlaps_partially(etaT, lam0, state_bytes) ||
+      (lamT && lamT == (const float*)eta0) || (etaT && etaT == (const float*)lam0))
+    return KLA_ERR_INVALID_ARG;
+  if (lamT && overlaps_partially(lamT, etaT, state_bytes)) return KLA_ERR_INVALID_ARG;
+  if (lamT && lamT == etaT) return KLA_ERR_INVALID_ARG;
+  if (bh == 0) return KLA_OK;
+
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  Plan p{};
+  if ((st = make_plan(B, H, T, dk, dv, io, opt, sms, &p)) != KLA_OK) return st;
+  if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return KLA_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return KLA_ERR_MISALIGNED;
+
+  kla::ForwardArgs f{q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, (int)io};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (T == 0) {
+    e = kla::launch_init_state(f, s);
+  } else if (p.strategy == KLA_SEQUENTIAL) {
+    e = kla::launch_forward(f, p, nullptr, s);
+  } else {
+    const long long elems = bh * dk * dv;
+    float* maps = reinterpret_cast<float*>(workspace);
+    float* starts = maps + (size_t)7 * (p.num_chunks - 1) * elems;
+    e = kla::launch_compose(f, p, maps, s);
+    if (e == cudaSuccess) e = kla::launch_carry(f, p, maps, starts, s);
+    if (e == cudaSuccess) e = kla::launch_forward(f, p, starts, s);
+  }
+  return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_step(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                    const void* pbar, float* lam, float* eta, void* y, int B, int H, int dk, int dv, kla_dtype io,
+                    void* stream) {
+  kla_status st = check_shape(B, H, 1, dk, dv);
+  if (st != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  if (bh > 0 && (!q || !k || !v || !lam_v || !a || !pbar || !lam || !eta || !y)) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, lam_v, a, pbar, lam, eta, y};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  const size_t state_bytes = (size_t)bh * dk * dv * sizeof(float);
+  if (lam && (lam == eta || overlaps_partially(lam, eta, state_bytes))) return KLA_ERR_INVALID_ARG;
+  if (bh == 0) return KLA_OK;
+  kla::StepArgs sa{q, k, v, lam_v, a, pbar, lam, eta, y, B, H, dk, dv, (int)io};
+  const cudaError_t e = kla::launch_step(sa, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+}  // extern "C"

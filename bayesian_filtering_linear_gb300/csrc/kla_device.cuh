@@ -1,0 +1,92 @@
+// Device-side helpers shared by the KLA kernels (sm_103a): packed fp32x2
+// arithmetic, the hardware reciprocal, I/O dtype conversion and 16-byte
+// asynchronous global→shared copies.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace kla {
+
+// k² is raised by 2^-40 before it is used as a scale, and a is floored at
+// 2^-40, so every scaled quantity in the forward recursion stays a normal
+// fp32 number (see kla_forward.cu). For |k| ≥ 2^-8 the raised k² rounds back
+// to k² exactly; below that it adds 2^-40·Λ^v to the observation precision.
+constexpr float kK2Floor = 0x1p-40f;
+constexpr float kAMin = 0x1p-40f;
+
+// ---- packed fp32x2 (one instruction issues two fp32 lanes) -------------------
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(f2 v) {
+  float lo;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(f2 v) {
+  float hi;
+  asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Hardware approximate reciprocal (one MUFU op, ≤ 1 ulp off for normal input).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ f2 f2_rcp(f2 d) {
+  return f2_make(rcp_approx(f2_lo(d)), rcp_approx(f2_hi(d)));
+}
+
+// ---- I/O dtypes ------------------------------------------------------------
+template <typename IO>
+__device__ __forceinline__ float to_f32(IO x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename IO>
+__device__ __forceinline__ IO from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---- 16-byte asynchronous copies (global → shared, L2-only caching) ---------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem_dst)), "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+}  // namespace kla

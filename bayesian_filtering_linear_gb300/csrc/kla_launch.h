@@ -1,0 +1,59 @@
+// Host-side interface between the C ABI (kla_api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kla {
+
+enum IoType { IO_F32 = 0, IO_BF16 = 1 };
+
+struct ForwardArgs {
+  const void *q, *k, *v, *lam_v, *a, *pbar;
+  const float *lam0, *eta0;
+  void* y;
+  float *lamT, *etaT;
+  int B, H, T, dk, dv;
+  int io;  // IoType
+};
+
+// Launch geometry shared by the planner and the launchers.
+struct Plan {
+  int strategy;        // 1 sequential, 2 chunked
+  int chunk_len;       // tokens per chunk (multiple of the tile length)
+  int num_chunks;
+  int cols_per_block;  // CC: d_v columns per thread block
+  int rows_per_lane;   // RL: d_k rows held by one lane
+  int tile;            // TC: tokens staged per shared-memory tile
+  size_t ws_bytes;
+};
+
+// Geometry constants of the sequential / apply kernel.
+int rows_per_lane_for(int dk);
+int tile_for(int dk, int io);
+int warp_cols(int dk);  // columns covered by one warp
+size_t forward_smem_bytes(int dk, int io, int cc, int tile);
+size_t compose_smem_bytes(int dk, int io, int cc, int tile);
+
+// Workspace layout for the chunked path (fp32 elements):
+//   maps   [S-1][7][B·H·dk·dv]  per-chunk homogeneous maps (A,B,C,D,E,F,G)
+//   starts [S][2][B·H·dk·dv]    chunk-start (P, μ)
+size_t chunk_workspace_bytes(long long elems, int num_chunks);
+
+cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s);
+cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cudaStream_t s);
+cudaError_t launch_carry(const ForwardArgs& f, const Plan& p, const float* maps, float* starts,
+                         cudaStream_t s);
+cudaError_t launch_init_state(const ForwardArgs& f, cudaStream_t s);
+
+struct StepArgs {
+  const void *q, *k, *v, *lam_v, *a, *pbar;
+  float *lam, *eta;
+  void* y;
+  int B, H, dk, dv;
+  int io;
+};
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+
+}  // namespace kla

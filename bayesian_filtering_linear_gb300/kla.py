@@ -1,0 +1,186 @@
+"""Thin ctypes binding of ``libkla.so`` (the C ABI in ``include/kla.h``).
+
+Argument marshalling only: tensors are checked for device, dtype and layout,
+outputs and workspace are allocated with torch when not given, and the raw
+device pointers plus torch's current CUDA stream are passed to the library.
+Every step of the scan runs in the library's CUDA kernels; there is no other
+implementation here. If the library is missing this module fails to import.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkla.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+F32, BF16 = 0, 1
+AUTO, SEQUENTIAL, CHUNKED = 0, 1, 2
+_STRATEGIES = {"auto": AUTO, "sequential": SEQUENTIAL, "chunked": CHUNKED}
+_IO = {torch.float32: F32, torch.bfloat16: BF16}
+# Every function the header declares, for the export check.
+EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
+           "kla_status_string", "kla_version")
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("num_chunks", ctypes.c_int),
+                ("cols_per_block", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python -m bayesian_filtering_linear_gb300.build` "
+                          "(needs nvcc) — there is no fallback implementation")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.kla_status_string.restype = ctypes.c_char_p
+    lib.kla_status_string.argtypes = [i]
+    lib.kla_version.restype = i
+    lib.kla_version.argtypes = []
+    lib.kla_plan.restype = i
+    lib.kla_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
+    lib.kla_plan_for_sms.restype = i
+    lib.kla_plan_for_sms.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Options), i, ctypes.POINTER(PlanInfo)]
+    lib.kla_forward_workspace_size.restype = sz
+    lib.kla_forward_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(Options)]
+    lib.kla_forward.restype = i
+    lib.kla_forward.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, ctypes.POINTER(Options), vp]
+    lib.kla_step.restype = i
+    lib.kla_step.argtypes = [vp] * 9 + [i] * 5 + [vp]
+    return lib
+
+
+LIB = _load()
+
+
+class KlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {LIB.kla_status_string(status).decode()} (status {status})")
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise KlaError(status, where)
+
+
+def status_string(status: int) -> str:
+    return LIB.kla_status_string(status).decode()
+
+
+def options(strategy: str | int = "auto", chunk_len: int = 0) -> Options:
+    s = _STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
+    return Options(s, int(chunk_len))
+
+
+def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strategy: str | int = "auto",
+         chunk_len: int = 0, num_sms: int | None = None) -> dict:
+    """The launch plan kla_forward uses (for the current device, or for a
+    device with ``num_sms`` SMs without touching CUDA)."""
+    io_code = {"f32": F32, "bf16": BF16}.get(io, io)
+    info = PlanInfo()
+    opt = options(strategy, chunk_len)
+    if num_sms is None:
+        st = LIB.kla_plan(B, H, T, dk, dv, io_code, ctypes.byref(opt), ctypes.byref(info))
+    else:
+        st = LIB.kla_plan_for_sms(B, H, T, dk, dv, io_code, ctypes.byref(opt), int(num_sms), ctypes.byref(info))
+    _check(st, "kla_plan")
+    return {"strategy": {SEQUENTIAL: "sequential", CHUNKED: "chunked"}[info.strategy],
+            "chunk_len": info.chunk_len, "num_chunks": info.num_chunks,
+            "cols_per_block": info.cols_per_block, "workspace_bytes": int(info.workspace_bytes)}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None, etaT=None,
+            strategy: str | int = "auto", chunk_len: int = 0, workspace=None, stream=None,
+            final_state: bool = True):
+    """Whole-sequence KLA scan. Returns ``(y, lamT, etaT)`` (the last two are
+    None when ``final_state`` is False and none were given)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    dt = q.dtype
+    if dt not in _IO:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    for name, t, last in (("q", q, dk), ("k", k, dk), ("a", a, dk), ("pbar", pbar, dk),
+                          ("v", v, dv), ("lam_v", lam_v, dv)):
+        _need(t, name, dt, (B, H, T, last), dev)
+    st_shape = (B, H, dk, dv)
+    for name, t in (("lam0", lam0), ("eta0", eta0), ("lamT", lamT), ("etaT", etaT)):
+        if t is not None:
+            _need(t, name, torch.float32, st_shape, dev)
+    if y is None:
+        y = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    else:
+        _need(y, "y", dt, (B, H, T, dv), dev)
+    if final_state and lamT is None:
+        lamT = torch.empty(st_shape, dtype=torch.float32, device=dev)
+        etaT = torch.empty(st_shape, dtype=torch.float32, device=dev)
+    opt = options(strategy, chunk_len)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            info = PlanInfo()
+            _check(LIB.kla_plan(B, H, T, dk, dv, _IO[dt], ctypes.byref(opt), ctypes.byref(info)), "kla_plan")
+            nbytes = int(info.workspace_bytes)
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = LIB.kla_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam0), _ptr(eta0),
+                             _ptr(y), _ptr(lamT), _ptr(etaT), B, H, T, dk, dv, _IO[dt],
+                             _ptr(workspace), ws_bytes, ctypes.byref(opt), _stream(stream))
+    _check(st, "kla_forward")
+    return y, lamT, etaT
+
+
+def step(q, k, v, lam_v, a, pbar, lam, eta, *, y=None, stream=None):
+    """One decode step: q, k, a, pbar ``[B,H,dk]``, v, lam_v ``[B,H,dv]``;
+    updates the fp32 state (lam, eta) ``[B,H,dk,dv]`` in place; returns y."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dt not in _IO:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    for name, t, last in (("q", q, dk), ("k", k, dk), ("a", a, dk), ("pbar", pbar, dk),
+                          ("v", v, dv), ("lam_v", lam_v, dv)):
+        _need(t, name, dt, (B, H, last), dev)
+    _need(lam, "lam", torch.float32, (B, H, dk, dv), dev)
+    _need(eta, "eta", torch.float32, (B, H, dk, dv), dev)
+    if y is None:
+        y = torch.empty((B, H, dv), dtype=dt, device=dev)
+    else:
+        _need(y, "y", dt, (B, H, dv), dev)
+    with torch.cuda.device(dev):
+        st = LIB.kla_step(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam), _ptr(eta),
+                          _ptr(y), B, H, dk, dv, _IO[dt], _stream(stream))
+    _check(st, "kla_step")
+    return y

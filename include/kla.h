@@ -1,0 +1,134 @@
+/* kla.h — C ABI of the GB300 Kalman Linear Attention (KLA) scan library.
+ *
+ * The operation: "Technische Samenvatting: Kalman Linear Attention (KLA)"
+ * (gist.science/nl/paper/2602.10743). Methodologie §1 "Probabilistische
+ * Formulering" gives the model — an exactly discretised Ornstein–Uhlenbeck
+ * prior with process noise p̄_t, tokens observed through an operator k_t with
+ * value precision Λ^v_t, and a readout of the posterior mean through q_t.
+ * Methodologie §2 "Parallelisatie via Möbius-transformaties" gives the filter
+ * in information form: the precision is a Möbius map of the previous one,
+ *     λ_t = (α λ_{t-1} + β) / (γ λ_{t-1} + δ),
+ * these maps compose associatively (a prefix scan over T), and the
+ * information mean follows an affine map. "Belangrijkste Bijdragen" item 1
+ * fixes the diagonal structure: each head's d_k × d_v state elements are
+ * independent scalar filters.
+ *
+ * Per head (b, h), element (i, j) and token t, with c = k_{t,i}² Λ^v_{t,j}:
+ *     α = 1 + c p̄_{t,i},  β = c a_{t,i}²,  γ = p̄_{t,i},  δ = a_{t,i}²
+ *     λ_pred = λ_{t-1} / (a² + p̄ λ_{t-1})
+ *     λ_t = λ_pred + c                        (= the Möbius step above)
+ *     η_t = (a λ_pred / λ_{t-1}) η_{t-1} + k_{t,i} Λ^v_{t,j} v_{t,j}
+ *     y_{t,j} = Σ_i q_{t,i} η_{t,i,j} / λ_{t,i,j}
+ * (λ0, η0) is the belief before the first token; the readout of token t uses
+ * the posterior that includes token t.
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory and keeps no state beyond a per-device cache
+ *    of the SM count. Work is queued on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and the call returns without synchronising.
+ *  - Layout is contiguous row-major with no strides:
+ *      q, k, a, pbar : [B, H, T, d_k]     v, lam_v, y : [B, H, T, d_v]
+ *      lam0, eta0, lamT, etaT : [B, H, d_k, d_v], always fp32.
+ *    The I/O dtype (`io`) applies to q, k, v, lam_v, a, pbar and y.
+ *  - d_k and d_v must each be one of 16, 32, 64, 128; B, H ≥ 0 and T ≥ 0
+ *    (an empty batch or T = 0 is valid; T = 0 copies the initial state).
+ *  - Every array pointer must be 16-byte aligned.
+ *  - Arguments are validated before anything is launched; on error nothing is
+ *    queued and no CUDA call has been made. An asynchronous fault of an
+ *    earlier kernel is reported by a later call as KLA_ERR_CUDA.
+ *  - Domain (the caller's contract): 0 < a ≤ 1, p̄ ≥ 0, Λ^v ≥ 0, λ0 > 0. The
+ *    kernels raise a below 2^-40 to 2^-40 and add 2^-40 to k², which changes
+ *    results only below fp32 resolution for |k| ≥ 2^-8; other violations
+ *    give NaN/Inf and never a trap.
+ *  - Entry points are thread-safe; calls on one stream are ordered.
+ */
+#ifndef KLA_H_
+#define KLA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kla_status {
+  KLA_OK = 0,
+  KLA_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, bad enum    */
+  KLA_ERR_UNSUPPORTED_SHAPE = 2, /* d_k/d_v not in {16,32,64,128}, too large */
+  KLA_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned          */
+  KLA_ERR_WORKSPACE = 4,         /* workspace missing or smaller than needed */
+  KLA_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed      */
+  KLA_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up        */
+} kla_status;
+
+typedef enum kla_dtype { KLA_F32 = 0, KLA_BF16 = 1 } kla_dtype;
+
+/* Sequential-per-element scan over all T, or chunk-parallel over T
+ * (compose per-chunk maps, carry them across chunks, re-run each chunk). */
+typedef enum kla_strategy { KLA_AUTO = 0, KLA_SEQUENTIAL = 1, KLA_CHUNKED = 2 } kla_strategy;
+
+typedef struct kla_options {
+  int strategy;  /* kla_strategy */
+  int chunk_len; /* tokens per chunk for KLA_CHUNKED; 0 = automatic; multiple of 32 */
+} kla_options;
+
+/* The launch plan kla_forward would use for this shape on the current device. */
+typedef struct kla_plan_info {
+  int strategy;           /* KLA_SEQUENTIAL or KLA_CHUNKED (never AUTO)      */
+  int chunk_len;          /* tokens per chunk (T for the sequential path)    */
+  int num_chunks;         /* ceil(T / chunk_len)                              */
+  int cols_per_block;     /* d_v columns handled by one thread block          */
+  size_t workspace_bytes; /* device workspace kla_forward needs (0 if none)   */
+} kla_plan_info;
+
+/* Plan for the current CUDA device. Errors: INVALID_ARG (out NULL, negative
+ * size, bad strategy/chunk_len), UNSUPPORTED_SHAPE, CUDA (no device). */
+kla_status kla_plan(int B, int H, int T, int dk, int dv, kla_dtype io, const kla_options* opt,
+                    kla_plan_info* out);
+
+/* The same plan for a device with `num_sms` SMs (host-only; no CUDA call). */
+kla_status kla_plan_for_sms(int B, int H, int T, int dk, int dv, kla_dtype io,
+                            const kla_options* opt, int num_sms, kla_plan_info* out);
+
+/* Bytes of device workspace kla_forward needs on the current device for
+ * either I/O dtype; 0 when the plan needs none, (size_t)-1 if the arguments
+ * are invalid or no device is available. */
+size_t kla_forward_workspace_size(int B, int H, int T, int dk, int dv, const kla_options* opt);
+
+/* Whole-sequence scan (Methodologie §1–§2 of the summary cited above).
+ *   q, k, a, pbar [B,H,T,dk] and v, lam_v [B,H,T,dv] in `io`  (inputs)
+ *   lam0, eta0 [B,H,dk,dv] fp32; both NULL means λ0 = 1, η0 = 0; one NULL and
+ *     the other not is INVALID_ARG.
+ *   y [B,H,T,dv] in `io` (output; required unless B·H·T = 0)
+ *   lamT, etaT [B,H,dk,dv] fp32 final state (may be NULL; may alias lam0 /
+ *     eta0 exactly for an in-place update; partial overlap is not allowed).
+ *   workspace / ws_bytes: device scratch of at least
+ *     kla_forward_workspace_size() bytes (may be NULL when that is 0).
+ *   opt: NULL means KLA_AUTO with an automatic chunk length. */
+kla_status kla_forward(const void* q, const void* k, const void* v, const void* lam_v,
+                       const void* a, const void* pbar, const float* lam0, const float* eta0,
+                       void* y, float* lamT, float* etaT,
+                       int B, int H, int T, int dk, int dv, kla_dtype io,
+                       void* workspace, size_t ws_bytes, const kla_options* opt, void* stream);
+
+/* One recurrent decode step, identical in meaning to kla_forward with T = 1
+ * and the state updated in place (same summary, same sections).
+ *   q, k, a, pbar [B,H,dk] and v, lam_v [B,H,dv] in `io` (one token)
+ *   lam, eta [B,H,dk,dv] fp32, read and overwritten with the posterior
+ *   y [B,H,dv] in `io`. */
+kla_status kla_step(const void* q, const void* k, const void* v, const void* lam_v,
+                    const void* a, const void* pbar, float* lam, float* eta, void* y,
+                    int B, int H, int dk, int dv, kla_dtype io, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* kla_status_string(kla_status s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int kla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KLA_H_ */

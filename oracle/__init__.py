@@ -105,18 +105,21 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, precision: str = "
     (fp64 only) the condition scales ``y_scale`` and ``eta_scale``, and
     ``violations`` — the count of invariant violations (0 expected).
     """
+    if heads is not None:
+        # gather the selected heads first (before widening), as [n, 1, ...]
+        B0, H0 = q.shape[:2]
+        idx = list(heads)
+
+        def sel(x):
+            if x is None:
+                return None
+            flat = x.reshape((B0 * H0,) + tuple(x.shape[2:]))
+            return flat[idx][:, None] if not isinstance(flat, np.ndarray) else flat[np.asarray(idx)][:, None]
+        q, k, v, lam_v, a, pbar, lam0, eta0 = (sel(x) for x in (q, k, v, lam_v, a, pbar, lam0, eta0))
     arrs = [_f32(x) for x in (q, k, v, lam_v, a, pbar)]
     l0, e0 = _f32(lam0), _f32(eta0)
     B, H, T, dk = arrs[0].shape
     dv = arrs[2].shape[-1]
-    if heads is not None:
-        idx = np.asarray(list(heads), dtype=np.int64)
-
-        def sel(x):
-            return None if x is None else np.ascontiguousarray(x.reshape((B * H,) + x.shape[2:])[idx][:, None])
-        arrs = [sel(x) for x in arrs]
-        l0, e0 = sel(l0), sel(e0)
-        B, H = len(idx), 1
     for x, last in zip(arrs, (dk, dk, dv, dv, dk, dk)):
         if x.shape != (B, H, T, last):
             raise ValueError(f"bad input shape {x.shape}, expected {(B, H, T, last)}")

@@ -1,0 +1,151 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+``include/kla.h`` declares, rejects bad arguments with the documented status
+before making any CUDA call, and plans launches deterministically.
+
+Only argument combinations that fail validation are passed with placeholder
+pointers, so nothing here can reach a kernel even on a machine with a GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from bayesian_filtering_linear_gb300 import kla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kla.h")
+L = kla.LIB
+P = ctypes.c_void_p(0x10000)      # 16-byte aligned placeholder (never dereferenced)
+MIS = ctypes.c_void_p(0x10004)    # misaligned placeholder
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kla_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    declared = header_functions()
+    assert set(declared) == set(kla.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", kla.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = set(re.findall(r"\bT (kla_[a-z_]+)", out.stdout))
+    missing = [f for f in declared if f not in exported]
+    assert not missing, missing
+    for f in declared:
+        assert hasattr(L, f)
+
+
+def test_version_and_status_strings():
+    assert L.kla_version() == 100
+    for s in range(7):
+        assert kla.status_string(s)
+    assert "unknown" in kla.status_string(99)
+
+
+def fwd(B=1, H=1, T=8, dk=16, dv=16, io=kla.F32, ptrs=None, lam0=None, eta0=None, lamT=None, etaT=None,
+        ws=None, ws_bytes=0, opt=None):
+    ptrs = ptrs or {}
+    g = lambda n: ptrs.get(n, P)
+    return L.kla_forward(g("q"), g("k"), g("v"), g("lam_v"), g("a"), g("pbar"), lam0, eta0, g("y"), lamT, etaT,
+                         B, H, T, dk, dv, io, ws, ws_bytes, opt, None)
+
+
+@pytest.mark.parametrize("dk,dv", [(8, 16), (16, 24), (256, 16), (48, 64), (0, 16)])
+def test_unsupported_head_dims(dk, dv):
+    assert fwd(dk=dk, dv=dv) == kla.ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("B,H,T", [(-1, 1, 8), (1, -2, 8), (1, 1, -5)])
+def test_negative_sizes(B, H, T):
+    assert fwd(B=B, H=H, T=T) == kla.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "lam_v", "a", "pbar", "y"])
+def test_null_required_pointer(name):
+    assert fwd(ptrs={name: None}) == kla.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["q", "k", "v", "lam_v", "a", "pbar", "y"])
+def test_misaligned_pointer(name):
+    assert fwd(ptrs={name: MIS}) == kla.ERR_MISALIGNED
+
+
+def test_state_pointers_must_come_in_pairs_and_not_overlap():
+    assert fwd(lam0=P) == kla.ERR_INVALID_ARG
+    assert fwd(lamT=P) == kla.ERR_INVALID_ARG
+    assert fwd(lam0=P, eta0=MIS) == kla.ERR_MISALIGNED
+    a, b = ctypes.c_void_p(0x20000), ctypes.c_void_p(0x20000 + 16)
+    # 16x16 fp32 state = 1 KiB: lamT starting 16 bytes into lam0 is a partial overlap
+    assert fwd(lam0=a, eta0=ctypes.c_void_p(0x40000), lamT=b, etaT=ctypes.c_void_p(0x60000)) == kla.ERR_INVALID_ARG
+    assert fwd(lamT=a, etaT=a) == kla.ERR_INVALID_ARG
+
+
+def test_bad_io_and_options():
+    assert fwd(io=7) == kla.ERR_INVALID_ARG
+    assert fwd(opt=ctypes.byref(kla.Options(9, 0))) == kla.ERR_INVALID_ARG
+    assert fwd(opt=ctypes.byref(kla.Options(kla.CHUNKED, 48))) == kla.ERR_INVALID_ARG
+    assert fwd(opt=ctypes.byref(kla.Options(kla.CHUNKED, -32))) == kla.ERR_INVALID_ARG
+
+
+def test_empty_batch_is_ok_without_any_cuda_call():
+    assert fwd(B=0, ptrs={n: None for n in ("q", "k", "v", "lam_v", "a", "pbar", "y")}) == kla.OK
+    assert L.kla_step(None, None, None, None, None, None, None, None, None, 0, 4, 16, 16, kla.F32, None) == kla.OK
+
+
+def test_step_validation():
+    s = lambda **kw: L.kla_step(*(kw.get(n, P) for n in ("q", "k", "v", "lam_v", "a", "pbar", "lam", "eta", "y")),
+                                kw.get("B", 1), 1, kw.get("dk", 16), 16, kw.get("io", kla.F32), None)
+    assert s(dk=20) == kla.ERR_UNSUPPORTED_SHAPE
+    assert s(lam=None) == kla.ERR_INVALID_ARG
+    assert s(y=MIS) == kla.ERR_MISALIGNED
+    assert s(io=3) == kla.ERR_INVALID_ARG
+    assert s(B=-1) == kla.ERR_INVALID_ARG
+    assert s(lam=P, eta=P) == kla.ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_arguments_without_a_device_report_cuda_error():
+    # Validation passes, so the first CUDA call (device query) fails cleanly.
+    assert fwd() == kla.ERR_CUDA
+    info = kla.PlanInfo()
+    assert L.kla_plan(1, 1, 8, 16, 16, kla.F32, None, ctypes.byref(info)) == kla.ERR_CUDA
+    assert L.kla_forward_workspace_size(1, 1, 8, 16, 16, None) == ctypes.c_size_t(-1).value
+
+
+def test_planner_headline_shape_is_sequential_on_152_sms():
+    p = kla.plan(8, 16, 4096, 64, 64, "bf16", num_sms=152)
+    assert p["strategy"] == "sequential" and p["num_chunks"] == 1 and p["workspace_bytes"] == 0
+    assert 64 % p["cols_per_block"] == 0
+
+
+def test_planner_low_parallelism_goes_chunked_and_sizes_workspace():
+    p = kla.plan(1, 2, 16384, 64, 64, "bf16", num_sms=152)
+    assert p["strategy"] == "chunked"
+    S, elems = p["num_chunks"], 2 * 64 * 64
+    assert p["chunk_len"] % 32 == 0 and S == -(-16384 // p["chunk_len"]) and S >= 2
+    assert p["workspace_bytes"] == (7 * (S - 1) + 2 * S) * elems * 4
+
+
+def test_planner_forced_strategies_and_chunk_len():
+    seq = kla.plan(1, 2, 16384, 64, 64, "f32", strategy="sequential", num_sms=152)
+    assert seq["strategy"] == "sequential" and seq["workspace_bytes"] == 0
+    ch = kla.plan(8, 16, 4096, 64, 64, "bf16", strategy="chunked", chunk_len=1024, num_sms=152)
+    assert ch["strategy"] == "chunked" and ch["chunk_len"] == 1024 and ch["num_chunks"] == 4
+    # a chunk as long as the sequence leaves nothing to parallelise: sequential
+    one = kla.plan(1, 1, 64, 16, 16, "f32", strategy="chunked", chunk_len=64, num_sms=152)
+    assert one["strategy"] == "sequential"
+    with pytest.raises(kla.KlaError):
+        kla.plan(1, 1, 64, 16, 16, "f32", strategy="chunked", chunk_len=40, num_sms=152)
+
+
+@pytest.mark.parametrize("dk,dv,io", [(16, 16, "f32"), (32, 128, "bf16"), (128, 16, "f32"), (128, 128, "bf16"),
+                                      (64, 32, "f32")])
+def test_planner_blocks_fit_the_hardware(dk, dv, io):
+    for B, H, T in [(1, 1, 33), (4, 8, 2048), (1, 16, 65536), (256, 16, 1)]:
+        p = kla.plan(B, H, T, dk, dv, io, num_sms=152)
+        cc = p["cols_per_block"]
+        assert dv % cc == 0 and cc * (2 if io == "bf16" else 4) % 16 == 0
