@@ -63,17 +63,18 @@ struct Candidate {
   double cost;
 };
 
-int blocks_per_sm_limit(int dk, int io, int cc, int tile, int wc) {
-  const size_t smem = kla::forward_smem_bytes(dk, io, cc, tile);
+int blocks_per_sm_limit(int dk, int io, int cc, int tile, int wc, bool compose) {
+  const size_t smem = compose ? kla::compose_smem_bytes(dk, io, cc, tile) : kla::forward_smem_bytes(dk, io, cc, tile);
   if (smem > kMaxSmem) return 0;
   const int by_smem = (int)((kMaxSmem + 1024) / (smem + 1024));
   const int by_threads = 2048 / (32 * (cc / wc));
+  if (32 * (cc / wc) > kla::max_threads()) return 0;
   return std::max(0, std::min(by_smem, by_threads));
 }
 
 double pass_cost(long long bh, int dk, int dv, int io, int cc, int tile, int wc, int num_sms, long long blocks_z,
                  double step_cost, long long tokens) {
-  const int bps = blocks_per_sm_limit(dk, io, cc, tile, wc);
+  const int bps = blocks_per_sm_limit(dk, io, cc, tile, wc, step_cost > 1.0);
   if (bps == 0) return INFINITY;
   const long long blocks = bh * (dv / cc) * blocks_z;
   const long long per_sm = (blocks + num_sms - 1) / num_sms;
@@ -101,7 +102,7 @@ kla_status make_plan(int B, int H, int T, int dk, int dv, int io, const kla_opti
   const int wc = kla::warp_cols(dk);
   const int tile = kla::tile_for(dk, io);
   const int cc_min = std::max<int>(wc, (int)(16 / io_size(io)));
-  const int cc_max = std::min(dv, 8 * wc);
+  const int cc_max = std::min(dv, kla::max_threads() / 32 * wc);
 
   auto best_cc = [&](int num_chunks, int chunk_len, double* cost_out) {
     Candidate best{cc_min, INFINITY};

@@ -1,0 +1,157 @@
+// Pieces shared by the sequence kernels (scan and chunk composition): launch
+// parameters, the lane geometry and the asynchronous staging of input tiles.
+#pragma once
+
+#include "kla_device.cuh"
+#include "kla_launch.h"
+
+namespace kla {
+
+#ifndef KLA_CL
+#define KLA_CL 2
+#endif
+#ifndef KLA_MAXT
+#define KLA_MAXT 256
+#endif
+#ifndef KLA_RL64
+#define KLA_RL64 8
+#endif
+#ifndef KLA_UNROLL
+#define KLA_UNROLL 2
+#endif
+
+constexpr int CL = KLA_CL;             // d_v columns per lane (2 or 4)
+constexpr int kMaxThreads = KLA_MAXT;  // per block (256 leaves up to 255 registers per thread)
+constexpr int kUnroll = KLA_UNROLL;    // token-loop unroll factor of the scan
+
+// Rows per lane for a head size (compile-time twin of rows_per_lane_for()).
+template <int DK>
+struct RowsPerLane {
+  static constexpr int value = DK <= 32 ? 4 : (DK == 64 ? KLA_RL64 : 8);
+};
+
+// A lane owns RL rows × CL columns of one head; rows are paired so that one
+// packed fp32x2 instruction serves two rows. Rows vary slowest across lanes,
+// so the eight lanes of a quarter-warp share rows and per-row coefficient
+// loads from shared memory are broadcasts.
+template <int DK, int RL>
+struct Geo {
+  static constexpr int LANES_I = DK / RL;       // lanes along rows
+  static constexpr int LANES_J = 32 / LANES_I;  // lanes along columns
+  static constexpr int WC = LANES_J * CL;       // columns per warp
+  static constexpr int XR = CL == 4 ? 2 : 1;    // exchange rounds of the readout reduction
+  static constexpr int NP = LANES_I / CL;       // partial sums per output left for shared memory
+  static_assert(LANES_I >= CL && LANES_I <= 32 && RL % 4 == 0 && (CL == 2 || CL == 4), "unsupported geometry");
+};
+
+struct KernelParams {
+  const void *q, *k, *v, *lam_v, *a, *pbar;
+  const float *lam0, *eta0;
+  const float* starts;  // [S][2][elems] chunk-start (P, μ), or nullptr
+  float* maps;          // compose output [S-1][7][elems]
+  void* y;
+  float *lamT, *etaT;
+  int T, dv, chunk_len, cc, log2cc;
+  long long elems;  // B·H·dk·dv
+};
+
+// One staged tile of raw inputs: the four per-row arrays q, k, a, p̄
+// ([TC][DK] each, contiguous in global memory) followed by the two per-column
+// arrays v, Λ^v ([TC][cc], rows dv apart in global memory).
+template <typename IO, int DK, int TC>
+struct RawTile {
+  __host__ __device__ static constexpr size_t row_bytes() { return (size_t)TC * DK * sizeof(IO); }
+  __host__ __device__ static size_t col_bytes(int cc) { return (size_t)TC * cc * sizeof(IO); }
+  __host__ __device__ static size_t bytes(int cc) { return 4 * row_bytes() + 2 * col_bytes(cc); }
+};
+
+// Queue 16-byte asynchronous copies of tokens [t0, t0 + tl) of this block's
+// inputs into the raw tile at `dst`.
+template <typename IO, int DK, int TC>
+__device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* dst, long long bh, int jb, int t0,
+                                          int tl) {
+  using R = RawTile<IO, DK, TC>;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const size_t row_i = (size_t)DK * sizeof(IO);
+  const int chunks_i = (int)(tl * row_i / 16);
+  const size_t base_i = ((size_t)bh * p.T + t0) * row_i;
+#pragma unroll
+  for (int arr = 0; arr < 4; ++arr) {
+    const char* src = (const char*)(arr == 0 ? p.q : arr == 1 ? p.k : arr == 2 ? p.a : p.pbar) + base_i;
+    unsigned char* d = dst + arr * R::row_bytes();
+    for (int c = tid; c < chunks_i; c += nthr) cp_async16(d + (size_t)c * 16, src + (size_t)c * 16);
+  }
+  const int cpr = (int)(p.cc * sizeof(IO) / 16);  // 16-byte chunks per staged row
+  const int chunks_j = tl * cpr;
+  const size_t row_j = (size_t)p.dv * sizeof(IO);
+  const size_t base_j = ((size_t)bh * p.T + t0) * row_j + (size_t)jb * sizeof(IO);
+#pragma unroll
+  for (int arr = 0; arr < 2; ++arr) {
+    const char* src = (const char*)(arr == 0 ? p.v : p.lam_v) + base_j;
+    unsigned char* d = dst + 4 * R::row_bytes() + arr * R::col_bytes(p.cc);
+    for (int c = tid; c < chunks_j; c += nthr) {
+      const int row = c / cpr, col = c - row * cpr;
+      cp_async16(d + (size_t)c * 16, src + (size_t)row * row_j + (size_t)col * 16);
+    }
+  }
+}
+
+// Four consecutive I/O values from shared memory, widened to fp32.
+template <typename IO>
+__device__ __forceinline__ float4 load4(const IO* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xffff0000u));
+}
+
+// Per-(t, j) column terms (Λ^v, Λ^v, Λ^v·v, Λ^v·v) of a staged tile, four
+// columns per thread: the duplicated pairs let one packed instruction serve
+// two rows.
+template <typename IO, int DK, int TC>
+__device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl) {
+  using R = RawTile<IO, DK, TC>;
+  const IO* rv = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes());
+  const IO* rL = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes() + R::col_bytes(cc));
+  for (int g = threadIdx.x; g < tl * cc / 4; g += blockDim.x) {
+    const float4 L = load4<IO>(rL + 4 * g);
+    const float4 v = load4<IO>(rv + 4 * g);
+    pj[4 * g + 0] = make_float4(L.x, L.x, L.x * v.x, L.x * v.x);
+    pj[4 * g + 1] = make_float4(L.y, L.y, L.y * v.y, L.y * v.y);
+    pj[4 * g + 2] = make_float4(L.z, L.z, L.z * v.z, L.z * v.z);
+    pj[4 * g + 3] = make_float4(L.w, L.w, L.w * v.w, L.w * v.w);
+  }
+}
+
+// ---- host helpers -------------------------------------------------------------
+inline KernelParams make_params(const ForwardArgs& f, const Plan& p) {
+  KernelParams kp{};
+  kp.q = f.q; kp.k = f.k; kp.v = f.v; kp.lam_v = f.lam_v; kp.a = f.a; kp.pbar = f.pbar;
+  kp.lam0 = f.lam0; kp.eta0 = f.eta0;
+  kp.y = f.y; kp.lamT = f.lamT; kp.etaT = f.etaT;
+  kp.T = f.T; kp.dv = f.dv; kp.chunk_len = p.chunk_len; kp.cc = p.cols_per_block;
+  int l2 = 0;
+  while ((1 << l2) < p.cols_per_block) ++l2;
+  kp.log2cc = l2;
+  kp.elems = (long long)f.B * f.H * f.dk * f.dv;
+  return kp;
+}
+
+// Launch with the dynamic shared memory a kernel needs (opting in above 48 KB).
+template <typename Kern>
+inline cudaError_t launch_kernel(Kern fn, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                                 const KernelParams& kp) {
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  fn<<<grid, threads, smem, s>>>(kp);
+  return cudaGetLastError();
+}
+
+}  // namespace kla

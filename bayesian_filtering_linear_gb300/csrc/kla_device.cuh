@@ -56,8 +56,21 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
+#ifndef KLA_RCP_ASM
+#define KLA_RCP_ASM 1
+#endif
+// Reciprocal of both halves of a pair, written so that the two results land
+// in the halves of one 64-bit register without extra moves.
 __device__ __forceinline__ f2 f2_rcp(f2 d) {
+#if KLA_RCP_ASM
+  f2 r;
+  asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\trcp.approx.ftz.f32 lo, lo;\n\t"
+      "rcp.approx.ftz.f32 hi, hi;\n\tmov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r) : "l"(d));
+  return r;
+#else
   return f2_make(rcp_approx(f2_lo(d)), rcp_approx(f2_hi(d)));
+#endif
 }
 
 // ---- I/O dtypes ------------------------------------------------------------

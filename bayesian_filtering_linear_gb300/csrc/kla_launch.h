@@ -33,6 +33,7 @@ struct Plan {
 int rows_per_lane_for(int dk);
 int tile_for(int dk, int io);
 int warp_cols(int dk);  // columns covered by one warp
+int max_threads();      // largest thread block of the scan kernels
 size_t forward_smem_bytes(int dk, int io, int cc, int tile);
 size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 

@@ -1,0 +1,370 @@
+// Sequence scan of the KLA filter for sm_103a (the sequential path, and the
+// re-run of each chunk on the chunk-parallel path).
+//
+// The operation is the diagonal information-form Kalman filter of
+// "Technische Samenvatting: Kalman Linear Attention (KLA)"
+// (gist.science/nl/paper/2602.10743), Methodologie §1 (OU prior, observation
+// through k with value precision Λ^v, posterior-mean readout through q) and
+// §2 (Möbius precision recursion, affine information-mean recursion).
+//
+// ---------------------------------------------------------------------------
+// Arithmetic (per element (i, j), token t; c = k²Λ^v, b = kΛ^v v)
+//
+// The filter is run in variance form, P = 1/λ and μ = η/λ, which needs one
+// reciprocal per element-step instead of the two of the printed information
+// form. The state is carried with a per-row scale so that the recurrence
+// costs 7 fp32 operations and one hardware reciprocal per element-step:
+//
+//   K_t = k_t² + 2^-40 (per row), P̃ = K_{t-1}·P (K_{-1} := 1 at a chunk start)
+//   ŝ  = A_t·P̃ + B_t          A_t = K_t a_t / K_{t-1},  B_t = K_t p̄_t / a_t
+//   d  = ŝ·Λ^v_j + 1/a_t       (= (1 + c·s)/a with s = a²P + p̄ the predicted variance)
+//   w̃  = 1/d                   (= a·w, w the Kalman weight 1/(1 + c s))
+//   P̃  = ŝ·w̃                   (= K_t·P_t)
+//   m  = (ŝ·Λ^v_j v_j)·(k_t/K_t) + μ
+//   μ  = m·w̃                   (= w·(aμ + s·b), the posterior mean)
+//   y_j += q_t·μ
+//
+// K_t and a_t are floored at 2^-40, so every scaled quantity stays a normal
+// fp32 number.
+//
+// ---------------------------------------------------------------------------
+// Work layout and pipeline
+//
+// A thread block owns one head (grid.x), a block of CC columns (grid.y) and
+// one chunk of tokens (grid.z); all d_k rows of those columns. Each lane
+// holds RL rows × CL columns in registers for the whole chunk — the state is
+// never written per token. Tokens stream through shared memory in tiles of
+// TC with one barrier per tile:
+//
+//   iteration n:  queue raw tile n+2 (16-byte cp.async)
+//                 scan tile n        (coef/pj[n%2] → partial y sums ypart[n%2])
+//                 store y of tile n-1 (finish the d_k reduction from ypart)
+//                 precompute tile n+1 (raw → per-row coefficients and
+//                                      per-column terms into coef/pj[(n+1)%2])
+//                 wait for raw tile n+2; barrier
+//
+// so a warp that finishes its share of the scan moves on to the next tile's
+// coefficients while the others are still scanning. The per-row coefficients
+// (A, B, 1/a, k/K, q) are computed once per (t, i) and serve all CC columns;
+// the per-column terms (Λ^v, Λ^v v) once per (t, j) for all d_k rows.
+// ---------------------------------------------------------------------------
+#include "kla_common.cuh"
+#include "kla_launch.h"
+
+namespace kla {
+
+namespace {
+
+constexpr int kTile = 16;  // tokens per shared-memory tile
+
+// Byte offsets of the double-buffered shared-memory regions of one block.
+template <typename IO, int DK, int TC, int NP>
+struct ScanLayout {
+  int cc;
+  __host__ __device__ explicit ScanLayout(int cc_) : cc(cc_) {}
+  __host__ __device__ size_t raw_bytes() const { return RawTile<IO, DK, TC>::bytes(cc); }
+  __host__ __device__ size_t coef_bytes() const { return (size_t)TC * 5 * DK * sizeof(float); }
+  __host__ __device__ size_t pj_bytes() const { return (size_t)TC * cc * sizeof(float4); }
+  __host__ __device__ size_t ypart_bytes() const { return (size_t)TC * cc * NP * sizeof(float); }
+  __host__ __device__ size_t raw(int b) const { return b * raw_bytes(); }
+  __host__ __device__ size_t coef(int b) const { return 2 * raw_bytes() + b * coef_bytes(); }
+  __host__ __device__ size_t pj(int b) const { return coef(2) + b * pj_bytes(); }
+  __host__ __device__ size_t ypart(int b) const { return pj(2) + b * ypart_bytes(); }
+  __host__ __device__ size_t kprev(int b) const { return ypart(2) + b * DK * sizeof(float); }
+  __host__ __device__ size_t total() const { return kprev(2); }
+};
+
+// Per-(t, i) row coefficients of a staged tile, four rows per thread:
+// coef[t][0..4][i] = (A, B, 1/a, k/K, q). kp_cur holds K of the row before
+// the tile (1 at a chunk start); K of the tile's last row goes to kp_nxt.
+template <typename IO, int DK, int TC>
+__device__ __forceinline__ void row_coefficients(const unsigned char* raw, float* coef, const float* kp_cur,
+                                                 float* kp_nxt, int tl) {
+  using R = RawTile<IO, DK, TC>;
+  const IO* rq = reinterpret_cast<const IO*>(raw);
+  const IO* rk = reinterpret_cast<const IO*>(raw + R::row_bytes());
+  const IO* ra = reinterpret_cast<const IO*>(raw + 2 * R::row_bytes());
+  const IO* rp = reinterpret_cast<const IO*>(raw + 3 * R::row_bytes());
+  for (int g = threadIdx.x; g < tl * (DK / 4); g += blockDim.x) {
+    const int t = g / (DK / 4), i = 4 * (g % (DK / 4));
+    const int o = t * DK + i;
+    const float4 k4 = load4<IO>(rk + o), a4 = load4<IO>(ra + o), p4 = load4<IO>(rp + o), q4 = load4<IO>(rq + o);
+    float4 kp4;
+    if (t == 0) {
+      kp4 = *reinterpret_cast<const float4*>(kp_cur + i);
+    } else {
+      const float4 km = load4<IO>(rk + o - DK);
+      kp4 = make_float4(fmaf(km.x, km.x, kK2Floor), fmaf(km.y, km.y, kK2Floor), fmaf(km.z, km.z, kK2Floor),
+                        fmaf(km.w, km.w, kK2Floor));
+    }
+    const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
+    const float pv[4] = {p4.x, p4.y, p4.z, p4.w}, kpv[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
+    float A[4], B[4], AI[4], KI[4], Kt[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float at = fmaxf(av[u], kAMin);
+      Kt[u] = fmaf(kv[u], kv[u], kK2Floor);
+      const float aK = at * Kt[u];
+      const float r = rcp_approx(aK * kpv[u]);  // 1 / (a K_t K_{t-1})
+      AI[u] = (Kt[u] * kpv[u]) * r;             // 1/a
+      A[u] = aK * (aK * r);                     // K_t a / K_{t-1}
+      B[u] = (Kt[u] * pv[u]) * AI[u];           // K_t p̄ / a
+      KI[u] = kv[u] * (at * kpv[u] * r);        // k / K_t
+    }
+    float* ct = coef + t * 5 * DK + i;
+    *reinterpret_cast<float4*>(ct + 0 * DK) = make_float4(A[0], A[1], A[2], A[3]);
+    *reinterpret_cast<float4*>(ct + 1 * DK) = make_float4(B[0], B[1], B[2], B[3]);
+    *reinterpret_cast<float4*>(ct + 2 * DK) = make_float4(AI[0], AI[1], AI[2], AI[3]);
+    *reinterpret_cast<float4*>(ct + 3 * DK) = make_float4(KI[0], KI[1], KI[2], KI[3]);
+    *reinterpret_cast<float4*>(ct + 4 * DK) = q4;
+    if (t == tl - 1) *reinterpret_cast<float4*>(kp_nxt + i) = make_float4(Kt[0], Kt[1], Kt[2], Kt[3]);
+  }
+}
+
+// Finish the d_k reduction of one tile (NP partial sums per output) and store
+// y rows [t0, t0 + tl) of this block's columns, four columns per thread.
+template <typename IO, int NP>
+__device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int tl) {
+  for (int g = threadIdx.x; g < tl * cc / 4; g += blockDim.x) {
+    const int t = (4 * g) / cc, c = (4 * g) % cc;
+    float s[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float* src = ypart + (size_t)(4 * g + u) * NP;
+      float acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < NP; ++q) acc += src[q];
+      s[u] = acc;
+    }
+    IO* dst = yout + (size_t)t * dv + c;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[u] = from_f32<IO>(s[u]);
+  }
+}
+
+template <typename IO, int DK, int RL, int TC>
+__global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParams p) {
+  using G = Geo<DK, RL>;
+  constexpr int NPR = RL / 2;  // row pairs per lane
+  extern __shared__ __align__(16) unsigned char smem[];
+  const ScanLayout<IO, DK, TC, G::NP> L(p.cc);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long bh = blockIdx.x;
+  const int jb = blockIdx.y * p.cc;
+  const int z = blockIdx.z;
+  const int t_begin = z * p.chunk_len;
+  const int t_end = min(p.T, t_begin + p.chunk_len);
+  const int ntiles = (t_end - t_begin + TC - 1) / TC;
+  const int li = lane / G::LANES_J, lj = lane % G::LANES_J;
+  const int i0 = li * RL;
+  const int cl0 = warp * G::WC + lj * CL;  // block-local first column of this lane
+  const size_t E = (size_t)DK * p.dv;
+  IO* ybase = reinterpret_cast<IO*>(p.y) + ((size_t)bh * p.T) * p.dv + jb;
+  auto tile_len = [&](int n) { return min(TC, t_end - (t_begin + n * TC)); };
+
+  // ---- chunk-start state: P̃ = P (scale K := 1), μ ---------------------------
+  f2 Pt[NPR][CL], Mu[NPR][CL];
+#pragma unroll
+  for (int r = 0; r < NPR; ++r) {
+#pragma unroll
+    for (int c = 0; c < CL; ++c) {
+      float P2[2], M2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const size_t e = (size_t)bh * E + (size_t)(i0 + 2 * r + h) * p.dv + jb + cl0 + c;
+        if (p.starts) {
+          P2[h] = p.starts[(size_t)(2 * z) * p.elems + e];
+          M2[h] = p.starts[(size_t)(2 * z + 1) * p.elems + e];
+        } else if (p.lam0) {
+          P2[h] = 1.0f / p.lam0[e];
+          M2[h] = p.eta0[e] * P2[h];
+        } else {
+          P2[h] = 1.0f;
+          M2[h] = 0.0f;
+        }
+      }
+      Pt[r][c] = f2_make(P2[0], P2[1]);
+      Mu[r][c] = f2_make(M2[0], M2[1]);
+    }
+  }
+  float* kp0 = reinterpret_cast<float*>(smem + L.kprev(0));
+  for (int i = tid; i < DK; i += blockDim.x) kp0[i] = 1.0f;
+
+  // ---- prologue: tiles 0 and 1 in flight, coefficients of tile 0 ------------
+  stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, tile_len(0));
+  cp_async_commit();
+  if (ntiles > 1) stage_raw<IO, DK, TC>(p, smem + L.raw(1), bh, jb, t_begin + TC, tile_len(1));
+  cp_async_commit();
+  cp_async_wait<1>();
+  __syncthreads();
+  row_coefficients<IO, DK, TC>(smem + L.raw(0), reinterpret_cast<float*>(smem + L.coef(0)), kp0,
+                               reinterpret_cast<float*>(smem + L.kprev(1)), tile_len(0));
+  column_terms<IO, DK, TC>(smem + L.raw(0), reinterpret_cast<float4*>(smem + L.pj(0)), p.cc, tile_len(0));
+  cp_async_wait<0>();
+  __syncthreads();
+
+  for (int n = 0; n < ntiles; ++n) {
+    const int b = n & 1;
+    const int tl = tile_len(n);
+    if (n + 2 < ntiles) stage_raw<IO, DK, TC>(p, smem + L.raw(b), bh, jb, t_begin + (n + 2) * TC, tile_len(n + 2));
+    cp_async_commit();
+
+    // ---- the scan over tile n ------------------------------------------------
+    {
+      const float* __restrict__ coef = reinterpret_cast<const float*>(smem + L.coef(b)) + i0;
+      const float4* __restrict__ pj = reinterpret_cast<const float4*>(smem + L.pj(b)) + cl0;
+      float* __restrict__ ypart = reinterpret_cast<float*>(smem + L.ypart(b));
+#pragma unroll kUnroll
+      for (int t = 0; t < tl; ++t) {
+        const float* ct = coef + t * 5 * DK;
+        f2 A[NPR], Bc[NPR], AI[NPR], KI[NPR], Q[NPR];
+#pragma unroll
+        for (int m = 0; m < NPR / 2; ++m) {
+          const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(ct + 0 * DK + 4 * m);
+          const ulonglong2 b4 = *reinterpret_cast<const ulonglong2*>(ct + 1 * DK + 4 * m);
+          const ulonglong2 i4 = *reinterpret_cast<const ulonglong2*>(ct + 2 * DK + 4 * m);
+          const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(ct + 3 * DK + 4 * m);
+          const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(ct + 4 * DK + 4 * m);
+          A[2 * m] = a4.x;  A[2 * m + 1] = a4.y;
+          Bc[2 * m] = b4.x; Bc[2 * m + 1] = b4.y;
+          AI[2 * m] = i4.x; AI[2 * m + 1] = i4.y;
+          KI[2 * m] = k4.x; KI[2 * m + 1] = k4.y;
+          Q[2 * m] = q4.x;  Q[2 * m + 1] = q4.y;
+        }
+        float yc[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
+          const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(pj + t * p.cc + c);
+          const f2 L2 = lv.x, V2 = lv.y;
+          f2 y2 = f2_make(0.0f, 0.0f);
+#pragma unroll
+          for (int r = 0; r < NPR; ++r) {
+            const f2 s = f2_fma(A[r], Pt[r][c], Bc[r]);
+            const f2 d = f2_fma(s, L2, AI[r]);
+            const f2 w = f2_rcp(d);
+            Pt[r][c] = f2_mul(s, w);
+            const f2 g = f2_mul(s, V2);
+            const f2 m = f2_fma(g, KI[r], Mu[r][c]);
+            Mu[r][c] = f2_mul(m, w);
+            y2 = f2_fma(Q[r], Mu[r][c], y2);
+          }
+          yc[c] = f2_lo(y2) + f2_hi(y2);
+        }
+        // Exchange rounds with the lanes holding neighbouring rows halve the
+        // partial sums each time; after XR rounds a lane holds one column's
+        // sum over 2^XR row groups.
+        int colofs = 0;
+#pragma unroll
+        for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) {
+          const bool hi = ((li >> r) & 1) != 0;
+#pragma unroll
+          for (int u = 0; u < nv / 2; ++u) {
+            const float send = hi ? yc[u] : yc[u + nv / 2];
+            const float keep = hi ? yc[u + nv / 2] : yc[u];
+            yc[u] = keep + __shfl_xor_sync(0xffffffffu, send, G::LANES_J << r);
+          }
+          colofs += hi ? nv / 2 : 0;
+        }
+        ypart[(t * p.cc + cl0 + colofs) * G::NP + (li >> G::XR)] = yc[0];
+      }
+    }
+
+    // ---- y of the previous tile; coefficients of the next one ---------------
+    if (n >= 1)
+      store_y<IO, G::NP>(reinterpret_cast<const float*>(smem + L.ypart(b ^ 1)),
+                         ybase + (size_t)(t_begin + (n - 1) * TC) * p.dv, p.dv, p.cc, tile_len(n - 1));
+    if (n + 1 < ntiles) {
+      row_coefficients<IO, DK, TC>(smem + L.raw(b ^ 1), reinterpret_cast<float*>(smem + L.coef(b ^ 1)),
+                                   reinterpret_cast<const float*>(smem + L.kprev(b ^ 1)),
+                                   reinterpret_cast<float*>(smem + L.kprev(b)), tile_len(n + 1));
+      column_terms<IO, DK, TC>(smem + L.raw(b ^ 1), reinterpret_cast<float4*>(smem + L.pj(b ^ 1)), p.cc,
+                               tile_len(n + 1));
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+  }
+  store_y<IO, G::NP>(reinterpret_cast<const float*>(smem + L.ypart((ntiles - 1) & 1)),
+                     ybase + (size_t)(t_begin + (ntiles - 1) * TC) * p.dv, p.dv, p.cc, tile_len(ntiles - 1));
+
+  // ---- final state of the last chunk: λ_T = K_last / P̃, η_T = μ λ_T ---------
+  if (z == (int)gridDim.z - 1 && p.lamT) {
+    const float* klast = reinterpret_cast<const float*>(smem + L.kprev(ntiles & 1));
+#pragma unroll
+    for (int r = 0; r < NPR; ++r) {
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = i0 + 2 * r + h;
+          const size_t e = (size_t)bh * E + (size_t)i * p.dv + jb + cl0 + c;
+          const float pt = h ? f2_hi(Pt[r][c]) : f2_lo(Pt[r][c]);
+          const float mu = h ? f2_hi(Mu[r][c]) : f2_lo(Mu[r][c]);
+          const float lam = klast[i] / pt;
+          p.lamT[e] = lam;
+          p.etaT[e] = mu * lam;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host side: geometry and launch.
+// ---------------------------------------------------------------------------
+int rows_per_lane_for(int dk) {
+  switch (dk) {
+    case 16: return RowsPerLane<16>::value;
+    case 32: return RowsPerLane<32>::value;
+    case 64: return RowsPerLane<64>::value;
+    default: return RowsPerLane<128>::value;
+  }
+}
+int tile_for(int /*dk*/, int /*io*/) { return kTile; }
+int max_threads() { return kMaxThreads; }
+int warp_cols(int dk) { return (32 / (dk / rows_per_lane_for(dk))) * CL; }
+
+namespace {
+template <typename IO, int DK>
+size_t scan_smem(int cc) {
+  return ScanLayout<IO, DK, kTile, Geo<DK, RowsPerLane<DK>::value>::NP>(cc).total();
+}
+template <typename IO>
+size_t scan_smem_io(int dk, int cc) {
+  switch (dk) {
+    case 16: return scan_smem<IO, 16>(cc);
+    case 32: return scan_smem<IO, 32>(cc);
+    case 64: return scan_smem<IO, 64>(cc);
+    default: return scan_smem<IO, 128>(cc);
+  }
+}
+template <typename IO>
+cudaError_t scan_dispatch(int dk, dim3 grid, int threads, size_t smem, cudaStream_t s, const KernelParams& kp) {
+  switch (dk) {
+    case 16: return launch_kernel(kla_scan_kernel<IO, 16, RowsPerLane<16>::value, kTile>, grid, threads, smem, s, kp);
+    case 32: return launch_kernel(kla_scan_kernel<IO, 32, RowsPerLane<32>::value, kTile>, grid, threads, smem, s, kp);
+    case 64: return launch_kernel(kla_scan_kernel<IO, 64, RowsPerLane<64>::value, kTile>, grid, threads, smem, s, kp);
+    case 128:
+      return launch_kernel(kla_scan_kernel<IO, 128, RowsPerLane<128>::value, kTile>, grid, threads, smem, s, kp);
+    default: return cudaErrorInvalidValue;
+  }
+}
+}  // namespace
+
+size_t forward_smem_bytes(int dk, int io, int cc, int /*tile*/) {
+  return io == IO_BF16 ? scan_smem_io<__nv_bfloat16>(dk, cc) : scan_smem_io<float>(dk, cc);
+}
+
+cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s) {
+  KernelParams kp = make_params(f, p);
+  kp.starts = starts;
+  const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
+  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk));
+  const size_t smem = forward_smem_bytes(f.dk, f.io, p.cols_per_block, p.tile);
+  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, grid, threads, smem, s, kp)
+                         : scan_dispatch<float>(f.dk, grid, threads, smem, s, kp);
+}
+
+}  // namespace kla

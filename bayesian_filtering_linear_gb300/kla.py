@@ -35,11 +35,12 @@ class PlanInfo(ctypes.Structure):
                 ("cols_per_block", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
 
 
-def _load():
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is not built; run `python -m bayesian_filtering_linear_gb300.build` "
+def load_library(path: str = LIB_PATH):
+    """Open a build of the library and declare the C signatures."""
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run `python -m bayesian_filtering_linear_gb300.build` "
                           "(needs nvcc) — there is no fallback implementation")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.kla_status_string.restype = ctypes.c_char_p
     lib.kla_status_string.argtypes = [i]
@@ -58,7 +59,7 @@ def _load():
     return lib
 
 
-LIB = _load()
+LIB = load_library()
 
 
 class KlaError(RuntimeError):

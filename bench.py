@@ -31,7 +31,7 @@ FLOPS_PER_ELEMENT_STEP = 13  # algorithmic count of the printed recursion (see D
 WORKLOAD = "headline"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_headline.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "bayesian_filtering_linear_gb300", "csrc", f)
-                  for f in ("kla_forward.cu", "kla_device.cuh")]
+                  for f in ("kla_scan.cu", "kla_common.cuh", "kla_device.cuh")]
 
 
 def kernel_source_hash() -> str:
