@@ -23,7 +23,7 @@ _STRATEGIES = {"auto": AUTO, "sequential": SEQUENTIAL, "chunked": CHUNKED}
 _IO = {torch.float32: F32, torch.bfloat16: BF16}
 # Every function the header declares, for the export check.
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
-           "kla_status_string", "kla_version")
+           "kla_status_string", "kla_version", "kla_forward_chunked_noalloc")
 
 
 class Options(ctypes.Structure):

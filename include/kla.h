@@ -121,6 +121,28 @@ kla_status kla_step(const void* q, const void* k, const void* v, const void* lam
                     const void* a, const void* pbar, float* lam, float* eta, void* y,
                     int B, int H, int dk, int dv, kla_dtype io, void* stream);
 
+/* kla_forward on the chunk-parallel path, for callers that cannot allocate
+ * device memory. (Library-side addition: the summary has no counterpart.)
+ * Callers that run inside an allocator or memory-pool callback, in a loop
+ * that must never take the driver's allocation lock, or under a framework
+ * that owns every device allocation cannot provide kla_forward's workspace;
+ * this entry point uses a fixed 32 MiB scratch array that the library keeps
+ * in device memory instead, so it allocates nothing.
+ *   Arguments are those of kla_forward without workspace/options; the
+ *   strategy is KLA_CHUNKED with chunk_len tokens per chunk (0 = automatic,
+ *   else a multiple of 32).
+ *   Returns KLA_ERR_WORKSPACE, before launching anything, when the plan's
+ *   workspace (kla_plan with strategy KLA_CHUNKED) exceeds 32 MiB.
+ *   The first call on a device looks up the scratch address on that device
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls on a device share the scratch: calls whose work overlaps on the
+ *   GPU (different streams, unordered host threads) race; order them. */
+kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void* v, const void* lam_v,
+                                       const void* a, const void* pbar, const float* lam0,
+                                       const float* eta0, void* y, float* lamT, float* etaT,
+                                       int B, int H, int T, int dk, int dv, kla_dtype io,
+                                       int chunk_len, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kla_status_string(kla_status s);
 
