@@ -19,6 +19,9 @@ namespace kla {
 #ifndef KLA_UNROLL
 #define KLA_UNROLL 2
 #endif
+#ifndef KLA_XR
+#define KLA_XR -1
+#endif
 
 constexpr int CL = KLA_CL;             // d_v columns per lane (2 or 4)
 constexpr int kMaxThreads = KLA_MAXT;  // per block (256 leaves up to 255 registers per thread)
@@ -39,9 +42,13 @@ struct Geo {
   static constexpr int LANES_I = DK / RL;       // lanes along rows
   static constexpr int LANES_J = 32 / LANES_I;  // lanes along columns
   static constexpr int WC = LANES_J * CL;       // columns per warp
-  static constexpr int XR = CL == 4 ? 2 : 1;    // exchange rounds of the readout reduction
-  static constexpr int NP = LANES_I / CL;       // partial sums per output left for shared memory
-  static_assert(LANES_I >= CL && LANES_I <= 32 && RL % 4 == 0 && (CL == 2 || CL == 4), "unsupported geometry");
+  // Lane-exchange rounds of the readout reduction (each halves the partial
+  // sums a lane holds) and the partial sums per output left for shared memory.
+  static constexpr int XR = KLA_XR >= 0 ? KLA_XR : (CL == 4 ? 2 : 1);
+  static constexpr int NP = LANES_I >> XR;
+  static constexpr int VALS = CL >> XR;          // partial sums a lane stores per token
+  static_assert(LANES_I >= (1 << XR) && LANES_I <= 32 && RL % 4 == 0 && (CL == 2 || CL == 4) && VALS >= 1,
+                "unsupported geometry");
 };
 
 struct KernelParams {

@@ -65,7 +65,10 @@ struct ScanLayout {
   __host__ __device__ size_t raw_bytes() const { return RawTile<IO, DK, TC>::bytes(cc); }
   __host__ __device__ size_t coef_bytes() const { return (size_t)TC * 5 * DK * sizeof(float); }
   __host__ __device__ size_t pj_bytes() const { return (size_t)TC * cc * sizeof(float4); }
-  __host__ __device__ size_t ypart_bytes() const { return (size_t)TC * cc * NP * sizeof(float); }
+  // Partial sums, token-major per (partial, column): [NP][cc][TC + 4] (the
+  // padding keeps 128-bit stores of four tokens free of bank conflicts).
+  static constexpr int TCP = TC + 4;
+  __host__ __device__ size_t ypart_bytes() const { return (size_t)cc * NP * TCP * sizeof(float); }
   __host__ __device__ size_t raw(int b) const { return b * raw_bytes(); }
   __host__ __device__ size_t coef(int b) const { return 2 * raw_bytes() + b * coef_bytes(); }
   __host__ __device__ size_t pj(int b) const { return coef(2) + b * pj_bytes(); }
@@ -121,24 +124,25 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
   }
 }
 
-// Finish the d_k reduction of one tile (NP partial sums per output) and store
-// y rows [t0, t0 + tl) of this block's columns, four columns per thread.
-template <typename IO, int NP>
+// Finish the d_k reduction of one tile (NP partial sums per output, layout
+// [NP][cc][TCP]) and store y rows [t0, t0 + tl) of this block's columns; a
+// thread handles one column and four tokens.
+template <typename IO, int NP, int TC, int TCP>
 __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int tl) {
-  for (int g = threadIdx.x; g < tl * cc / 4; g += blockDim.x) {
-    const int t = (4 * g) / cc, c = (4 * g) % cc;
-    float s[4];
+  for (int g = threadIdx.x; g < cc * (TC / 4); g += blockDim.x) {
+    const int col = g / (TC / 4), t4 = 4 * (g % (TC / 4));
+    if (t4 >= tl) continue;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float* src = ypart + (size_t)(4 * g + u) * NP;
-      float acc = 0.0f;
-#pragma unroll
-      for (int q = 0; q < NP; ++q) acc += src[q];
-      s[u] = acc;
+    for (int q = 0; q < NP; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(ypart + ((size_t)q * cc + col) * TCP + t4);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
-    IO* dst = yout + (size_t)t * dv + c;
+    const float sv[4] = {s.x, s.y, s.z, s.w};
+    IO* dst = yout + (size_t)t4 * dv + col;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) dst[u] = from_f32<IO>(s[u]);
+    for (int u = 0; u < 4; ++u)
+      if (t4 + u < tl) dst[(size_t)u * dv] = from_f32<IO>(sv[u]);
   }
 }
 
@@ -215,10 +219,33 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
       const float* __restrict__ coef = reinterpret_cast<const float*>(smem + L.coef(b)) + i0;
       const float4* __restrict__ pj = reinterpret_cast<const float4*>(smem + L.pj(b)) + cl0;
       float* __restrict__ ypart = reinterpret_cast<float*>(smem + L.ypart(b));
-#pragma unroll kUnroll
-      for (int t = 0; t < tl; ++t) {
+      // Exchange rounds with the lanes holding neighbouring rows halve the
+      // partial sums each time; after XR rounds a lane holds VALS columns'
+      // sums over 2^XR row groups, at columns cl0 + colofs + u.
+      int colofs = 0;
+#pragma unroll
+      for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) colofs += ((li >> r) & 1) ? nv / 2 : 0;
+      float* __restrict__ ydst = ypart + ((size_t)(li >> G::XR) * p.cc + cl0 + colofs) * L.TCP;
+      auto exchange = [&](const float* yc, float* ex) {
+        float v[CL];
+#pragma unroll
+        for (int c = 0; c < CL; ++c) v[c] = yc[c];
+#pragma unroll
+        for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) {
+          const bool hi = ((li >> r) & 1) != 0;
+#pragma unroll
+          for (int u = 0; u < nv / 2; ++u) {
+            const float send = hi ? v[u] : v[u + nv / 2];
+            const float keep = hi ? v[u + nv / 2] : v[u];
+            v[u] = keep + __shfl_xor_sync(0xffffffffu, send, G::LANES_J << r);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < G::VALS; ++u) ex[u] = v[u];
+      };
+      f2 A[NPR], Bc[NPR], AI[NPR], KI[NPR], Q[NPR], L2[CL], V2[CL];
+      auto load_coef = [&](int t) {
         const float* ct = coef + t * 5 * DK;
-        f2 A[NPR], Bc[NPR], AI[NPR], KI[NPR], Q[NPR];
 #pragma unroll
         for (int m = 0; m < NPR / 2; ++m) {
           const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(ct + 0 * DK + 4 * m);
@@ -232,47 +259,78 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
           KI[2 * m] = k4.x; KI[2 * m + 1] = k4.y;
           Q[2 * m] = q4.x;  Q[2 * m + 1] = q4.y;
         }
-        float yc[CL];
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
           const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(pj + t * p.cc + c);
-          const f2 L2 = lv.x, V2 = lv.y;
+          L2[c] = lv.x; V2[c] = lv.y;
+        }
+      };
+      auto compute = [&](float* yc) {
+#pragma unroll
+        for (int c = 0; c < CL; ++c) {
           f2 y2 = f2_make(0.0f, 0.0f);
 #pragma unroll
           for (int r = 0; r < NPR; ++r) {
             const f2 s = f2_fma(A[r], Pt[r][c], Bc[r]);
-            const f2 d = f2_fma(s, L2, AI[r]);
+            const f2 d = f2_fma(s, L2[c], AI[r]);
             const f2 w = f2_rcp(d);
             Pt[r][c] = f2_mul(s, w);
-            const f2 g = f2_mul(s, V2);
+            const f2 g = f2_mul(s, V2[c]);
             const f2 m = f2_fma(g, KI[r], Mu[r][c]);
             Mu[r][c] = f2_mul(m, w);
             y2 = f2_fma(Q[r], Mu[r][c], y2);
           }
           yc[c] = f2_lo(y2) + f2_hi(y2);
         }
-        // Exchange rounds with the lanes holding neighbouring rows halve the
-        // partial sums each time; after XR rounds a lane holds one column's
-        // sum over 2^XR row groups.
-        int colofs = 0;
+      };
+      if (tl == TC) {
+        // Full tile: tokens in batches of four. The previous batch's partial
+        // sums are exchanged while this batch computes and stored with one
+        // 128-bit store per value, so no store waits on a fresh result.
+        float pb[4][CL];
+#pragma unroll 1
+        for (int t4 = 0; t4 < TC; t4 += 4) {
+          float cur[4][CL], ex[4][G::VALS];
 #pragma unroll
-        for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) {
-          const bool hi = ((li >> r) & 1) != 0;
-#pragma unroll
-          for (int u = 0; u < nv / 2; ++u) {
-            const float send = hi ? yc[u] : yc[u + nv / 2];
-            const float keep = hi ? yc[u + nv / 2] : yc[u];
-            yc[u] = keep + __shfl_xor_sync(0xffffffffu, send, G::LANES_J << r);
+          for (int u = 0; u < 4; ++u) {
+            load_coef(t4 + u);
+            if (t4 > 0) exchange(pb[u], ex[u]);
+            compute(cur[u]);
           }
-          colofs += hi ? nv / 2 : 0;
+          if (t4 > 0) {
+#pragma unroll
+            for (int v = 0; v < G::VALS; ++v)
+              *reinterpret_cast<float4*>(ydst + (size_t)v * L.TCP + t4 - 4) =
+                  make_float4(ex[0][v], ex[1][v], ex[2][v], ex[3][v]);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int c = 0; c < CL; ++c) pb[u][c] = cur[u][c];
         }
-        ypart[(t * p.cc + cl0 + colofs) * G::NP + (li >> G::XR)] = yc[0];
+        float ex[4][G::VALS];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) exchange(pb[u], ex[u]);
+#pragma unroll
+        for (int v = 0; v < G::VALS; ++v)
+          *reinterpret_cast<float4*>(ydst + (size_t)v * L.TCP + TC - 4) =
+              make_float4(ex[0][v], ex[1][v], ex[2][v], ex[3][v]);
+      } else {
+        // Ragged last tile: one token at a time.
+        for (int t = 0; t < tl; ++t) {
+          float yc[CL], ex[G::VALS];
+          load_coef(t);
+          compute(yc);
+          exchange(yc, ex);
+#pragma unroll
+          for (int v = 0; v < G::VALS; ++v) ydst[(size_t)v * L.TCP + t] = ex[v];
+        }
       }
     }
 
     // ---- y of the previous tile; coefficients of the next one ---------------
     if (n >= 1)
-      store_y<IO, G::NP>(reinterpret_cast<const float*>(smem + L.ypart(b ^ 1)),
+      store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b ^ 1)),
                          ybase + (size_t)(t_begin + (n - 1) * TC) * p.dv, p.dv, p.cc, tile_len(n - 1));
     if (n + 1 < ntiles) {
       row_coefficients<IO, DK, TC>(smem + L.raw(b ^ 1), reinterpret_cast<float*>(smem + L.coef(b ^ 1)),
@@ -284,7 +342,7 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
     cp_async_wait<0>();
     __syncthreads();
   }
-  store_y<IO, G::NP>(reinterpret_cast<const float*>(smem + L.ypart((ntiles - 1) & 1)),
+  store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart((ntiles - 1) & 1)),
                      ybase + (size_t)(t_begin + (ntiles - 1) * TC) * p.dv, p.dv, p.cc, tile_len(ntiles - 1));
 
   // ---- final state of the last chunk: λ_T = K_last / P̃, η_T = μ λ_T ---------
