@@ -163,6 +163,14 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
   const int li = lane / G::LANES_J, lj = lane % G::LANES_J;
   const int i0 = li * RL;
   const int cl0 = warp * G::WC + lj * CL;  // block-local first column of this lane
+  // Register c of a lane holds column cl0 + (c ^ swz), swz = the low XR bits
+  // of li bit-reversed into the top bits of the column index: then in every
+  // exchange round each lane keeps the low half of its registers and sends
+  // the high half (no per-lane select).
+  constexpr int kLogCL = CL == 4 ? 2 : 1;
+  int swz = 0;
+#pragma unroll
+  for (int r = 0; r < G::XR; ++r) swz |= ((li >> r) & 1) << (kLogCL - 1 - r);
   const size_t E = (size_t)DK * p.dv;
   IO* ybase = reinterpret_cast<IO*>(p.y) + ((size_t)bh * p.T) * p.dv + jb;
   auto tile_len = [&](int n) { return min(TC, t_end - (t_begin + n * TC)); };
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
       float P2[2], M2[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const size_t e = (size_t)bh * E + (size_t)(i0 + 2 * r + h) * p.dv + jb + cl0 + c;
+        const size_t e = (size_t)bh * E + (size_t)(i0 + 2 * r + h) * p.dv + jb + cl0 + (c ^ swz);
         if (p.starts) {
           P2[h] = p.starts[(size_t)(2 * z) * p.elems + e];
           M2[h] = p.starts[(size_t)(2 * z + 1) * p.elems + e];
@@ -222,23 +230,17 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
       // Exchange rounds with the lanes holding neighbouring rows halve the
       // partial sums each time; after XR rounds a lane holds VALS columns'
       // sums over 2^XR row groups, at columns cl0 + colofs + u.
-      int colofs = 0;
-#pragma unroll
-      for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) colofs += ((li >> r) & 1) ? nv / 2 : 0;
-      float* __restrict__ ydst = ypart + ((size_t)(li >> G::XR) * p.cc + cl0 + colofs) * L.TCP;
+      // After the exchange a lane holds registers 0..VALS-1: columns
+      // cl0 + (u ^ swz); with VALS = 1 that is column cl0 + swz.
+      float* __restrict__ ydst = ypart + ((size_t)(li >> G::XR) * p.cc + cl0 + swz) * L.TCP;
       auto exchange = [&](const float* yc, float* ex) {
         float v[CL];
 #pragma unroll
         for (int c = 0; c < CL; ++c) v[c] = yc[c];
 #pragma unroll
         for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) {
-          const bool hi = ((li >> r) & 1) != 0;
 #pragma unroll
-          for (int u = 0; u < nv / 2; ++u) {
-            const float send = hi ? v[u] : v[u + nv / 2];
-            const float keep = hi ? v[u + nv / 2] : v[u];
-            v[u] = keep + __shfl_xor_sync(0xffffffffu, send, G::LANES_J << r);
-          }
+          for (int u = 0; u < nv / 2; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u + nv / 2], G::LANES_J << r);
         }
 #pragma unroll
         for (int u = 0; u < G::VALS; ++u) ex[u] = v[u];
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
         }
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-          const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(pj + t * p.cc + c);
+          const ulonglong2 lv = *reinterpret_cast<const ulonglong2*>(pj + t * p.cc + (c ^ swz));
           L2[c] = lv.x; V2[c] = lv.y;
         }
       };
@@ -287,8 +289,10 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
         // Full tile: tokens in batches of four. The previous batch's partial
         // sums are exchanged while this batch computes and stored with one
         // 128-bit store per value, so no store waits on a fresh result.
+        // (Unrolled by two batches so that pb/cur are renamed, not copied: a
+        // register move would cost a slot on the busy FMA pipe.)
         float pb[4][CL];
-#pragma unroll 1
+#pragma unroll 2
         for (int t4 = 0; t4 < TC; t4 += 4) {
           float cur[4][CL], ex[4][G::VALS];
 #pragma unroll
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int i = i0 + 2 * r + h;
-          const size_t e = (size_t)bh * E + (size_t)i * p.dv + jb + cl0 + c;
+          const size_t e = (size_t)bh * E + (size_t)i * p.dv + jb + cl0 + (c ^ swz);
           const float pt = h ? f2_hi(Pt[r][c]) : f2_lo(Pt[r][c]);
           const float mu = h ? f2_hi(Mu[r][c]) : f2_lo(Mu[r][c]);
           const float lam = klast[i] / pt;
