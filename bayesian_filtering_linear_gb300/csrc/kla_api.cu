@@ -66,9 +66,10 @@ struct Candidate {
 int blocks_per_sm_limit(int dk, int io, int cc, int tile, int wc, bool compose) {
   const size_t smem = compose ? kla::compose_smem_bytes(dk, io, cc, tile) : kla::forward_smem_bytes(dk, io, cc, tile);
   if (smem > kMaxSmem) return 0;
-  const int by_smem = (int)((kMaxSmem + 1024) / (smem + 1024));
-  const int by_threads = 2048 / (32 * (cc / wc));
   if (32 * (cc / wc) > kla::max_threads()) return 0;
+  const int threads = 32 * (cc / wc) + (compose ? 0 : 32 * kla::producer_warps());
+  const int by_smem = (int)((kMaxSmem + 1024) / (smem + 1024));
+  const int by_threads = 2048 / threads;
   return std::max(0, std::min(by_smem, by_threads));
 }
 

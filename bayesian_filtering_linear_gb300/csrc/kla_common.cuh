@@ -26,6 +26,17 @@ namespace kla {
 constexpr int CL = KLA_CL;             // d_v columns per lane (2 or 4)
 constexpr int kMaxThreads = KLA_MAXT;  // per block (256 leaves up to 255 registers per thread)
 constexpr int kUnroll = KLA_UNROLL;    // token-loop unroll factor of the scan
+constexpr int kProducerWarps = 4;      // scan: warps that stage tiles, build coefficients and store y
+
+// Named barriers (ids 1..15; 0 is __syncthreads). bar.arrive counts this
+// warp in without waiting; bar.sync counts it in and waits for `count`
+// threads in total.
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // Rows per lane for a head size (compile-time twin of rows_per_lane_for()).
 template <int DK>
@@ -74,11 +85,11 @@ struct RawTile {
 
 // Queue 16-byte asynchronous copies of tokens [t0, t0 + tl) of this block's
 // inputs into the raw tile at `dst`.
+// (tid, nthr): this thread's index among the nthr threads sharing the work.
 template <typename IO, int DK, int TC>
 __device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* dst, long long bh, int jb, int t0,
-                                          int tl) {
+                                          int tl, int tid, int nthr) {
   using R = RawTile<IO, DK, TC>;
-  const int tid = threadIdx.x, nthr = blockDim.x;
   const size_t row_i = (size_t)DK * sizeof(IO);
   const int chunks_i = (int)(tl * row_i / 16);
   const size_t base_i = ((size_t)bh * p.T + t0) * row_i;
@@ -121,11 +132,11 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 // columns per thread: the duplicated pairs let one packed instruction serve
 // two rows.
 template <typename IO, int DK, int TC>
-__device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl) {
+__device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl, int tid, int nthr) {
   using R = RawTile<IO, DK, TC>;
   const IO* rv = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes());
   const IO* rL = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes() + R::col_bytes(cc));
-  for (int g = threadIdx.x; g < tl * cc / 4; g += blockDim.x) {
+  for (int g = tid; g < tl * cc / 4; g += nthr) {
     const float4 L = load4<IO>(rL + 4 * g);
     const float4 v = load4<IO>(rv + 4 * g);
     pj[4 * g + 0] = make_float4(L.x, L.x, L.x * v.x, L.x * v.x);

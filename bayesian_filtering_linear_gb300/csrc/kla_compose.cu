@@ -74,14 +74,14 @@ __global__ void __launch_bounds__(kMaxThreads) kla_compose_kernel(const KernelPa
       gg[r][c] = one;
     }
 
-  stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, min(TC, t_end - t_begin));
+  stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, min(TC, t_end - t_begin), tid, blockDim.x);
   cp_async_commit();
   for (int n = 0; n < ntiles; ++n) {
     const int t0 = t_begin + n * TC;
     const int tl = min(TC, t_end - t0);
     if (n + 1 < ntiles) {
       const int t1 = t0 + TC;
-      stage_raw<IO, DK, TC>(p, smem + L.raw((n + 1) & 1), bh, jb, t1, min(TC, t_end - t1));
+      stage_raw<IO, DK, TC>(p, smem + L.raw((n + 1) & 1), bh, jb, t1, min(TC, t_end - t1), tid, blockDim.x);
     }
     cp_async_commit();
     cp_async_wait<1>();
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kMaxThreads) kla_compose_kernel(const KernelPa
         ct[3 * DK] = kt;                           // k
         ct[4 * DK] = at;                           // a
       }
-      column_terms<IO, DK, TC>(buf, pj, p.cc, tl);
+      column_terms<IO, DK, TC>(buf, pj, p.cc, tl, tid, blockDim.x);
     }
     __syncthreads();
 

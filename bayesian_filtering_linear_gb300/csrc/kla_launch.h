@@ -33,7 +33,8 @@ struct Plan {
 int rows_per_lane_for(int dk);
 int tile_for(int dk, int io);
 int warp_cols(int dk);  // columns covered by one warp
-int max_threads();      // largest thread block of the scan kernels
+int max_threads();      // largest number of scanning threads in a block
+int producer_warps();   // extra warps per scan block that feed the scanning warps
 size_t forward_smem_bytes(int dk, int io, int cc, int tile);
 size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 

@@ -34,17 +34,19 @@
 // one chunk of tokens (grid.z); all d_k rows of those columns. Each lane
 // holds RL rows × CL columns in registers for the whole chunk — the state is
 // never written per token. Tokens stream through shared memory in tiles of
-// TC with one barrier per tile:
+// TC, double-buffered, between two groups of warps:
 //
-//   iteration n:  queue raw tile n+2 (16-byte cp.async)
-//                 scan tile n        (coef/pj[n%2] → partial y sums ypart[n%2])
-//                 store y of tile n-1 (finish the d_k reduction from ypart)
-//                 precompute tile n+1 (raw → per-row coefficients and
-//                                      per-column terms into coef/pj[(n+1)%2])
-//                 wait for raw tile n+2; barrier
+//   scan warps (CC/WC):   wait FULL[n%2]; scan tile n (coef/pj[n%2] → partial
+//                         y sums ypart[n%2]); arrive EMPTY[n%2]
+//   producer warps (4):   queue raw tile n+2 (16-byte cp.async); wait
+//                         EMPTY[n%2]; store y of tile n (finish the d_k
+//                         reduction from ypart); build the per-row
+//                         coefficients and per-column terms of tile n+2 into
+//                         coef/pj[n%2]; arrive FULL[n%2]
 //
-// so a warp that finishes its share of the scan moves on to the next tile's
-// coefficients while the others are still scanning. The per-row coefficients
+// (FULL/EMPTY are named barriers; bar.arrive does not wait.) The scan warps
+// do nothing but the recurrence; the producers' work overlaps it, and their
+// raw-tile loads have a whole tile of scanning to land. The per-row coefficients
 // (A, B, 1/a, k/K, q) are computed once per (t, i) and serve all CC columns;
 // the per-column terms (Λ^v, Λ^v v) once per (t, j) for all d_k rows.
 // ---------------------------------------------------------------------------
@@ -56,6 +58,10 @@ namespace kla {
 namespace {
 
 constexpr int kTile = 16;  // tokens per shared-memory tile
+// Named barrier ids of the scan's producer/consumer hand-off.
+constexpr int kBarFull0 = 1;      // 1, 2: coefficients of buffer 0 / 1 are ready
+constexpr int kBarEmpty0 = 3;     // 3, 4: the scan is done with buffer 0 / 1
+constexpr int kBarProducers = 5;  // producer warps only (staged raw tile visible)
 
 // Byte offsets of the double-buffered shared-memory regions of one block.
 template <typename IO, int DK, int TC, int NP>
@@ -82,13 +88,13 @@ struct ScanLayout {
 // the tile (1 at a chunk start); K of the tile's last row goes to kp_nxt.
 template <typename IO, int DK, int TC>
 __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float* coef, const float* kp_cur,
-                                                 float* kp_nxt, int tl) {
+                                                 float* kp_nxt, int tl, int tid, int nthr) {
   using R = RawTile<IO, DK, TC>;
   const IO* rq = reinterpret_cast<const IO*>(raw);
   const IO* rk = reinterpret_cast<const IO*>(raw + R::row_bytes());
   const IO* ra = reinterpret_cast<const IO*>(raw + 2 * R::row_bytes());
   const IO* rp = reinterpret_cast<const IO*>(raw + 3 * R::row_bytes());
-  for (int g = threadIdx.x; g < tl * (DK / 4); g += blockDim.x) {
+  for (int g = tid; g < tl * (DK / 4); g += nthr) {
     const int t = g / (DK / 4), i = 4 * (g % (DK / 4));
     const int o = t * DK + i;
     const float4 k4 = load4<IO>(rk + o), a4 = load4<IO>(ra + o), p4 = load4<IO>(rp + o), q4 = load4<IO>(rq + o);
@@ -128,8 +134,8 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
 // [NP][cc][TCP]) and store y rows [t0, t0 + tl) of this block's columns; a
 // thread handles one column and four tokens.
 template <typename IO, int NP, int TC, int TCP>
-__device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int tl) {
-  for (int g = threadIdx.x; g < cc * (TC / 4); g += blockDim.x) {
+__device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int tl, int tid, int nthr) {
+  for (int g = tid; g < cc * (TC / 4); g += nthr) {
     const int col = g / (TC / 4), t4 = 4 * (g % (TC / 4));
     if (t4 >= tl) continue;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -147,13 +153,17 @@ __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, in
 }
 
 template <typename IO, int DK, int RL, int TC>
-__global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParams p) {
+__global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_kernel(const KernelParams p) {
   using G = Geo<DK, RL>;
   constexpr int NPR = RL / 2;  // row pairs per lane
   extern __shared__ __align__(16) unsigned char smem[];
   const ScanLayout<IO, DK, TC, G::NP> L(p.cc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Warps [0, ncons) scan; the last kProducerWarps warps stage raw tiles,
+  // build per-row coefficients and per-column terms, and store y.
+  const int ncons = (int)(blockDim.x >> 5) - kProducerWarps;
+  const int nall = (int)blockDim.x;
   const long long bh = blockIdx.x;
   const int jb = blockIdx.y * p.cc;
   const int z = blockIdx.z;
@@ -175,6 +185,52 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
   IO* ybase = reinterpret_cast<IO*>(p.y) + ((size_t)bh * p.T) * p.dv + jb;
   auto tile_len = [&](int n) { return min(TC, t_end - (t_begin + n * TC)); };
 
+  if (warp >= ncons) {
+    // ================= producer warps =================
+    const int ptid = tid - 32 * ncons, pn = 32 * kProducerWarps;
+    float* kp0 = reinterpret_cast<float*>(smem + L.kprev(0));
+    for (int i = ptid; i < DK; i += pn) kp0[i] = 1.0f;
+    auto build = [&](int m) {  // coefficients of tile m into buffer m % 2
+      const int bm = m & 1;
+      row_coefficients<IO, DK, TC>(smem + L.raw(bm), reinterpret_cast<float*>(smem + L.coef(bm)),
+                                   reinterpret_cast<const float*>(smem + L.kprev(bm)),
+                                   reinterpret_cast<float*>(smem + L.kprev(bm ^ 1)), tile_len(m), ptid, pn);
+      column_terms<IO, DK, TC>(smem + L.raw(bm), reinterpret_cast<float4*>(smem + L.pj(bm)), p.cc, tile_len(m),
+                               ptid, pn);
+    };
+    stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, tile_len(0), ptid, pn);
+    cp_async_commit();
+    if (ntiles > 1) stage_raw<IO, DK, TC>(p, smem + L.raw(1), bh, jb, t_begin + TC, tile_len(1), ptid, pn);
+    cp_async_commit();
+    cp_async_wait<1>();
+    named_sync(kBarProducers, pn);  // raw tile 0 and kprev visible to all producers
+    build(0);
+    named_arrive(kBarFull0, nall);
+    if (ntiles > 1) {
+      cp_async_wait<0>();
+      named_sync(kBarProducers, pn);
+      build(1);
+      named_arrive(kBarFull0 + 1, nall);
+    }
+    for (int n = 0; n < ntiles; ++n) {
+      const int b = n & 1;
+      // raw[b] held tile n, already consumed by build(n)
+      if (n + 2 < ntiles) stage_raw<IO, DK, TC>(p, smem + L.raw(b), bh, jb, t_begin + (n + 2) * TC, tile_len(n + 2), ptid, pn);
+      cp_async_commit();
+      named_sync(kBarEmpty0 + b, nall);  // the scan of tile n is done with coef/pj[b] and ypart[b]
+      store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
+                                    ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
+      if (n + 2 < ntiles) {
+        cp_async_wait<0>();
+        named_sync(kBarProducers, pn);
+        build(n + 2);
+        named_arrive(kBarFull0 + b, nall);
+      }
+    }
+    return;
+  }
+
+  // ================= scan (consumer) warps =================
   // ---- chunk-start state: P̃ = P (scale K := 1), μ ---------------------------
   f2 Pt[NPR][CL], Mu[NPR][CL];
 #pragma unroll
@@ -200,38 +256,19 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
       Mu[r][c] = f2_make(M2[0], M2[1]);
     }
   }
-  float* kp0 = reinterpret_cast<float*>(smem + L.kprev(0));
-  for (int i = tid; i < DK; i += blockDim.x) kp0[i] = 1.0f;
-
-  // ---- prologue: tiles 0 and 1 in flight, coefficients of tile 0 ------------
-  stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, tile_len(0));
-  cp_async_commit();
-  if (ntiles > 1) stage_raw<IO, DK, TC>(p, smem + L.raw(1), bh, jb, t_begin + TC, tile_len(1));
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();
-  row_coefficients<IO, DK, TC>(smem + L.raw(0), reinterpret_cast<float*>(smem + L.coef(0)), kp0,
-                               reinterpret_cast<float*>(smem + L.kprev(1)), tile_len(0));
-  column_terms<IO, DK, TC>(smem + L.raw(0), reinterpret_cast<float4*>(smem + L.pj(0)), p.cc, tile_len(0));
-  cp_async_wait<0>();
-  __syncthreads();
-
   for (int n = 0; n < ntiles; ++n) {
     const int b = n & 1;
     const int tl = tile_len(n);
-    if (n + 2 < ntiles) stage_raw<IO, DK, TC>(p, smem + L.raw(b), bh, jb, t_begin + (n + 2) * TC, tile_len(n + 2));
-    cp_async_commit();
-
+    named_sync(kBarFull0 + b, nall);  // coefficients of tile n are ready
     // ---- the scan over tile n ------------------------------------------------
     {
       const float* __restrict__ coef = reinterpret_cast<const float*>(smem + L.coef(b)) + i0;
       const float4* __restrict__ pj = reinterpret_cast<const float4*>(smem + L.pj(b)) + cl0;
       float* __restrict__ ypart = reinterpret_cast<float*>(smem + L.ypart(b));
       // Exchange rounds with the lanes holding neighbouring rows halve the
-      // partial sums each time; after XR rounds a lane holds VALS columns'
-      // sums over 2^XR row groups, at columns cl0 + colofs + u.
-      // After the exchange a lane holds registers 0..VALS-1: columns
-      // cl0 + (u ^ swz); with VALS = 1 that is column cl0 + swz.
+      // partial sums each time; after XR rounds a lane holds registers
+      // 0..VALS-1, the sums over 2^XR row groups of columns cl0 + (u ^ swz)
+      // (with VALS = 1: column cl0 + swz).
       float* __restrict__ ydst = ypart + ((size_t)(li >> G::XR) * p.cc + cl0 + swz) * L.TCP;
       auto exchange = [&](const float* yc, float* ex) {
         float v[CL];
@@ -332,22 +369,8 @@ __global__ void __launch_bounds__(kMaxThreads) kla_scan_kernel(const KernelParam
       }
     }
 
-    // ---- y of the previous tile; coefficients of the next one ---------------
-    if (n >= 1)
-      store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b ^ 1)),
-                         ybase + (size_t)(t_begin + (n - 1) * TC) * p.dv, p.dv, p.cc, tile_len(n - 1));
-    if (n + 1 < ntiles) {
-      row_coefficients<IO, DK, TC>(smem + L.raw(b ^ 1), reinterpret_cast<float*>(smem + L.coef(b ^ 1)),
-                                   reinterpret_cast<const float*>(smem + L.kprev(b ^ 1)),
-                                   reinterpret_cast<float*>(smem + L.kprev(b)), tile_len(n + 1));
-      column_terms<IO, DK, TC>(smem + L.raw(b ^ 1), reinterpret_cast<float4*>(smem + L.pj(b ^ 1)), p.cc,
-                               tile_len(n + 1));
-    }
-    cp_async_wait<0>();
-    __syncthreads();
+    named_arrive(kBarEmpty0 + b, nall);
   }
-  store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart((ntiles - 1) & 1)),
-                     ybase + (size_t)(t_begin + (ntiles - 1) * TC) * p.dv, p.dv, p.cc, tile_len(ntiles - 1));
 
   // ---- final state of the last chunk: λ_T = K_last / P̃, η_T = μ λ_T ---------
   if (z == (int)gridDim.z - 1 && p.lamT) {
@@ -386,6 +409,7 @@ int rows_per_lane_for(int dk) {
 }
 int tile_for(int /*dk*/, int /*io*/) { return kTile; }
 int max_threads() { return kMaxThreads; }
+int producer_warps() { return kProducerWarps; }
 int warp_cols(int dk) { return (32 / (dk / rows_per_lane_for(dk))) * CL; }
 
 namespace {
@@ -423,7 +447,7 @@ cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* sta
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
-  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk));
+  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk) + kProducerWarps);
   const size_t smem = forward_smem_bytes(f.dk, f.io, p.cols_per_block, p.tile);
   return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, grid, threads, smem, s, kp)
                          : scan_dispatch<float>(f.dk, grid, threads, smem, s, kp);
