@@ -36,10 +36,18 @@ kla_status check_shape(int B, int H, int T, int dk, int dv) {
   return KLA_OK;
 }
 
-kla_status check_options(const kla_options* opt) {
+// Options for a head of dk rows (dk already checked).
+kla_status check_options(const kla_options* opt, int dk) {
   if (!opt) return KLA_OK;
   if (opt->strategy < KLA_AUTO || opt->strategy > KLA_CHUNKED) return KLA_ERR_INVALID_ARG;
   if (opt->chunk_len < 0 || opt->chunk_len % kChunkAlign != 0) return KLA_ERR_INVALID_ARG;
+  if (opt->rows_per_lane != 0) {  // must be a geometry the scan kernel is built for
+    int rls[2];
+    const int nrl = kla::scan_rows_per_lane(dk, rls);
+    bool ok = false;
+    for (int n = 0; n < nrl; ++n) ok = ok || rls[n] == opt->rows_per_lane;
+    if (!ok) return KLA_ERR_INVALID_ARG;
+  }
   return KLA_OK;
 }
 
@@ -51,21 +59,25 @@ kla_status check_options(const kla_options* opt) {
 // block's warps over the 4 sub-partitions, so the busiest sub-partition
 // carries ceil(ceil(blocks/SMs) · warps/4) warps. Per-row coefficients cost
 // about 4.5 columns' worth of work per block; a sub-partition with a single
-// warp issues at ~0.7 of its rate (latency), two or more at ~0.9. Chunk
-// composition costs ~1.6× a scan step. Fixed costs: ~2 tiles of pipeline fill
-// per block, ~4000 cycles per kernel launch, and the carry kernel's traffic
-// (9 floats per element per chunk at ~6.6 TB/s, ~1.95 GHz).
+// warp issues at ~0.7 of its rate (latency), two or more at ~0.9. With four
+// rows per lane the per-element share of coefficient loads and readout is
+// larger: ~1.15× the work per element-step at d_k = 64 and ~1.45× at 128
+// (sixteen partial sums per output instead of eight). Chunk composition costs ~1.6× a
+// scan step. Fixed costs: ~2 tiles of pipeline fill per block, ~4000 cycles
+// per kernel launch, and the carry kernel's traffic (9 floats per element per
+// chunk at ~6.6 TB/s, ~1.95 GHz).
 constexpr double kLaunchCycles = 4000.0;
 constexpr double kCyclesPerByte = 1.95e9 / 6.6e12;
 
 struct Candidate {
-  int cc;
+  int cc, rl;
   double cost;
 };
 
-int blocks_per_sm_limit(int dk, int io, int cc, int tile, int wc, bool compose) {
-  const size_t smem = compose ? kla::compose_smem_bytes(dk, io, cc, tile) : kla::forward_smem_bytes(dk, io, cc, tile);
-  if (smem > kMaxSmem) return 0;
+int blocks_per_sm_limit(int dk, int rl, int io, int cc, int tile, int wc, bool compose) {
+  const size_t smem =
+      compose ? kla::compose_smem_bytes(dk, io, cc, tile) : kla::forward_smem_bytes(dk, rl, io, cc, tile);
+  if (smem == 0 || smem > kMaxSmem) return 0;
   if (32 * (cc / wc) > kla::max_threads()) return 0;
   const int threads = 32 * (cc / wc) + (compose ? 0 : 32 * kla::producer_warps());
   const int by_smem = (int)((kMaxSmem + 1024) / (smem + 1024));
@@ -73,9 +85,12 @@ int blocks_per_sm_limit(int dk, int io, int cc, int tile, int wc, bool compose) 
   return std::max(0, std::min(by_smem, by_threads));
 }
 
-double pass_cost(long long bh, int dk, int dv, int io, int cc, int tile, int wc, int num_sms, long long blocks_z,
-                 double step_cost, long long tokens) {
-  const int bps = blocks_per_sm_limit(dk, io, cc, tile, wc, step_cost > 1.0);
+// One pass (scan, or composition when `compose`) over `tokens` tokens of
+// every block: bh heads × dv/cc column blocks × blocks_z chunks.
+double pass_cost(long long bh, int dk, int rl, int dv, int io, int cc, int tile, int num_sms, long long blocks_z,
+                 bool compose, long long tokens) {
+  const int wc = kla::warp_cols(dk, rl);
+  const int bps = blocks_per_sm_limit(dk, rl, io, cc, tile, wc, compose);
   if (bps == 0) return INFINITY;
   const long long blocks = bh * (dv / cc) * blocks_z;
   const long long per_sm = (blocks + num_sms - 1) / num_sms;
@@ -84,7 +99,8 @@ double pass_cost(long long bh, int dk, int dv, int io, int cc, int tile, int wc,
   const long long warps_sm = resident * (cc / wc);
   const long long warps_smsp = (warps_sm + 3) / 4;
   const double eff = warps_smsp >= 2 ? 0.9 : 0.7;
-  const double warp_token = 8.0 * kla::rows_per_lane_for(dk) * 2;  // cycles per warp per token
+  const double step_cost = (compose ? 1.6 : 1.0) * (rl == 4 && dk >= 64 ? (dk == 64 ? 1.15 : 1.45) : 1.0);
+  const double warp_token = 8.0 * rl * 2;  // cycles per warp per token
   return kLaunchCycles + (double)waves * (double)(tokens + 2 * tile) * (double)warps_smsp * warp_token *
                              (step_cost + 4.5 / cc) / eff;
 }
@@ -93,66 +109,80 @@ kla_status make_plan(int B, int H, int T, int dk, int dv, int io, const kla_opti
                      Plan* out) {
   kla_status st = check_shape(B, H, T, dk, dv);
   if (st != KLA_OK) return st;
-  if ((st = check_options(opt)) != KLA_OK) return st;
+  if ((st = check_options(opt, dk)) != KLA_OK) return st;
   if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
   if (num_sms < 1) return KLA_ERR_INVALID_ARG;
   const int strategy = opt ? opt->strategy : KLA_AUTO;
   const int fixed_len = opt ? opt->chunk_len : 0;
   const long long bh = (long long)B * H;
   const long long elems = bh * dk * dv;
-  const int wc = kla::warp_cols(dk);
   const int tile = kla::tile_for(dk, io);
-  const int cc_min = std::max<int>(wc, (int)(16 / io_size(io)));
-  const int cc_max = std::min(dv, kla::max_threads() / 32 * wc);
+  int rls[2];
+  int nrl = kla::scan_rows_per_lane(dk, rls);
+  if (opt && opt->rows_per_lane != 0) {  // fixed by the caller (checked above)
+    rls[0] = opt->rows_per_lane;
+    nrl = 1;
+  }
+  const int rl_compose = kla::rows_per_lane_for(dk);
 
-  auto best_cc = [&](int num_chunks, int chunk_len, double* cost_out) {
-    Candidate best{cc_min, INFINITY};
-    for (int cc = cc_max; cc >= cc_min; cc /= 2) {
-      double c = pass_cost(bh, dk, dv, io, cc, tile, wc, num_sms, num_chunks, 1.0, chunk_len);
-      if (num_chunks > 1) {
-        c += pass_cost(bh, dk, dv, io, cc, tile, wc, num_sms, num_chunks - 1, 1.6, chunk_len);
-        c += kLaunchCycles + kCyclesPerByte * 36.0 * (double)num_chunks * (double)elems;
+  // Cheapest (column block, rows per lane) for a split into num_chunks
+  // chunks of chunk_len tokens.
+  auto best_geometry = [&](int num_chunks, int chunk_len) {
+    Candidate best{0, 0, INFINITY};
+    for (int n = 0; n < nrl; ++n) {
+      const int rl = rls[n], wc = kla::warp_cols(dk, rl);
+      int cc_min = std::max<int>(wc, (int)(16 / io_size(io)));
+      if (num_chunks > 1) cc_min = std::max(cc_min, kla::warp_cols(dk, rl_compose));
+      if (n == 0) best = {cc_min, rl, INFINITY};  // kept only if nothing fits
+      const int cc_max = std::min(dv, kla::max_threads() / 32 * wc);
+      for (int cc = cc_max; cc >= cc_min; cc /= 2) {
+        double c = pass_cost(bh, dk, rl, dv, io, cc, tile, num_sms, num_chunks, false, chunk_len);
+        if (num_chunks > 1) {
+          c += pass_cost(bh, dk, rl_compose, dv, io, cc, tile, num_sms, num_chunks - 1, true, chunk_len);
+          c += kLaunchCycles + kCyclesPerByte * 36.0 * (double)num_chunks * (double)elems;
+        }
+        if (c < best.cost) best = {cc, rl, c};
       }
-      if (c < best.cost) best = {cc, c};
     }
-    *cost_out = best.cost;
-    return best.cc;
+    return best;
   };
 
   Plan p{};
-  p.rows_per_lane = kla::rows_per_lane_for(dk);
   p.tile = tile;
   const long long Tl = std::max(T, 1);
-  double seq_cost = 0.0;
-  const int seq_cc = best_cc(1, (int)Tl, &seq_cost);
+  const Candidate seq = best_geometry(1, (int)Tl);
   p.strategy = KLA_SEQUENTIAL;
   p.chunk_len = (int)Tl;
   p.num_chunks = 1;
-  p.cols_per_block = seq_cc;
+  p.cols_per_block = seq.cc;
+  p.rows_per_lane = seq.rl;
 
   if (strategy == KLA_CHUNKED || strategy == KLA_AUTO) {
-    int best_len = 0, best_cc_c = 0;
-    double best_cost = INFINITY;
+    int best_len = 0;
+    Candidate best_c{0, 0, INFINITY};
     auto consider = [&](long long len) {
       len = ((len + kChunkAlign - 1) / kChunkAlign) * kChunkAlign;
       if (len < kChunkAlign) len = kChunkAlign;
       const long long S = (Tl + len - 1) / len;
       if (S < 2 || S > 65535) return;
-      double c = 0.0;
-      const int cc = best_cc((int)S, (int)len, &c);
-      if (c < best_cost) { best_cost = c; best_len = (int)len; best_cc_c = cc; }
+      const Candidate c = best_geometry((int)S, (int)len);
+      if (c.cost < best_c.cost) {
+        best_c = c;
+        best_len = (int)len;
+      }
     };
     if (fixed_len > 0) {
       consider(fixed_len);
     } else {
       for (int S = 2; S <= 256; S = S < 8 ? S + 1 : S * 2) consider((Tl + S - 1) / S);
     }
-    const bool take = strategy == KLA_CHUNKED ? best_len > 0 : (best_len > 0 && best_cost < seq_cost);
+    const bool take = strategy == KLA_CHUNKED ? best_len > 0 : (best_len > 0 && best_c.cost < seq.cost);
     if (take) {
       p.strategy = KLA_CHUNKED;
       p.chunk_len = best_len;
       p.num_chunks = (int)((Tl + best_len - 1) / best_len);
-      p.cols_per_block = best_cc_c;
+      p.cols_per_block = best_c.cc;
+      p.rows_per_lane = best_c.rl;
     }
   }
   p.ws_bytes = p.strategy == KLA_CHUNKED ? kla::chunk_workspace_bytes(elems, p.num_chunks) : 0;
@@ -189,6 +219,7 @@ void fill_info(const Plan& p, kla_plan_info* out) {
   out->num_chunks = p.num_chunks;
   out->cols_per_block = p.cols_per_block;
   out->workspace_bytes = p.ws_bytes;
+  out->rows_per_lane = p.rows_per_lane;
 }
 
 }  // namespace
@@ -252,7 +283,7 @@ kla_status kla_forward(const void* q, const void* k, const void* v, const void* 
   // ---- validation: no CUDA call before it passes ---------------------------
   kla_status st = check_shape(B, H, T, dk, dv);
   if (st != KLA_OK) return st;
-  if ((st = check_options(opt)) != KLA_OK) return st;
+  if ((st = check_options(opt, dk)) != KLA_OK) return st;
   if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
   const long long bh = (long long)B * H;
   const long long tokens = bh * T;

@@ -259,7 +259,7 @@ cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cud
   KernelParams kp = make_params(f, p);
   kp.maps = maps;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)(p.num_chunks - 1));
-  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk));
+  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, rows_per_lane_for(f.dk)));
   const size_t smem = compose_smem_bytes(f.dk, f.io, p.cols_per_block, 0);
   return f.io == IO_BF16 ? compose_dispatch<__nv_bfloat16>(f.dk, grid, threads, smem, s, kp)
                          : compose_dispatch<float>(f.dk, grid, threads, smem, s, kp);

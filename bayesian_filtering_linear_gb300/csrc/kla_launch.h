@@ -24,18 +24,22 @@ struct Plan {
   int chunk_len;       // tokens per chunk (multiple of the tile length)
   int num_chunks;
   int cols_per_block;  // CC: d_v columns per thread block
-  int rows_per_lane;   // RL: d_k rows held by one lane
+  int rows_per_lane;   // RL: d_k rows held by one lane of the scan kernel
   int tile;            // TC: tokens staged per shared-memory tile
   size_t ws_bytes;
 };
 
-// Geometry constants of the sequential / apply kernel.
+// Geometry of the sequential / apply (scan) kernel and of the chunk
+// composition kernel. The scan kernel is built for every RL that
+// scan_rows_per_lane() lists for d_k; composition always uses
+// rows_per_lane_for(d_k).
 int rows_per_lane_for(int dk);
+int scan_rows_per_lane(int dk, int* rl_out);  // the RL choices for d_k (at most 2); returns their count
 int tile_for(int dk, int io);
-int warp_cols(int dk);  // columns covered by one warp
-int max_threads();      // largest number of scanning threads in a block
-int producer_warps();   // extra warps per scan block that feed the scanning warps
-size_t forward_smem_bytes(int dk, int io, int cc, int tile);
+int warp_cols(int dk, int rl);  // columns covered by one warp
+int max_threads();              // largest number of scanning threads in a block
+int producer_warps();           // extra warps per scan block that feed the scanning warps
+size_t forward_smem_bytes(int dk, int rl, int io, int cc, int tile);
 size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 
 // Workspace layout for the chunked path (fp32 elements):

@@ -407,50 +407,67 @@ int rows_per_lane_for(int dk) {
     default: return RowsPerLane<128>::value;
   }
 }
+int scan_rows_per_lane(int dk, int* rl_out) {
+  // d_k <= 32: four rows per lane only (a warp covers the head's rows with
+  // no more than 8 lanes); 64 and 128: eight rows per lane, or four for
+  // finer column blocks (more blocks for few heads).
+  if (dk <= 32) {
+    rl_out[0] = 4;
+    return 1;
+  }
+  rl_out[0] = 8;
+  rl_out[1] = 4;
+  return 2;
+}
 int tile_for(int /*dk*/, int /*io*/) { return kTile; }
 int max_threads() { return kMaxThreads; }
 int producer_warps() { return kProducerWarps; }
-int warp_cols(int dk) { return (32 / (dk / rows_per_lane_for(dk))) * CL; }
+int warp_cols(int dk, int rl) { return (32 / (dk / rl)) * CL; }
 
 namespace {
-template <typename IO, int DK>
+template <typename IO, int DK, int RL>
 size_t scan_smem(int cc) {
-  return ScanLayout<IO, DK, kTile, Geo<DK, RowsPerLane<DK>::value>::NP>(cc).total();
+  return ScanLayout<IO, DK, kTile, Geo<DK, RL>::NP>(cc).total();
 }
 template <typename IO>
-size_t scan_smem_io(int dk, int cc) {
-  switch (dk) {
-    case 16: return scan_smem<IO, 16>(cc);
-    case 32: return scan_smem<IO, 32>(cc);
-    case 64: return scan_smem<IO, 64>(cc);
-    default: return scan_smem<IO, 128>(cc);
+size_t scan_smem_io(int dk, int rl, int cc) {
+  switch (dk * 16 + rl) {
+    case 16 * 16 + 4: return scan_smem<IO, 16, 4>(cc);
+    case 32 * 16 + 4: return scan_smem<IO, 32, 4>(cc);
+    case 64 * 16 + 4: return scan_smem<IO, 64, 4>(cc);
+    case 64 * 16 + 8: return scan_smem<IO, 64, 8>(cc);
+    case 128 * 16 + 4: return scan_smem<IO, 128, 4>(cc);
+    case 128 * 16 + 8: return scan_smem<IO, 128, 8>(cc);
+    default: return 0;
   }
 }
 template <typename IO>
-cudaError_t scan_dispatch(int dk, dim3 grid, int threads, size_t smem, cudaStream_t s, const KernelParams& kp) {
-  switch (dk) {
-    case 16: return launch_kernel(kla_scan_kernel<IO, 16, RowsPerLane<16>::value, kTile>, grid, threads, smem, s, kp);
-    case 32: return launch_kernel(kla_scan_kernel<IO, 32, RowsPerLane<32>::value, kTile>, grid, threads, smem, s, kp);
-    case 64: return launch_kernel(kla_scan_kernel<IO, 64, RowsPerLane<64>::value, kTile>, grid, threads, smem, s, kp);
-    case 128:
-      return launch_kernel(kla_scan_kernel<IO, 128, RowsPerLane<128>::value, kTile>, grid, threads, smem, s, kp);
+cudaError_t scan_dispatch(int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                          const KernelParams& kp) {
+  switch (dk * 16 + rl) {
+    case 16 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 16, 4, kTile>, grid, threads, smem, s, kp);
+    case 32 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 32, 4, kTile>, grid, threads, smem, s, kp);
+    case 64 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 64, 4, kTile>, grid, threads, smem, s, kp);
+    case 64 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 64, 8, kTile>, grid, threads, smem, s, kp);
+    case 128 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 128, 4, kTile>, grid, threads, smem, s, kp);
+    case 128 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 128, 8, kTile>, grid, threads, smem, s, kp);
     default: return cudaErrorInvalidValue;
   }
 }
 }  // namespace
 
-size_t forward_smem_bytes(int dk, int io, int cc, int /*tile*/) {
-  return io == IO_BF16 ? scan_smem_io<__nv_bfloat16>(dk, cc) : scan_smem_io<float>(dk, cc);
+size_t forward_smem_bytes(int dk, int rl, int io, int cc, int /*tile*/) {
+  return io == IO_BF16 ? scan_smem_io<__nv_bfloat16>(dk, rl, cc) : scan_smem_io<float>(dk, rl, cc);
 }
 
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s) {
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
-  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk) + kProducerWarps);
-  const size_t smem = forward_smem_bytes(f.dk, f.io, p.cols_per_block, p.tile);
-  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, grid, threads, smem, s, kp)
-                         : scan_dispatch<float>(f.dk, grid, threads, smem, s, kp);
+  const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, p.rows_per_lane) + kProducerWarps);
+  const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile);
+  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, p.rows_per_lane, grid, threads, smem, s, kp)
+                         : scan_dispatch<float>(f.dk, p.rows_per_lane, grid, threads, smem, s, kp);
 }
 
 }  // namespace kla

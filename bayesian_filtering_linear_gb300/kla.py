@@ -27,12 +27,13 @@ EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_fo
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int)]
+    _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("rows_per_lane", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("num_chunks", ctypes.c_int),
-                ("cols_per_block", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+                ("cols_per_block", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+                ("rows_per_lane", ctypes.c_int)]
 
 
 def load_library(path: str = LIB_PATH):
@@ -77,18 +78,18 @@ def status_string(status: int) -> str:
     return LIB.kla_status_string(status).decode()
 
 
-def options(strategy: str | int = "auto", chunk_len: int = 0) -> Options:
+def options(strategy: str | int = "auto", chunk_len: int = 0, rows_per_lane: int = 0) -> Options:
     s = _STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
-    return Options(s, int(chunk_len))
+    return Options(s, int(chunk_len), int(rows_per_lane))
 
 
 def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strategy: str | int = "auto",
-         chunk_len: int = 0, num_sms: int | None = None) -> dict:
+         chunk_len: int = 0, num_sms: int | None = None, rows_per_lane: int = 0) -> dict:
     """The launch plan kla_forward uses (for the current device, or for a
     device with ``num_sms`` SMs without touching CUDA)."""
     io_code = {"f32": F32, "bf16": BF16}.get(io, io)
     info = PlanInfo()
-    opt = options(strategy, chunk_len)
+    opt = options(strategy, chunk_len, rows_per_lane)
     if num_sms is None:
         st = LIB.kla_plan(B, H, T, dk, dv, io_code, ctypes.byref(opt), ctypes.byref(info))
     else:
@@ -96,7 +97,8 @@ def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strat
     _check(st, "kla_plan")
     return {"strategy": {SEQUENTIAL: "sequential", CHUNKED: "chunked"}[info.strategy],
             "chunk_len": info.chunk_len, "num_chunks": info.num_chunks,
-            "cols_per_block": info.cols_per_block, "workspace_bytes": int(info.workspace_bytes)}
+            "cols_per_block": info.cols_per_block, "workspace_bytes": int(info.workspace_bytes),
+            "rows_per_lane": info.rows_per_lane}
 
 
 def _ptr(t):
@@ -123,7 +125,7 @@ def _need(t, name, dtype, shape, device):
 
 def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None, etaT=None,
             strategy: str | int = "auto", chunk_len: int = 0, workspace=None, stream=None,
-            final_state: bool = True):
+            final_state: bool = True, rows_per_lane: int = 0):
     """Whole-sequence KLA scan. Returns ``(y, lamT, etaT)`` (the last two are
     None when ``final_state`` is False and none were given)."""
     B, H, T, dk = q.shape
@@ -148,7 +150,7 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
     if final_state and lamT is None:
         lamT = torch.empty(st_shape, dtype=torch.float32, device=dev)
         etaT = torch.empty(st_shape, dtype=torch.float32, device=dev)
-    opt = options(strategy, chunk_len)
+    opt = options(strategy, chunk_len, rows_per_lane)
     with torch.cuda.device(dev):
         if workspace is None:
             info = PlanInfo()

@@ -276,6 +276,7 @@ def run_kla(args, world, rank, local):
         "config": {"workload": "headline B8 H16 T4096 dk64 dv64 bf16 I/O, fp32 state", "B": w.B, "H": w.H,
                    "T": w.T, "dk": w.dk, "dv": w.dv, "io": w.io, "strategy": plan["strategy"],
                    "chunk_len": plan["chunk_len"], "cols_per_block": plan["cols_per_block"],
+                   "rows_per_lane": plan["rows_per_lane"],
                    "l2": "inputs (403 MB) larger than L2; no flush", "parallelism": f"{world} independent batches"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": traffic,

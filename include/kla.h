@@ -69,8 +69,10 @@ typedef enum kla_dtype { KLA_F32 = 0, KLA_BF16 = 1 } kla_dtype;
 typedef enum kla_strategy { KLA_AUTO = 0, KLA_SEQUENTIAL = 1, KLA_CHUNKED = 2 } kla_strategy;
 
 typedef struct kla_options {
-  int strategy;  /* kla_strategy */
-  int chunk_len; /* tokens per chunk for KLA_CHUNKED; 0 = automatic; multiple of 32 */
+  int strategy;      /* kla_strategy */
+  int chunk_len;     /* tokens per chunk for KLA_CHUNKED; 0 = automatic; multiple of 32 */
+  int rows_per_lane; /* scan-kernel rows per lane: 0 = automatic, else 4 or 8 (8 needs d_k >= 64);
+                        another value is INVALID_ARG. Results do not depend on it. */
 } kla_options;
 
 /* The launch plan kla_forward would use for this shape on the current device. */
@@ -80,6 +82,7 @@ typedef struct kla_plan_info {
   int num_chunks;         /* ceil(T / chunk_len)                              */
   int cols_per_block;     /* d_v columns handled by one thread block          */
   size_t workspace_bytes; /* device workspace kla_forward needs (0 if none)   */
+  int rows_per_lane;      /* d_k rows one lane of the scan kernel holds (4, 8) */
 } kla_plan_info;
 
 /* Plan for the current CUDA device. Errors: INVALID_ARG (out NULL, negative

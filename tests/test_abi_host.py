@@ -89,6 +89,10 @@ def test_bad_io_and_options():
     assert fwd(opt=ctypes.byref(kla.Options(9, 0))) == kla.ERR_INVALID_ARG
     assert fwd(opt=ctypes.byref(kla.Options(kla.CHUNKED, 48))) == kla.ERR_INVALID_ARG
     assert fwd(opt=ctypes.byref(kla.Options(kla.CHUNKED, -32))) == kla.ERR_INVALID_ARG
+    for rl in (-4, 2, 6, 16):
+        assert fwd(opt=ctypes.byref(kla.Options(kla.AUTO, 0, rl))) == kla.ERR_INVALID_ARG
+    # eight rows per lane needs a head of at least 64 rows
+    assert fwd(dk=32, opt=ctypes.byref(kla.Options(kla.AUTO, 0, 8))) == kla.ERR_INVALID_ARG
 
 
 def test_empty_batch_is_ok_without_any_cuda_call():
@@ -149,3 +153,22 @@ def test_planner_blocks_fit_the_hardware(dk, dv, io):
         p = kla.plan(B, H, T, dk, dv, io, num_sms=152)
         cc = p["cols_per_block"]
         assert dv % cc == 0 and cc * (2 if io == "bf16" else 4) % 16 == 0
+
+
+def test_planner_rows_per_lane_choice():
+    # Many heads: eight rows per lane (fewer coefficient loads per element).
+    assert kla.plan(8, 16, 4096, 64, 64, "bf16", num_sms=152)["rows_per_lane"] == 8
+    # Few heads: four rows per lane gives twice as many column blocks.
+    assert kla.plan(4, 8, 2048, 64, 64, "f32", num_sms=152)["rows_per_lane"] == 4
+    # Small heads only have four.
+    assert kla.plan(8, 16, 4096, 32, 64, "bf16", num_sms=152)["rows_per_lane"] == 4
+    for dk in (64, 128):
+        for rl in (4, 8):
+            for strategy, cl in (("sequential", 0), ("chunked", 64)):
+                p = kla.plan(2, 3, 1000, dk, 64, "f32", strategy, cl, num_sms=152, rows_per_lane=rl)
+                assert p["rows_per_lane"] == rl and p["strategy"] == strategy
+                # the column block is a whole number of warps of that geometry
+                wc = 32 // (dk // rl) * 2
+                assert p["cols_per_block"] % wc == 0
+    with pytest.raises(kla.KlaError):
+        kla.plan(1, 1, 64, 16, 16, "f32", rows_per_lane=8, num_sms=152)

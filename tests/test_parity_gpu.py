@@ -42,6 +42,30 @@ def test_small_shapes_match_oracle(shape, strategy, chunk_len):
     assert_close(errors(y, lamT, etaT, ref), TOL[IO[io]], f"{shape} {strategy}/{chunk_len}")
 
 
+# Both scan geometries for the head sizes that have two (rows per lane 4 and
+# 8), whichever the planner would pick, on the sequential and chunked paths.
+RL_SHAPES = [
+    (2, 2, 93, 64, 64, "f32"),
+    (1, 2, 130, 64, 32, "bf16"),
+    (1, 1, 70, 128, 128, "f32"),
+    (2, 1, 161, 128, 16, "bf16"),
+]
+
+
+@pytest.mark.parametrize("shape", RL_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("rows_per_lane", [4, 8])
+@pytest.mark.parametrize("strategy,chunk_len", [("sequential", 0), ("chunked", 32)], ids=lambda s: str(s))
+def test_rows_per_lane_choices_match_oracle(shape, rows_per_lane, strategy, chunk_len):
+    B, H, T, dk, dv, io = shape
+    x = make_inputs(B, H, T, dk, dv, io=io, seed=300 + T + dk, random_state=True)
+    ref = run_oracle(x)
+    info = kla.plan(B, H, T, dk, dv, io, strategy, chunk_len, rows_per_lane=rows_per_lane)
+    assert info["rows_per_lane"] == rows_per_lane
+    y, lamT, etaT = gpu_forward(to_dev(x), strategy=strategy, chunk_len=chunk_len, rows_per_lane=rows_per_lane)
+    torch.cuda.synchronize()
+    assert_close(errors(y, lamT, etaT, ref), TOL[IO[io]], f"{shape} RL{rows_per_lane} {strategy}")
+
+
 def test_tiny_workload_default_state():
     x = make_workload("tiny")
     ref = run_oracle(x, with_state=False)
