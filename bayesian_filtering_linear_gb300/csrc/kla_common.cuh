@@ -128,21 +128,19 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
                      __uint_as_float(u.y & 0xffff0000u));
 }
 
-// Per-(t, j) column terms (Λ^v, Λ^v, Λ^v·v, Λ^v·v) of a staged tile, four
-// columns per thread: the duplicated pairs let one packed instruction serve
-// two rows.
+// Per-(t, j) column terms (Λ^v, Λ^v, Λ^v·v, Λ^v·v) of a staged tile, one
+// (t, j) per thread so that consecutive threads store consecutive 16-byte
+// entries (no bank conflicts); the duplicated pairs let one packed
+// instruction serve two rows.
 template <typename IO, int DK, int TC>
 __device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl, int tid, int nthr) {
   using R = RawTile<IO, DK, TC>;
   const IO* rv = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes());
   const IO* rL = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes() + R::col_bytes(cc));
-  for (int g = tid; g < tl * cc / 4; g += nthr) {
-    const float4 L = load4<IO>(rL + 4 * g);
-    const float4 v = load4<IO>(rv + 4 * g);
-    pj[4 * g + 0] = make_float4(L.x, L.x, L.x * v.x, L.x * v.x);
-    pj[4 * g + 1] = make_float4(L.y, L.y, L.y * v.y, L.y * v.y);
-    pj[4 * g + 2] = make_float4(L.z, L.z, L.z * v.z, L.z * v.z);
-    pj[4 * g + 3] = make_float4(L.w, L.w, L.w * v.w, L.w * v.w);
+  for (int g = tid; g < tl * cc; g += nthr) {
+    const float L = to_f32<IO>(rL[g]);
+    const float Lv = L * to_f32<IO>(rv[g]);
+    pj[g] = make_float4(L, L, Lv, Lv);
   }
 }
 

@@ -135,8 +135,11 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
 // thread handles one column and four tokens.
 template <typename IO, int NP, int TC, int TCP>
 __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int tl, int tid, int nthr) {
+  // Columns vary fastest across threads: the partial-sum loads (columns
+  // TCP floats apart) hit distinct banks and each y row is written by
+  // consecutive threads.
   for (int g = tid; g < cc * (TC / 4); g += nthr) {
-    const int col = g / (TC / 4), t4 = 4 * (g % (TC / 4));
+    const int col = g % cc, t4 = 4 * (g / cc);
     if (t4 >= tl) continue;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
