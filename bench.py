@@ -1,13 +1,19 @@
-"""Benchmark of the KLA scan on the headline workload (one JSON line).
+"""Benchmark of the KLA scan (one JSON line).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kla|reference]
+                    [--workload headline|medium|long|tiny|decode]
 
-A step is one kla_forward over the headline workload — B=8, H=16, T=4096,
-d_k=d_v=64, bf16 inputs/outputs, fp32 state — with inputs resident in HBM.
-The inputs (403 MB) exceed the 135 MB L2, so no flush is needed between
-steps. Under torchrun every rank runs its own independent batch (weak
-scaling; no collective on the data path) and rank 0 reports the whole-job
-throughput over the slowest rank's time.
+By default a step is one kla_forward over the headline workload — B=8, H=16,
+T=4096, d_k=d_v=64, bf16 inputs/outputs, fp32 state — with inputs resident
+in HBM. The inputs (403 MB) exceed the 135 MB L2, so no flush is needed
+between steps. The other workloads print the same line for their own
+configuration: medium (B4 H8 T2048 d64 fp32; its 120 MB of inputs fit in L2,
+so L2 is flushed between steps), long (B1 H16 T65536 d128 bf16), tiny
+(B1 H1 T256 d16 fp32, launch-bound) and decode (one kla_step over B256 H16
+d64 fp32 per step, state from a 1024-token prefix; HBM-bound). Under
+torchrun every rank runs its own independent batch (weak scaling; no
+collective on the data path) and rank 0 reports the whole-job throughput over
+the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle (the stand-in reference arm,
 on this host's cores) on a bounded sample of the same workload.
@@ -26,10 +32,23 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "KLA scan tokens/s (B·H·T/s) at H=16,d=64,T=4096 bf16; % of roofline"
+METRICS = {
+    "headline": "KLA scan tokens/s (B·H·T/s) at H=16,d=64,T=4096 bf16; % of roofline",
+    "medium": "KLA scan tokens/s (B·H·T/s) at B=4,H=8,d=64,T=2048 fp32; % of roofline",
+    "long": "KLA scan tokens/s (B·H·T/s) at H=16,d=128,T=65536 bf16; % of roofline",
+    "tiny": "KLA scan tokens/s (B·H·T/s) at B=1,H=1,d=16,T=256 fp32",
+    "decode": "KLA decode step tokens/s (B·H per step) at B=256,H=16,d=64 fp32; % of HBM roofline",
+}
+DESCRIPTIONS = {
+    "headline": "headline B8 H16 T4096 dk64 dv64 bf16 I/O, fp32 state",
+    "medium": "medium B4 H8 T2048 dk64 dv64 fp32 I/O",
+    "long": "long context B1 H16 T65536 dk128 dv128 bf16 I/O, fp32 state, a=sigmoid(N(4,1))",
+    "tiny": "tiny B1 H1 T256 dk16 dv16 fp32 I/O",
+    "decode": "decode kla_step B256 H16 dk64 dv64 fp32, state from a 1024-token kla_forward prefix",
+}
 FLOPS_PER_ELEMENT_STEP = 13  # algorithmic count of the printed recursion
-WORKLOAD = "headline"
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_headline.json")
+L2_FLUSH_BYTES = 256 << 20   # written between steps when a workload's inputs fit in L2
+TRAFFIC_FILES = {"headline": os.path.join(ROOT, "profiles", "traffic_headline.json")}
 KERNEL_SOURCES = [os.path.join(ROOT, "bayesian_filtering_linear_gb300", "csrc", f)
                   for f in ("kla_scan.cu", "kla_common.cuh", "kla_device.cuh")]
 
@@ -121,34 +140,58 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
-def cpu_oracle_sample(heads: int, tokens: int, nthreads: int) -> tuple[float, dict]:
-    """Time the fp64 oracle, as it stands, on `heads` heads × `tokens` tokens of
-    the headline recipe. Returns (tokens/s, description)."""
+def cpu_oracle_sample(wname: str, nthreads: int) -> tuple[float, dict]:
+    """Time the fp64 oracle, as it stands, on a bounded sample of a workload's
+    recipe (same shapes per head, fresh draws): whole heads of the forward
+    workloads, or 64 single-token steps over all heads for decode. Returns
+    (tokens/s, description)."""
     import oracle
     from bayesian_filtering_linear_gb300.inputs import WORKLOADS, make_inputs
-    w = WORKLOADS[WORKLOAD]
-    x = make_inputs(1, heads, tokens, w.dk, w.dv, io=w.io, seed=w.seed)
+    w = WORKLOADS[wname]
     oracle.build()
+    if wname == "decode":
+        heads, steps = w.B * w.H, 64
+        x = make_inputs(1, heads, 1, w.dk, w.dv, io=w.io, seed=w.seed, random_state=True)
+        lam, eta = x["lam0"], x["eta0"]
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            r = oracle.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], lam, eta,
+                               nthreads=nthreads, want_scales=False)
+            lam, eta = r["lamT"], r["etaT"]
+        dt = time.perf_counter() - t0
+        used = min(nthreads, heads)
+        return heads * steps / dt, {
+            "kind": "oracle", "cores": used,
+            "sample": f"{steps} single-token steps over {heads} heads (d_k=d_v={w.dk}), fp64 C++ loop, "
+                      f"{used} threads, state converted to fp32 between steps"}
+    heads = w.B * w.H
+    tokens = w.T
+    x = make_inputs(1, heads, tokens, w.dk, w.dv, io=w.io, seed=w.seed, a_logit_mean=w.a_logit_mean)
     t0 = time.perf_counter()
     oracle.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
                    nthreads=nthreads, want_scales=False)
     dt = time.perf_counter() - t0
     used = min(nthreads, heads)
-    return heads * tokens / dt, {"kind": "oracle", "cores": used,
-                                 "sample": f"{heads} heads x {tokens} tokens of the headline recipe "
-                                           f"(d_k=d_v=64, bf16-rounded inputs), fp64 C++ loop, {used} threads"}
+    return heads * tokens / dt, {
+        "kind": "oracle", "cores": used,
+        "sample": f"all {heads} heads x {tokens} tokens of the {wname} recipe (d_k={w.dk}, d_v={w.dv}, "
+                  f"{w.io}-rounded inputs), fp64 C++ loop, {used} threads"}
 
 
 def run_reference(args, world, rank):
-    """Reference arm: the CPU oracle on bounded samples, timed per step."""
+    """Reference arm: the CPU oracle on bounded samples of the workload, timed
+    per step (rank 0 only)."""
     if rank != 0:
         return
-    heads, tokens = 16, 256
-    nthreads = min(os.cpu_count() or 1, heads)
     import oracle
     from bayesian_filtering_linear_gb300.inputs import WORKLOADS, make_inputs
-    w = WORKLOADS[WORKLOAD]
-    x = make_inputs(1, heads, tokens, w.dk, w.dv, io=w.io, seed=w.seed)
+    wname = args.workload
+    w = WORKLOADS[wname]
+    heads = 16
+    tokens = 1 if wname == "decode" else max(1, min(w.T, (256 * 64 * 64) // (w.dk * w.dv)))
+    nthreads = min(os.cpu_count() or 1, heads)
+    x = make_inputs(1, heads, tokens, w.dk, w.dv, io=w.io, seed=w.seed, a_logit_mean=w.a_logit_mean,
+                    random_state=wname == "decode")
     oracle.build()
     run = lambda: oracle.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
                                  nthreads=nthreads, want_scales=False)
@@ -159,43 +202,28 @@ def run_reference(args, world, rank):
         run()
     dt = time.perf_counter() - t0
     value = heads * tokens * args.steps / dt
-    sample = f"each step: {heads} heads x {tokens} tokens of the headline recipe, fp64 C++ oracle"
+    sample = f"each step: {heads} heads x {tokens} tokens of the {wname} recipe, fp64 C++ oracle"
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRICS[wname], "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "headline B8 H16 T4096 dk64 dv64 bf16 I/O (sampled)", "B": 8, "H": 16, "T": 4096,
-                   "dk": 64, "dv": 64, "io": "bf16"},
+        "config": {"workload": DESCRIPTIONS[wname] + " (sampled)", "B": w.B, "H": w.H, "T": w.T,
+                   "dk": w.dk, "dv": w.dv, "io": w.io},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
-def run_kla(args, world, rank, local):
+def timed_steps(step, args, world, local, stream, flush=None):
+    """Warm up, then time exactly args.steps calls of `step` with CUDA events on
+    `stream` (barrier + synchronize on both sides), sampling clocks meanwhile.
+    Returns (total ms over the slowest rank, mean per-launch ms, clocks).
+    With `flush`, it runs between steps, outside the per-launch events."""
     import torch
-    from bayesian_filtering_linear_gb300 import kla
-    from bayesian_filtering_linear_gb300.inputs import WORKLOADS, make_workload
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    w = WORKLOADS[WORKLOAD]
-    x = make_workload(w, device=dev)
-    x = {n: t for n, t in x.items()}
-    if rank:  # independent batch per rank
-        from bayesian_filtering_linear_gb300.inputs import make_inputs
-        x = make_inputs(w.B, w.H, w.T, w.dk, w.dv, io=w.io, seed=w.seed + 1000 * rank, device=dev)
-    plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io)
-    ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev) if plan["workspace_bytes"] else None
-    y = torch.empty((w.B, w.H, w.T, w.dv), dtype=x["q"].dtype, device=dev)
-    lamT = torch.empty_like(x["lam0"])
-    etaT = torch.empty_like(x["eta0"])
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        kla.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
-                    y=y, lamT=lamT, etaT=etaT, workspace=ws, stream=stream)
-
     for _ in range(max(args.warmup, 3)):
         step()
+        if flush:
+            flush()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
@@ -205,22 +233,81 @@ def run_kla(args, world, rank, local):
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for i in range(args.steps):
+            if flush:
+                flush()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-    total_ms = start.elapsed_time(end)
     per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    total_ms = max_over_ranks(total_ms, world)
-    ms_per_step = total_ms / args.steps
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    return total_ms, max_over_ranks(per_launch_ms, world), clocks
+
+
+def e2e_timing(e2e_step, args, world, stream) -> float:
+    """Mean ms of an end-to-end step (host copies inside), slowest rank."""
+    import torch
+    steps = max(5, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e) / steps, world)
+    barrier(world)
+    return ms
+
+
+def run_kla(args, world, rank, local):
+    import torch
+    from bayesian_filtering_linear_gb300 import kla
+    from bayesian_filtering_linear_gb300.inputs import WORKLOADS, make_workload, make_inputs
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wname = args.workload
+    w = WORKLOADS[wname]
+    if rank == 0:
+        x = make_workload(w, device=dev)
+    else:  # independent batch per rank
+        x = make_inputs(w.B, w.H, w.T, w.dk, w.dv, io=w.io, seed=w.seed + 1000 * rank,
+                        a_logit_mean=w.a_logit_mean, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ("q", "k", "v", "lam_v", "a", "pbar", "lam0", "eta0")
+    if wname == "decode":
+        return run_kla_decode(args, world, rank, local, w, x, stream)
+
+    plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io)
+    ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev) if plan["workspace_bytes"] else None
+    y = torch.empty((w.B, w.H, w.T, w.dv), dtype=x["q"].dtype, device=dev)
+    lamT = torch.empty_like(x["lam0"])
+    etaT = torch.empty_like(x["eta0"])
+    in_bytes = sum(x[n].numel() * x[n].element_size() for n in names)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = None
+    if in_bytes < 2 * l2:
+        scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = lambda: scratch.fill_(1.0)
+
+    def step():
+        kla.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
+                    y=y, lamT=lamT, etaT=etaT, workspace=ws, stream=stream)
+
+    total_ms, per_launch_ms, clocks = timed_steps(step, args, world, local, stream, flush)
+    # With a flush between steps the step time is the launch time (events
+    # around each forward); otherwise the whole timed region over K steps.
+    ms_per_step = per_launch_ms if flush else total_ms / args.steps
     tokens = w.B * w.H * w.T
     value = tokens * world / (ms_per_step * 1e-3)
 
     # ---- end to end through host buffers: H2D of the inputs, the call, D2H of
     # the outputs, every step, inside the timed region ------------------------
-    names = ("q", "k", "v", "lam_v", "a", "pbar", "lam0", "eta0")
     host = {n: x[n].cpu().pin_memory() for n in names}
     devb = {n: torch.empty_like(x[n]) for n in names}
     y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
@@ -228,7 +315,6 @@ def run_kla(args, world, rank, local):
     e_h = torch.empty(etaT.shape, dtype=etaT.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in (y_h, l_h, e_h))
-    e2e_steps = max(5, min(args.steps, 50))
 
     def e2e_step():
         for n in names:
@@ -239,18 +325,7 @@ def run_kla(args, world, rank, local):
         l_h.copy_(lamT, non_blocking=True)
         e_h.copy_(etaT, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / e2e_steps, world)
-    barrier(world)
+    e2e_ms = e2e_timing(e2e_step, args, world, stream)
     if rank != 0:
         return
 
@@ -262,25 +337,29 @@ def run_kla(args, world, rank, local):
     achieved = flops / (per_launch_ms * 1e-3) / 1e12
     traffic = None
     try:
-        rec = json.load(open(TRAFFIC_FILE))
+        rec = json.load(open(TRAFFIC_FILES[wname]))
         if rec.get("source_hash") == kernel_source_hash() and rec.get("plan") == plan:
             traffic = rec["dram_bytes_per_launch"]
-    except (OSError, ValueError, KeyError):
+    except (KeyError, OSError, ValueError):
         pass
-    cpu_value, cpu_desc = cpu_oracle_sample(32, 4096, os.cpu_count() or 1)
+    cpu_value, cpu_desc = cpu_oracle_sample(wname, os.cpu_count() or 1)
     launches_per_step = 1 if plan["strategy"] == "sequential" else 3
+    l2_note = (f"inputs ({in_bytes / 1e6:.0f} MB) fit in L2: {L2_FLUSH_BYTES >> 20} MB written between steps, "
+               "step time from per-launch events" if flush else
+               f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2; no flush")
     print(json.dumps({
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRICS[wname], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "headline B8 H16 T4096 dk64 dv64 bf16 I/O, fp32 state", "B": w.B, "H": w.H,
+        "config": {"workload": DESCRIPTIONS[wname], "B": w.B, "H": w.H,
                    "T": w.T, "dk": w.dk, "dv": w.dv, "io": w.io, "strategy": plan["strategy"],
                    "chunk_len": plan["chunk_len"], "cols_per_block": plan["cols_per_block"],
                    "rows_per_lane": plan["rows_per_lane"],
-                   "l2": "inputs (403 MB) larger than L2; no flush", "parallelism": f"{world} independent batches"},
+                   "l2": l2_note, "parallelism": f"{world} independent batches"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": traffic,
-                     "kernel": "kla_scan_kernel", "kernel_ms": per_launch_ms,
+                     "kernel": "kla_scan_kernel" if plan["strategy"] == "sequential" else "whole chunked pass",
+                     "kernel_ms": per_launch_ms,
                      "peak_basis": f"{nsm} SMs x 128 fp32 lanes x 2 flop x {sm_mhz:.0f} MHz (max SM clock)",
                      "flops_per_launch": flops},
         "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
@@ -291,12 +370,86 @@ def run_kla(args, world, rank, local):
     }), flush=True)
 
 
+def run_kla_decode(args, world, rank, local, w, x, stream):
+    """Decode: one kla_step over all B·H heads per step, the fp32 state
+    (λ, η) resident in HBM and updated in place; state from a kla_forward over
+    the first 1024 tokens, then the remaining tokens' inputs are fed in turn
+    (cycling when the run is longer)."""
+    import torch
+    from bayesian_filtering_linear_gb300 import kla
+    from bayesian_filtering_linear_gb300.inputs import DECODE_PREFIX
+    dev = x["q"].device
+    per_tok = ("q", "k", "v", "lam_v", "a", "pbar")
+    pre = {n: x[n][:, :, :DECODE_PREFIX].contiguous() for n in per_tok}
+    _, lam, eta = kla.forward(*(pre[n] for n in per_tok), x["lam0"], x["eta0"])
+    del pre
+    n_steps = w.T - DECODE_PREFIX
+    toks = [{n: x[n][:, :, DECODE_PREFIX + s].contiguous() for n in per_tok} for s in range(n_steps)]
+    y = torch.empty((w.B, w.H, w.dv), dtype=x["q"].dtype, device=dev)
+    it = [0]
+
+    def step():
+        t = toks[it[0] % n_steps]
+        it[0] += 1
+        kla.step(t["q"], t["k"], t["v"], t["lam_v"], t["a"], t["pbar"], lam, eta, y=y, stream=stream)
+
+    total_ms, per_launch_ms, clocks = timed_steps(step, args, world, local, stream)
+    ms_per_step = total_ms / args.steps
+    heads = w.B * w.H
+    value = heads * world / (ms_per_step * 1e-3)
+
+    host = [{n: t[n].cpu().pin_memory() for n in per_tok} for t in toks[:8]]
+    devb = {n: torch.empty_like(toks[0][n]) for n in per_tok}
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = y_h.numel() * y_h.element_size()
+    ie = [0]
+
+    def e2e_step():
+        h = host[ie[0] % len(host)]
+        ie[0] += 1
+        for n in per_tok:
+            devb[n].copy_(h[n], non_blocking=True)
+        kla.step(devb["q"], devb["k"], devb["v"], devb["lam_v"], devb["a"], devb["pbar"], lam, eta, y=y,
+                 stream=stream)
+        y_h.copy_(y, non_blocking=True)
+
+    e2e_ms = e2e_timing(e2e_step, args, world, stream)
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    io_size = x["q"].element_size()
+    bytes_per_step = 16 * heads * w.dk * w.dv + heads * (4 * w.dk + 3 * w.dv) * io_size
+    achieved = bytes_per_step / (per_launch_ms * 1e-3) / 1e9
+    cpu_value, cpu_desc = cpu_oracle_sample("decode", os.cpu_count() or 1)
+    print(json.dumps({
+        "metric": METRICS["decode"], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS["decode"], "B": w.B, "H": w.H, "dk": w.dk, "dv": w.dv, "io": w.io,
+                   "l2": f"state ({16 * heads * w.dk * w.dv / 1e6:.0f} MB read and written per step) larger "
+                         "than L2; no flush",
+                   "parallelism": f"{world} independent batches"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "kernel": "kla_step_kernel", "kernel_ms": per_launch_ms,
+                     "peak_basis": "measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "bytes_per_launch": bytes_per_step},
+        "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
+        "e2e": {"value": heads * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("kla", "reference"), default="kla")
+    ap.add_argument("--workload", choices=tuple(METRICS), default="headline")
     args = ap.parse_args(argv)
     world, rank, local = dist_info()
     if world > 1:
