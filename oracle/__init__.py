@@ -9,6 +9,10 @@ Contents
 --------
 * :func:`forward` — ctypes wrapper of ``kla_oracle.cpp``: the plain per-element
   variance-form Kalman loop in fp64 (or fp32), multithreaded over heads.
+* :func:`forward64` — the same loop on fp64 inputs (for finite differences).
+* :func:`backward` / :func:`backward64` — its exact reverse-mode derivative in
+  fp64 (gradients of a loss with respect to every input, given dL/dy and
+  optionally dL/dλ_T, dL/dη_T), with condition scales.
 * :mod:`oracle.exact` — exact-rational information-form Möbius recursion and
   dense Gaussian conditioning of the joint chain, used to pin the C++ loop.
 
@@ -55,6 +59,12 @@ def _declare(lib):
     lib.kla_oracle_forward_f64.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 5 + [ctypes.c_int]
     lib.kla_oracle_forward_f32.restype = ctypes.c_longlong
     lib.kla_oracle_forward_f32.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 3 + [ctypes.c_int]
+    lib.kla_oracle_forward_f64in.restype = ctypes.c_longlong
+    lib.kla_oracle_forward_f64in.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 3 + [ctypes.c_int]
+    for name in ("kla_oracle_backward_f64", "kla_oracle_backward_f64in"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_longlong
+        f.argtypes = [fp] * 11 + [ctypes.c_int] * 5 + [fp] * 16 + [ctypes.c_int]
     return lib
 
 
@@ -152,3 +162,100 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, precision: str = "
         raise ValueError("oracle rejected its arguments")
     out["violations"] = int(nv)
     return out
+
+
+def _f64(x):
+    if x is None:
+        return None
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu", torch.float64).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _shapes(arrs):
+    B, H, T, dk = arrs[0].shape
+    dv = arrs[2].shape[-1]
+    for x, last in zip(arrs, (dk, dk, dv, dv, dk, dk)):
+        if x.shape != (B, H, T, last):
+            raise ValueError(f"bad input shape {x.shape}, expected {(B, H, T, last)}")
+    return B, H, T, dk, dv
+
+
+def forward64(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, nthreads: int | None = None,
+              _mutant: int = 0) -> dict:
+    """The fp64 loop of :func:`forward` on fp64 inputs (no rounding of the
+    inputs to float32). Returns ``y``, ``lamT``, ``etaT``."""
+    arrs = [_f64(x) for x in (q, k, v, lam_v, a, pbar)]
+    l0, e0 = _f64(lam0), _f64(eta0)
+    B, H, T, dk, dv = _shapes(arrs)
+    y = np.empty((B, H, T, dv))
+    lamT = np.empty((B, H, dk, dv))
+    etaT = np.empty((B, H, dk, dv))
+    nv = _load(_mutant).kla_oracle_forward_f64in(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0), B, H, T, dk, dv,
+                                                 _ptr(y), _ptr(lamT), _ptr(etaT), int(nthreads or os.cpu_count() or 1))
+    if nv < 0:
+        raise ValueError("oracle rejected its arguments")
+    return {"y": y, "lamT": lamT, "etaT": etaT}
+
+
+GRAD_NAMES = ("dq", "dk", "da", "dpbar", "dv", "dlam_v", "dlam0", "deta0")
+
+
+def _backward(conv, entry, q, k, v, lam_v, a, pbar, lam0, eta0, dy, dlamT, detaT, nthreads, heads,
+              want_scales, _mutant):
+    if heads is not None:
+        B0, H0 = q.shape[:2]
+        idx = np.asarray(list(heads))
+
+        def sel(x):
+            if x is None:
+                return None
+            x = conv(x)
+            return x.reshape((B0 * H0,) + x.shape[2:])[idx][:, None]
+        q, k, v, lam_v, a, pbar, lam0, eta0, dy, dlamT, detaT = (
+            sel(x) for x in (q, k, v, lam_v, a, pbar, lam0, eta0, dy, dlamT, detaT))
+    arrs = [conv(x) for x in (q, k, v, lam_v, a, pbar)]
+    l0, e0, gy, gl, ge = (conv(x) for x in (lam0, eta0, dy, dlamT, detaT))
+    B, H, T, dk, dv = _shapes(arrs)
+    shapes = {"dq": (B, H, T, dk), "dk": (B, H, T, dk), "da": (B, H, T, dk), "dpbar": (B, H, T, dk),
+              "dv": (B, H, T, dv), "dlam_v": (B, H, T, dv), "dlam0": (B, H, dk, dv), "deta0": (B, H, dk, dv)}
+    for name, x in (("dy", gy), ("dlamT", gl), ("detaT", ge)):
+        want = (B, H, T, dv) if name == "dy" else (B, H, dk, dv)
+        if x is not None and x.shape != want:
+            raise ValueError(f"bad {name} shape {x.shape}, expected {want}")
+    grads = {n: np.zeros(shapes[n]) for n in GRAD_NAMES}
+    scales = {n: np.zeros(shapes[n]) for n in GRAD_NAMES} if want_scales else {n: None for n in GRAD_NAMES}
+    lib = _load(_mutant)
+    rc = getattr(lib, entry)(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0), _ptr(gy), _ptr(gl), _ptr(ge),
+                             B, H, T, dk, dv, *[_ptr(grads[n]) for n in GRAD_NAMES],
+                             *[_ptr(scales[n]) for n in GRAD_NAMES], int(nthreads or os.cpu_count() or 1))
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    out = dict(grads)
+    if want_scales:
+        out.update({n + "_scale": scales[n] for n in GRAD_NAMES})
+    return out
+
+
+def backward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, dy=None, dlamT=None, detaT=None, *,
+             nthreads: int | None = None, heads=None, want_scales: bool = True, _mutant: int = 0) -> dict:
+    """Gradients of a scalar loss L with respect to every input, given
+    dy = dL/dy ``[B,H,T,dv]`` and optionally dlamT, detaT = dL/dλ_T, dL/dη_T
+    ``[B,H,dk,dv]`` (None = 0), in fp64 from the float32 values the GPU reads.
+    Returns ``dq, dk, da, dpbar`` ``[B,H,T,dk]``, ``dv, dlam_v`` ``[B,H,T,dv]``,
+    ``dlam0, deta0`` ``[B,H,dk,dv]`` and, with ``want_scales``, a ``<name>_scale``
+    condition scale for each. ``heads`` selects flat head indices (returned
+    as a ``[n,1,...]`` batch), as in :func:`forward`."""
+    return _backward(_f32, "kla_oracle_backward_f64", q, k, v, lam_v, a, pbar, lam0, eta0, dy, dlamT, detaT,
+                     nthreads, heads, want_scales, _mutant)
+
+
+def backward64(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, dy=None, dlamT=None, detaT=None, *,
+               nthreads: int | None = None, want_scales: bool = False, _mutant: int = 0) -> dict:
+    """:func:`backward` on fp64 inputs (for finite-difference checks)."""
+    return _backward(_f64, "kla_oracle_backward_f64in", q, k, v, lam_v, a, pbar, lam0, eta0, dy, dlamT, detaT,
+                     nthreads, None, want_scales, _mutant)
