@@ -346,4 +346,48 @@ kla_status kla_step(const void* q, const void* k, const void* v, const void* lam
   return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 
+size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv) {
+  if (check_shape(B, H, T, dk, dv) != KLA_OK) return (size_t)-1;
+  const long long bh = (long long)B * H;
+  if (bh == 0) return 0;
+  int sms = 0;
+  if (device_sms(&sms) != KLA_OK) return (size_t)-1;
+  const kla::BwdPlan b = kla::backward_plan(bh, T, dk, dv, sms);
+  return b.ckpt_bytes + b.rowpart_bytes;
+}
+
+kla_status kla_backward(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                        const void* pbar, const float* lam0, const float* eta0, const void* gy,
+                        const float* glamT, const float* getaT, void* gq, void* gk, void* gv, void* glam_v,
+                        void* ga, void* gpbar, float* glam0, float* geta0, int B, int H, int T, int dk, int dv,
+                        kla_dtype io, void* workspace, size_t ws_bytes, void* stream) {
+  // ---- validation: no CUDA call before it passes ---------------------------
+  kla_status st = check_shape(B, H, T, dk, dv);
+  if (st != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  const long long tokens = bh * T;
+  if ((lam0 == nullptr) != (eta0 == nullptr)) return KLA_ERR_INVALID_ARG;
+  if ((glam0 == nullptr) != (geta0 == nullptr)) return KLA_ERR_INVALID_ARG;
+  if (tokens > 0 && (!q || !k || !v || !lam_v || !a || !pbar || !gq || !gk || !gv || !glam_v || !ga || !gpbar))
+    return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, lam_v, a, pbar, lam0, eta0, gy, glamT, getaT,
+                        gq, gk, gv, glam_v, ga, gpbar, glam0, geta0};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  if (glam0 && (glam0 == geta0 || overlaps_partially(glam0, geta0, (size_t)bh * dk * dv * sizeof(float))))
+    return KLA_ERR_INVALID_ARG;
+  if (bh == 0) return KLA_OK;
+
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  const kla::BwdPlan b = kla::backward_plan(bh, T, dk, dv, sms);
+  if (!workspace || ws_bytes < b.ckpt_bytes + b.rowpart_bytes) return KLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KLA_ERR_MISALIGNED;
+  kla::BackwardArgs f{q,  k,  v,  lam_v, a,     pbar, lam0, eta0, gy, glamT, getaT, gq, gk, ga,
+                      gpbar, gv, glam_v, glam0, geta0, B, H, T, dk, dv, (int)io};
+  const cudaError_t e = kla::launch_backward(f, b, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -53,6 +53,25 @@ cudaError_t launch_carry(const ForwardArgs& f, const Plan& p, const float* maps,
                          cudaStream_t s);
 cudaError_t launch_init_state(const ForwardArgs& f, cudaStream_t s);
 
+// Backward pass (kla_backward.cu): gradients of a loss given dL/dy and
+// optionally dL/dλ_T, dL/dη_T.
+struct BackwardArgs {
+  const void *q, *k, *v, *lam_v, *a, *pbar;
+  const float *lam0, *eta0;
+  const void* dy;                              // [B,H,T,dv] io, or null (zero)
+  const float *dlamT, *detaT;                  // [B,H,dk,dv] fp32, or null (zero)
+  void *dq, *dk_, *da, *dpbar, *dv_, *dlam_v;  // per-token gradients, io
+  float *dlam0, *deta0;                        // [B,H,dk,dv] fp32, or null
+  int B, H, T, dk, dv;
+  int io;
+};
+struct BwdPlan {
+  int cc, cpl, threads, ncb, nchunks;
+  size_t ckpt_bytes, rowpart_bytes, smem;
+};
+BwdPlan backward_plan(long long bh, int T, int dk, int dv, int num_sms);
+cudaError_t launch_backward(const BackwardArgs& f, const BwdPlan& b, void* workspace, cudaStream_t s);
+
 struct StepArgs {
   const void *q, *k, *v, *lam_v, *a, *pbar;
   float *lam, *eta;

@@ -23,7 +23,8 @@ _STRATEGIES = {"auto": AUTO, "sequential": SEQUENTIAL, "chunked": CHUNKED}
 _IO = {torch.float32: F32, torch.bfloat16: BF16}
 # Every function the header declares, for the export check.
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
-           "kla_status_string", "kla_version", "kla_forward_chunked_noalloc")
+           "kla_status_string", "kla_version", "kla_forward_chunked_noalloc", "kla_backward_workspace_size",
+           "kla_backward")
 
 
 class Options(ctypes.Structure):
@@ -57,6 +58,10 @@ def load_library(path: str = LIB_PATH):
     lib.kla_forward.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, ctypes.POINTER(Options), vp]
     lib.kla_step.restype = i
     lib.kla_step.argtypes = [vp] * 9 + [i] * 5 + [vp]
+    lib.kla_backward_workspace_size.restype = sz
+    lib.kla_backward_workspace_size.argtypes = [i] * 5
+    lib.kla_backward.restype = i
+    lib.kla_backward.argtypes = [vp] * 19 + [i] * 6 + [vp, sz, vp]
     return lib
 
 
@@ -187,3 +192,47 @@ def step(q, k, v, lam_v, a, pbar, lam, eta, *, y=None, stream=None):
                           _ptr(y), B, H, dk, dv, _IO[dt], _stream(stream))
     _check(st, "kla_step")
     return y
+
+
+def backward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, gy=None, glamT=None, getaT=None,
+             state_grads: bool = True, workspace=None, stream=None):
+    """Gradients of a scalar loss through :func:`forward`, given ``gy`` = dL/dy
+    ``[B,H,T,dv]`` (I/O dtype) and optionally ``glamT``, ``getaT`` = dL/dλ_T,
+    dL/dη_T (fp32 ``[B,H,dk,dv]``). Returns a dict with ``gq, gk, ga, gpbar``
+    ``[B,H,T,dk]`` and ``gv, glam_v`` ``[B,H,T,dv]`` in the I/O dtype and, with
+    ``state_grads``, ``glam0, geta0`` (fp32)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    if dt not in _IO:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    for name, t, last in (("q", q, dk), ("k", k, dk), ("a", a, dk), ("pbar", pbar, dk),
+                          ("v", v, dv), ("lam_v", lam_v, dv)):
+        _need(t, name, dt, (B, H, T, last), dev)
+    st_shape = (B, H, dk, dv)
+    for name, t in (("lam0", lam0), ("eta0", eta0), ("glamT", glamT), ("getaT", getaT)):
+        if t is not None:
+            _need(t, name, torch.float32, st_shape, dev)
+    if gy is not None:
+        _need(gy, "gy", dt, (B, H, T, dv), dev)
+    out = {n: torch.empty((B, H, T, dk), dtype=dt, device=dev) for n in ("gq", "gk", "ga", "gpbar")}
+    out.update({n: torch.empty((B, H, T, dv), dtype=dt, device=dev) for n in ("gv", "glam_v")})
+    if state_grads:
+        out["glam0"] = torch.empty(st_shape, dtype=torch.float32, device=dev)
+        out["geta0"] = torch.empty(st_shape, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            nbytes = LIB.kla_backward_workspace_size(B, H, T, dk, dv)
+            if nbytes == ctypes.c_size_t(-1).value:
+                raise KlaError(ERR_CUDA, "kla_backward_workspace_size")
+            workspace = torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        st = LIB.kla_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam0), _ptr(eta0),
+                              _ptr(gy), _ptr(glamT), _ptr(getaT), _ptr(out["gq"]), _ptr(out["gk"]), _ptr(out["gv"]),
+                              _ptr(out["glam_v"]), _ptr(out["ga"]), _ptr(out["gpbar"]), _ptr(out.get("glam0")),
+                              _ptr(out.get("geta0")), B, H, T, dk, dv, _IO[dt], _ptr(workspace), ws_bytes,
+                              _stream(stream))
+    _check(st, "kla_backward")
+    return out

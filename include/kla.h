@@ -146,6 +146,35 @@ kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void*
                                        int B, int H, int T, int dk, int dv, kla_dtype io,
                                        int chunk_len, void* stream);
 
+/* Backward pass: gradients of a scalar loss L through kla_forward. It is the
+ * exact reverse-mode derivative of the scan defined in Methodologie §1–§2 of
+ * the summary cited above (the summary itself states the forward only).
+ * A leading g names a gradient of L.
+ *   Forward inputs as for kla_forward (q, k, a, pbar, v, lam_v in `io`;
+ *     lam0, eta0 fp32 or both NULL for λ0 = 1, η0 = 0).
+ *   gy [B,H,T,dv] in `io`: dL/dy (NULL means zero).
+ *   glamT, getaT [B,H,dk,dv] fp32: dL/dλ_T, dL/dη_T (each may be NULL = zero).
+ *   Outputs, in `io`, written (not accumulated): gq, gk, ga, gpbar
+ *     [B,H,T,dk] and gv, glam_v [B,H,T,dv]. Required unless B·H·T = 0.
+ *   glam0, geta0 [B,H,dk,dv] fp32 outputs: dL/dλ0, dL/dη0 (both NULL to
+ *     skip; one NULL and the other not is INVALID_ARG). With lam0/eta0 NULL
+ *     they are the gradients at λ0 = 1, η0 = 0.
+ *   workspace / ws_bytes: device scratch of at least
+ *     kla_backward_workspace_size() bytes (required when B·H > 0; else
+ *     KLA_ERR_WORKSPACE): the forward state every 16 tokens plus, when a
+ *     head's columns are split over several blocks, per-row partial sums.
+ *   Outputs must not overlap inputs or each other. Pointers 16-byte aligned
+ *   (else MISALIGNED); shape rules and errors as for kla_forward. The order
+ *   of the per-row and per-column sums across warps is not fixed, so the
+ *   last bits of the results can differ between runs. */
+size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv);
+kla_status kla_backward(const void* q, const void* k, const void* v, const void* lam_v,
+                        const void* a, const void* pbar, const float* lam0, const float* eta0,
+                        const void* gy, const float* glamT, const float* getaT,
+                        void* gq, void* gk, void* gv, void* glam_v, void* ga, void* gpbar,
+                        float* glam0, float* geta0, int B, int H, int T, int dk, int dv,
+                        kla_dtype io, void* workspace, size_t ws_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kla_status_string(kla_status s);
 

@@ -172,3 +172,36 @@ def test_planner_rows_per_lane_choice():
                 assert p["cols_per_block"] % wc == 0
     with pytest.raises(kla.KlaError):
         kla.plan(1, 1, 64, 16, 16, "f32", rows_per_lane=8, num_sms=152)
+
+
+def bwd(B=1, H=1, T=8, dk=16, dv=16, io=kla.F32, ptrs=None, lam0=None, eta0=None, glam0=None, geta0=None,
+        ws=None, ws_bytes=0):
+    ptrs = ptrs or {}
+    g = lambda n: ptrs.get(n, P)
+    return L.kla_backward(g("q"), g("k"), g("v"), g("lam_v"), g("a"), g("pbar"), lam0, eta0, ptrs.get("gy"),
+                          ptrs.get("glamT"), ptrs.get("getaT"), g("gq"), g("gk"), g("gv"), g("glam_v"), g("ga"),
+                          g("gpbar"), glam0, geta0, B, H, T, dk, dv, io, ws, ws_bytes, None)
+
+
+def test_backward_validation_before_any_cuda_call():
+    assert bwd(dk=24) == kla.ERR_UNSUPPORTED_SHAPE
+    assert bwd(T=-1) == kla.ERR_INVALID_ARG
+    assert bwd(io=5) == kla.ERR_INVALID_ARG
+    assert bwd(lam0=P) == kla.ERR_INVALID_ARG                 # eta0 missing
+    assert bwd(glam0=P) == kla.ERR_INVALID_ARG                # geta0 missing
+    for out in ("gq", "gk", "gv", "glam_v", "ga", "gpbar", "q", "lam_v"):
+        assert bwd(ptrs={out: None}) == kla.ERR_INVALID_ARG, out
+    for name in ("gq", "gy", "glamT", "v"):
+        assert bwd(ptrs={name: MIS}) == kla.ERR_MISALIGNED, name
+    assert bwd(glam0=P, geta0=P) == kla.ERR_INVALID_ARG       # the two outputs alias
+    # nothing to do: OK without touching CUDA
+    assert bwd(B=0, ptrs={n: None for n in ("q", "k", "v", "lam_v", "a", "pbar", "gq", "gk", "gv", "glam_v",
+                                              "ga", "gpbar")}) == kla.OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_backward_without_a_device_reports_cuda_error():
+    assert bwd() == kla.ERR_CUDA
+    assert L.kla_backward_workspace_size(1, 1, 8, 16, 16) == ctypes.c_size_t(-1).value
+    assert L.kla_backward_workspace_size(0, 4, 8, 16, 16) == 0
+    assert L.kla_backward_workspace_size(1, 1, 8, 20, 16) == ctypes.c_size_t(-1).value
