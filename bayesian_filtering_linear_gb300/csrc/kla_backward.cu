@@ -22,20 +22,21 @@
 //  1. kla_bwd_checkpoint_kernel runs the forward once and stores the state
 //     (P, μ) of every element at the start of every chunk of kChunk tokens,
 //     and at the end, into the workspace.
-//  2. kla_bwd_kernel walks the chunks from last to first. For each chunk it
-//     re-runs the forward from the checkpoint, keeping the state before each
-//     token in thread-local memory (each thread reads back only what it
-//     wrote), then runs the adjoint recursion backwards over the chunk.
+//  2. kla_bwd_kernel walks the chunks from last to first, each in sub-chunks
+//     of kSub tokens from its end: it re-runs the forward from the chunk's
+//     checkpoint to the sub-chunk, keeps the states before the sub-chunk's
+//     tokens in registers, and runs the adjoint recursion back over them
+//     (forward work per token: about 2.5 steps, no state traffic to memory).
 //  3. kla_bwd_finish_kernel (only when a head's columns are split over
 //     several blocks) adds the per-row partial sums of the blocks.
 //
 // Layout of a block: (head, column block of cc columns, all d_k rows). A lane
-// owns one row and CPL consecutive columns, so every per-row sum (dq, dk, da,
-// dp̄) is first a sum inside the lane; a warp covers RW = min(32, d_k) rows
-// and 32/RW column groups; per-column sums (dv, dΛ^v) over the warp's rows
-// are a butterfly reduce-scatter across its lanes. Sums across warps go
-// through shared-memory atomics (their order is not fixed, so the last bits
-// of those sums can differ from run to run).
+// owns one row and kCpl = 8 consecutive columns (four fp32x2 pairs), so every
+// per-row sum (dq, dk, da, dp̄) is first a sum inside the lane; a warp covers
+// RW = min(32, d_k) rows and 32/RW column groups; per-column sums (dv, dΛ^v)
+// over the warp's rows are a butterfly reduce-scatter across its lanes. Sums
+// across warps go through shared-memory atomics (their order is not fixed,
+// so the last bits of those sums can differ from run to run).
 #include <algorithm>
 
 #include <cuda_runtime.h>
@@ -47,6 +48,8 @@ namespace kla {
 namespace {
 
 constexpr int kChunk = 16;  // tokens per checkpoint interval and per staged tile
+constexpr int kCpl = 8;     // columns per lane
+constexpr int kSub = 4;     // tokens per reverse sub-chunk (states kept in shared memory)
 
 struct BwdParams {
   const void *q, *k, *v, *lam_v, *a, *pbar;
@@ -56,7 +59,7 @@ struct BwdParams {
   void *gq, *gk, *gv, *glam_v, *ga, *gpbar;  // per-token gradients (io dtype)
   float *dlam0, *deta0;
   float* ckpt;     // [nchunks + 1][2][elems]: (P, μ) at each chunk start, then at T
-  float* rowpart;  // [ncb][4][B·H·T·d_k] per-row partial sums when ncb > 1, else null
+  float* rowpart;  // [B·H·T·d_k][4] fp32 per-row sums (dq, dk, da, dp̄) when ncb > 1, else null
   int T, dk, dv, cc, ncb, nchunks;
   long long elems;  // B·H·d_k·d_v
 };
@@ -67,15 +70,16 @@ struct BwdGeo {
   static constexpr int CG = 32 / RW;            // column groups per warp
   static constexpr int WCOLS = CG * CPL;        // columns per warp
   static constexpr int NWR = DK / RW;           // warps along rows
-  static constexpr int NV = 2 * CPL;            // per-column values a lane reduces per token
 };
 
 // Shared memory of one block (fp32): staged per-row inputs q, k, a, p̄
-// [kChunk][DK] and per-column inputs v, Λ^v, dy [kChunk][cc], and the
+// [kChunk][DK] and per-column inputs v, Λ^v, Λ^v·v, dy [kChunk][cc], the
 // per-token accumulators of the row sums [kChunk][4][DK] and column sums
-// [kChunk][2][cc].
+// [kChunk][2][cc], and each thread's states before the tokens of the current
+// sub-chunk, [kSub][2][kCpl/2][threads] fp32x2 (thread-fastest, so a warp's
+// accesses are contiguous).
 struct BwdSmem {
-  float *q, *k, *a, *p, *v, *L, *dy, *racc, *cacc;
+  float *q, *k, *a, *p, *v, *L, *Lv, *dy, *racc, *cacc, *st;
   __device__ BwdSmem(float* base, int dk, int cc) {
     q = base;
     k = q + kChunk * dk;
@@ -83,12 +87,15 @@ struct BwdSmem {
     p = a + kChunk * dk;
     v = p + kChunk * dk;
     L = v + kChunk * cc;
-    dy = L + kChunk * cc;
+    Lv = L + kChunk * cc;
+    dy = Lv + kChunk * cc;
     racc = dy + kChunk * cc;
     cacc = racc + kChunk * 4 * dk;
+    st = cacc + kChunk * 2 * cc;
   }
-  __host__ __device__ static size_t bytes(int dk, int cc) {
-    return sizeof(float) * ((size_t)kChunk * (4 * dk + 3 * cc) + (size_t)kChunk * 4 * dk + (size_t)kChunk * 2 * cc);
+  __host__ __device__ static size_t bytes(int dk, int cc, int threads) {
+    return sizeof(float) * ((size_t)kChunk * (4 * dk + 4 * cc) + (size_t)kChunk * 4 * dk + (size_t)kChunk * 2 * cc +
+                            (size_t)kSub * 2 * kCpl * threads);
   }
 };
 
@@ -115,6 +122,7 @@ __device__ void stage_chunk(const BwdParams& p, const BwdSmem& s, long long bh, 
     const size_t g = ((size_t)bh * p.T + t0 + t) * p.dv + jb + j;
     s.v[x] = ld<IO>(p.v, g);
     s.L[x] = ld<IO>(p.lam_v, g);
+    s.Lv[x] = s.L[x] * s.v[x];
     s.dy[x] = (with_dy && p.dy) ? ld<IO>(p.dy, g) : 0.0f;
   }
 }
@@ -213,127 +221,204 @@ __global__ void __launch_bounds__(512) kla_bwd_checkpoint_kernel(const BwdParams
 }
 
 // Butterfly reduce-scatter of NV per-lane values over the RW lanes of a
-// column group (lanes differing in their low log2(RW) bits): afterwards lane
-// holds, in v[0 .. NV/RW), the group sums of the values whose indices it
-// returns through `first` (consecutive from there).
+// column group (lanes differing in their low log2(RW) bits). While a lane
+// still holds more than one value, each round halves them (keeping one half,
+// sending the other); after that the rounds add whole values. Afterwards v[0]
+// holds the group sum of value `first`, and `owner` says whether this lane
+// is the one of the lanes holding that same sum that should publish it.
 template <int RW, int NV>
-__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane, int& first) {
-  static_assert(NV >= RW, "each lane keeps at least one value");
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane, int& first, bool& owner) {
   first = 0;
+  owner = true;
+  int nv = NV;
 #pragma unroll
-  for (int m = RW / 2, half = NV / 2; m >= 1; m >>= 1, half >>= 1) {
-    const bool upper = (lane & m) != 0;
+  for (int m = RW / 2; m >= 1; m >>= 1) {
+    if (nv > 1) {
+      const int half = nv / 2;
+      const bool upper = (lane & m) != 0;
 #pragma unroll
-    for (int u = 0; u < half; ++u) {
-      const float send = upper ? v[u] : v[u + half];
-      const float keep = upper ? v[u + half] : v[u];
-      v[u] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      for (int u = 0; u < NV / 2; ++u) {
+        if (u < half) {
+          const float send = upper ? v[u] : v[u + half];
+          const float keep = upper ? v[u + half] : v[u];
+          v[u] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      if (upper) first += half;
+      nv = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+      if (lane & m) owner = false;
     }
-    if (upper) first += half;
   }
 }
 
-// Pass 2: chunks from last to first; recompute, then the adjoint recursion.
+// Pass 2: chunks from last to first. A chunk (kChunk tokens, staged in
+// shared memory) is processed in sub-chunks of kSub tokens from its end: the
+// state at the sub-chunk's start is recomputed from the chunk's checkpoint,
+// the states before each of the sub-chunk's tokens are kept in registers,
+// and the adjoint recursion runs back over them. Arithmetic is packed fp32x2
+// over pairs of adjacent columns.
+
 template <typename IO, int DK, int CPL>
 __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
   using G = BwdGeo<DK, CPL>;
+  constexpr int NP = CPL / 2;  // column pairs per lane
   extern __shared__ __align__(16) float bwd_smem[];
   const BwdSmem s(bwd_smem, DK, p.cc);
   const long long bh = blockIdx.x;
   const int jb = blockIdx.y * p.cc;
   const BwdLane<DK, CPL> ln(p, bh, jb);
   const int i = ln.i, jl = ln.jl;
-  const size_t BHTdk = (size_t)gridDim.x * p.T * DK;
+  const f2 one2 = f2_make(1.0f, 1.0f), m1 = f2_make(-1.0f, -1.0f);
+
+  auto load_pairs = [&](const float* src, f2 (&P)[NP], f2 (&M)[NP]) {
+#pragma unroll
+    for (int u = 0; u < NP; u += 2) {
+      const ulonglong2 p4 = *reinterpret_cast<const ulonglong2*>(src + ln.e0 + 2 * u);
+      const ulonglong2 m4 = *reinterpret_cast<const ulonglong2*>(src + p.elems + ln.e0 + 2 * u);
+      P[u] = p4.x; P[u + 1] = p4.y;
+      M[u] = m4.x; M[u + 1] = m4.y;
+    }
+  };
+  // one forward token (staged token t) on the lane's column pairs
+  auto fwd = [&](int t, f2 (&P)[NP], f2 (&M)[NP]) {
+    const float at = s.a[t * DK + i], kt = s.k[t * DK + i];
+    const f2 a1 = f2_make(at, at), a2 = f2_make(at * at, at * at), pb = f2_make(s.p[t * DK + i], s.p[t * DK + i]);
+    const f2 k1 = f2_make(kt, kt), k2 = f2_make(kt * kt, kt * kt);
+#pragma unroll
+    for (int u = 0; u < NP; u += 2) {
+      const ulonglong2 L4 = *reinterpret_cast<const ulonglong2*>(s.L + t * p.cc + jl + 2 * u);
+      const ulonglong2 lv4 = *reinterpret_cast<const ulonglong2*>(s.Lv + t * p.cc + jl + 2 * u);
+      const f2 Ls[2] = {L4.x, L4.y}, Lvs[2] = {lv4.x, lv4.y};
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const f2 Pp = f2_fma(a2, P[u + x], pb);
+        const f2 w = f2_rcp(f2_fma(f2_mul(k2, Ls[x]), Pp, one2));
+        const f2 b = f2_mul(k1, Lvs[x]);
+        const f2 uu = f2_fma(Pp, b, f2_mul(a1, M[u + x]));
+        P[u + x] = f2_mul(w, Pp);
+        M[u + x] = f2_mul(w, uu);
+      }
+    }
+  };
 
   // terminal adjoints from dλ_T, dη_T through λ_T = 1/P_T, η_T = μ_T/P_T
-  float Pb[CPL], Mb[CPL];
+  f2 Pb[NP], Mb[NP];
   {
-    float PT[CPL], MT[CPL];
-    load_state<CPL>(p.ckpt + (size_t)p.nchunks * 2 * p.elems, ln.e0, p.elems, PT, MT);
+    f2 PT[NP], MT[NP];
+    load_pairs(p.ckpt + (size_t)p.nchunks * 2 * p.elems, PT, MT);
 #pragma unroll
-    for (int u = 0; u < CPL; ++u) {
-      const float dl = p.dlamT ? p.dlamT[ln.e0 + u] : 0.0f;
-      const float de = p.detaT ? p.detaT[ln.e0 + u] : 0.0f;
-      const float r = 1.0f / PT[u];
-      Pb[u] = -(dl + de * MT[u]) * r * r;
-      Mb[u] = de * r;
+    for (int u = 0; u < NP; ++u) {
+      float pbv[2], mbv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const size_t e = ln.e0 + 2 * u + h;
+        const float dl = p.dlamT ? p.dlamT[e] : 0.0f, de = p.detaT ? p.detaT[e] : 0.0f;
+        const float PTh = h ? f2_hi(PT[u]) : f2_lo(PT[u]), MTh = h ? f2_hi(MT[u]) : f2_lo(MT[u]);
+        const float r = 1.0f / PTh;
+        pbv[h] = -(dl + de * MTh) * r * r;
+        mbv[h] = de * r;
+      }
+      Pb[u] = f2_make(pbv[0], pbv[1]);
+      Mb[u] = f2_make(mbv[0], mbv[1]);
     }
   }
-  float Ps[kChunk][CPL], Ms[kChunk][CPL];  // states before each token of the chunk (thread-local)
+
   for (int c = p.nchunks - 1; c >= 0; --c) {
     const int t0 = c * kChunk, tl = min(kChunk, p.T - t0);
     __syncthreads();  // the previous chunk's staged inputs and sums are no longer read
     stage_chunk<IO>(p, s, bh, jb, t0, tl, true);
     for (int x = threadIdx.x; x < kChunk * (4 * DK + 2 * p.cc); x += blockDim.x) s.racc[x] = 0.0f;
     __syncthreads();
-    {  // recompute the chunk's states from its checkpoint
-      float P[CPL], M[CPL];
-      load_state<CPL>(p.ckpt + (size_t)c * 2 * p.elems, ln.e0, p.elems, P, M);
+    const float* ck = p.ckpt + (size_t)c * 2 * p.elems;
+    for (int sb = (tl - 1) / kSub; sb >= 0; --sb) {
+      const int ts = sb * kSub;
+      f2 P[NP], M[NP];
+      load_pairs(ck, P, M);
 #pragma unroll 1
-      for (int t = 0; t < tl; ++t) {
+      for (int t = 0; t < ts; ++t) fwd(t, P, M);
+      f2* st = reinterpret_cast<f2*>(s.st) + threadIdx.x;
+      const int nthr = blockDim.x;
+      auto Ps = [&](int r, int u) -> f2& { return st[((r * 2 + 0) * NP + u) * nthr]; };
+      auto Ms = [&](int r, int u) -> f2& { return st[((r * 2 + 1) * NP + u) * nthr]; };
 #pragma unroll
-        for (int u = 0; u < CPL; ++u) {
-          Ps[t][u] = P[u];
-          Ms[t][u] = M[u];
+      for (int r = 0; r < kSub; ++r) {
+#pragma unroll
+        for (int u = 0; u < NP; ++u) {
+          Ps(r, u) = P[u];
+          Ms(r, u) = M[u];
         }
-        forward_token<DK, CPL>(s, p.cc, t, i, jl, P, M);
+        if (r + 1 < kSub && ts + r < tl) fwd(ts + r, P, M);
       }
-    }
-#pragma unroll 1
-    for (int t = tl - 1; t >= 0; --t) {
-      const float at = s.a[t * DK + i], pt = s.p[t * DK + i], kt = s.k[t * DK + i], qt = s.q[t * DK + i];
-      const float a2 = at * at, k2 = kt * kt;
-      float rq = 0.f, rda1 = 0.f, rda2 = 0.f, rdp = 0.f, rdk1 = 0.f, rdk2 = 0.f;
-      float cv[G::NV];  // per column: k²c̄ + kv·b̄ (dΛ^v), then k·b̄ (dv / Λ^v)
 #pragma unroll
-      for (int u4 = 0; u4 < CPL; u4 += 4) {
-        const float4 L4 = *reinterpret_cast<const float4*>(s.L + t * p.cc + jl + u4);
-        const float4 v4 = *reinterpret_cast<const float4*>(s.v + t * p.cc + jl + u4);
-        const float4 g4 = *reinterpret_cast<const float4*>(s.dy + t * p.cc + jl + u4);
-        const float Ls[4] = {L4.x, L4.y, L4.z, L4.w}, vs[4] = {v4.x, v4.y, v4.z, v4.w};
-        const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+      for (int r = kSub - 1; r >= 0; --r) {
+        const int t = ts + r;
+        if (t >= tl) continue;
+        const float at = s.a[t * DK + i], kt = s.k[t * DK + i], qt = s.q[t * DK + i], pt = s.p[t * DK + i];
+        const f2 a1 = f2_make(at, at), a2 = f2_make(at * at, at * at), pb = f2_make(pt, pt);
+        const f2 k1 = f2_make(kt, kt), k2 = f2_make(kt * kt, kt * kt), q1 = f2_make(qt, qt);
+        const f2 nk2 = f2_make(-kt * kt, -kt * kt);
+        const f2 zero = f2_make(0.0f, 0.0f);
+        f2 rq = zero, rda1 = zero, rda2 = zero, rdp = zero, rdk1n = zero, rdk2 = zero;
+        float cv[2 * CPL];  // per column: k²c̄, then k·b̄
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const int u = u4 + x;
-          const float P = Ps[t][u], M = Ms[t][u];
-          const float Pp = fmaf(a2, P, pt);
-          const float cobs = k2 * Ls[x];
-          const float w = rcp_approx(fmaf(cobs, Pp, 1.0f));
-          const float Lv = Ls[x] * vs[x];
-          const float b = kt * Lv;
-          const float uu = fmaf(Pp, b, at * M);
-          const float mu_t = w * uu;
-          const float mb = fmaf(qt, gs[x], Mb[u]);
-          rq = fmaf(gs[x], mu_t, rq);
-          const float ub = mb * w;
-          const float wb = fmaf(mb, uu, Pb[u] * Pp);
-          const float w2 = w * w;
-          const float Ppb = fmaf(Pb[u], w, fmaf(ub, b, -wb * cobs * w2));
-          const float cb = -wb * Pp * w2;
-          const float bb = ub * Pp;
-          rda1 = fmaf(ub, M, rda1);
-          rda2 = fmaf(P, Ppb, rda2);
-          rdp += Ppb;
-          rdk1 = fmaf(Ls[x], cb, rdk1);
-          rdk2 = fmaf(Lv, bb, rdk2);
-          cv[u] = fmaf(kt * vs[x], bb, k2 * cb);
-          cv[CPL + u] = kt * bb;
-          Pb[u] = a2 * Ppb;
-          Mb[u] = at * ub;
+        for (int u = 0; u < NP; u += 2) {
+          const ulonglong2 L4 = *reinterpret_cast<const ulonglong2*>(s.L + t * p.cc + jl + 2 * u);
+          const ulonglong2 lv4 = *reinterpret_cast<const ulonglong2*>(s.Lv + t * p.cc + jl + 2 * u);
+          const ulonglong2 g4 = *reinterpret_cast<const ulonglong2*>(s.dy + t * p.cc + jl + 2 * u);
+          const f2 Ls[2] = {L4.x, L4.y}, Lvs[2] = {lv4.x, lv4.y}, gs[2] = {g4.x, g4.y};
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int uu2 = u + x;
+            const f2 P0 = Ps(r, uu2), M0 = Ms(r, uu2);
+            const f2 Pp = f2_fma(a2, P0, pb);
+            const f2 cobs = f2_mul(k2, Ls[x]);
+            const f2 w = f2_rcp(f2_fma(cobs, Pp, one2));
+            const f2 b = f2_mul(k1, Lvs[x]);
+            const f2 uu = f2_fma(Pp, b, f2_mul(a1, M0));
+            const f2 mu_t = f2_mul(w, uu);
+            const f2 mb = f2_fma(q1, gs[x], Mb[uu2]);
+            rq = f2_fma(gs[x], mu_t, rq);
+            const f2 ub = f2_mul(mb, w);
+            // With 1 − cP⁻w = w and μ̄w = ū, uw = μ':
+            //   P̄⁻ = P̄w + ūb − w̄cw² = P̄w² + ū(b − cμ'),
+            //   −c̄ = w̄P⁻w² = P⁻(ūμ' + P̄w²P⁻).
+            const f2 Pbw2 = f2_mul(Pb[uu2], f2_mul(w, w));
+            const f2 Ppb = f2_fma(ub, f2_fma(f2_mul(cobs, mu_t), m1, b), Pbw2);
+            const f2 cbn = f2_mul(Pp, f2_fma(Pbw2, Pp, f2_mul(ub, mu_t)));
+            const f2 bb = f2_mul(ub, Pp);
+            rda1 = f2_fma(ub, M0, rda1);
+            rda2 = f2_fma(P0, Ppb, rda2);
+            rdp = f2_add(rdp, Ppb);
+            rdk1n = f2_fma(Ls[x], cbn, rdk1n);
+            rdk2 = f2_fma(Lvs[x], bb, rdk2);
+            // dΛ^v_j = Σ_i k²c̄ + v_j Σ_i k b̄ and dv_j = Λ^v_j Σ_i k b̄: per element
+            // only −k²·(−c̄) and k·b̄ are summed over the rows.
+            const f2 xl = f2_mul(nk2, cbn);
+            const f2 zl = f2_mul(k1, bb);
+            cv[2 * uu2] = f2_lo(xl);
+            cv[2 * uu2 + 1] = f2_hi(xl);
+            cv[CPL + 2 * uu2] = f2_lo(zl);
+            cv[CPL + 2 * uu2 + 1] = f2_hi(zl);
+            Pb[uu2] = f2_mul(a2, Ppb);
+            Mb[uu2] = f2_mul(a1, ub);
+          }
         }
-      }
-      float* racc = s.racc + t * 4 * DK + i;
-      atomicAdd(racc + 0 * DK, rq);
-      atomicAdd(racc + 1 * DK, fmaf(2.0f * kt, rdk1, rdk2));
-      atomicAdd(racc + 2 * DK, fmaf(2.0f * at, rda2, rda1));
-      atomicAdd(racc + 3 * DK, rdp);
-      int first;
-      reduce_scatter<G::RW, G::NV>(cv, ln.lane, first);
+        float* racc = s.racc + t * 4 * DK + i;
+        atomicAdd(racc + 0 * DK, f2_lo(rq) + f2_hi(rq));
+        atomicAdd(racc + 1 * DK, fmaf(-2.0f * kt, f2_lo(rdk1n) + f2_hi(rdk1n), f2_lo(rdk2) + f2_hi(rdk2)));
+        atomicAdd(racc + 2 * DK, fmaf(2.0f * at, f2_lo(rda2) + f2_hi(rda2), f2_lo(rda1) + f2_hi(rda1)));
+        atomicAdd(racc + 3 * DK, f2_lo(rdp) + f2_hi(rdp));
+        int first;
+        bool owner;
+        reduce_scatter<G::RW, 2 * CPL>(cv, ln.lane, first, owner);
+        constexpr int KEEP = (2 * CPL) / G::RW > 0 ? (2 * CPL) / G::RW : 1;
 #pragma unroll
-      for (int r = 0; r < G::NV / G::RW; ++r) {
-        const int idx = first + r;
-        const int kind = idx / CPL, col = jl + idx % CPL;
-        atomicAdd(s.cacc + (t * 2 + kind) * p.cc + col, cv[r]);
+        for (int rr = 0; rr < KEEP; ++rr) {
+          const int idx = first + rr;
+          if (owner) atomicAdd(s.cacc + (t * 2 + idx / CPL) * p.cc + jl + idx % CPL, cv[rr]);
+        }
       }
     }
     __syncthreads();
@@ -347,44 +432,44 @@ __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
         reinterpret_cast<IO*>(p.gk)[g] = from_f32<IO>(acc[DK]);
         reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(acc[2 * DK]);
         reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(acc[3 * DK]);
-      } else {
-        float* part = p.rowpart + (size_t)blockIdx.y * 4 * BHTdk + g;
-#pragma unroll
-        for (int kq = 0; kq < 4; ++kq) part[kq * BHTdk] = acc[kq * DK];
+      } else {  // other column blocks add to the same rows: accumulate in fp32
+        atomicAdd(reinterpret_cast<float4*>(p.rowpart) + g, make_float4(acc[0], acc[DK], acc[2 * DK], acc[3 * DK]));
       }
     }
     for (int x = threadIdx.x; x < tl * p.cc; x += blockDim.x) {
       const int t = x / p.cc, j = x - t * p.cc;
       const size_t g = ((size_t)bh * p.T + t0 + t) * p.dv + jb + j;
-      reinterpret_cast<IO*>(p.glam_v)[g] = from_f32<IO>(s.cacc[(t * 2) * p.cc + j]);
-      reinterpret_cast<IO*>(p.gv)[g] = from_f32<IO>(s.L[t * p.cc + j] * s.cacc[(t * 2 + 1) * p.cc + j]);
+      const float sz = s.cacc[(t * 2 + 1) * p.cc + j];  // Σ_i k b̄
+      reinterpret_cast<IO*>(p.glam_v)[g] = from_f32<IO>(fmaf(s.v[t * p.cc + j], sz, s.cacc[(t * 2) * p.cc + j]));
+      reinterpret_cast<IO*>(p.gv)[g] = from_f32<IO>(s.L[t * p.cc + j] * sz);
     }
   }
   // initial-state gradients through P0 = 1/λ0, μ0 = η0/λ0
   if (p.dlam0) {
 #pragma unroll
-    for (int u = 0; u < CPL; ++u) {
-      const float l0 = p.lam0 ? p.lam0[ln.e0 + u] : 1.0f;
-      const float n0 = p.eta0 ? p.eta0[ln.e0 + u] : 0.0f;
-      const float r = 1.0f / l0;
-      p.dlam0[ln.e0 + u] = -(Pb[u] + Mb[u] * n0) * r * r;
-      p.deta0[ln.e0 + u] = Mb[u] * r;
+    for (int u = 0; u < NP; ++u) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const size_t e = ln.e0 + 2 * u + h;
+        const float l0 = p.lam0 ? p.lam0[e] : 1.0f, n0 = p.eta0 ? p.eta0[e] : 0.0f;
+        const float pbv = h ? f2_hi(Pb[u]) : f2_lo(Pb[u]), mbv = h ? f2_hi(Mb[u]) : f2_lo(Mb[u]);
+        const float r = 1.0f / l0;
+        p.dlam0[e] = -(pbv + mbv * n0) * r * r;
+        p.deta0[e] = mbv * r;
+      }
     }
   }
 }
 
-// Pass 3 (ncb > 1): add the column blocks' per-row partial sums.
+// Pass 3 (ncb > 1): convert the accumulated per-row sums to the I/O dtype.
 template <typename IO>
 __global__ void kla_bwd_finish_kernel(const BwdParams p, size_t BHTdk) {
   for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < BHTdk; g += (size_t)gridDim.x * blockDim.x) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int cb = 0; cb < p.ncb; ++cb)
-#pragma unroll
-      for (int kq = 0; kq < 4; ++kq) acc[kq] += p.rowpart[((size_t)cb * 4 + kq) * BHTdk + g];
-    reinterpret_cast<IO*>(p.gq)[g] = from_f32<IO>(acc[0]);
-    reinterpret_cast<IO*>(p.gk)[g] = from_f32<IO>(acc[1]);
-    reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(acc[2]);
-    reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(acc[3]);
+    const float4 acc = reinterpret_cast<const float4*>(p.rowpart)[g];
+    reinterpret_cast<IO*>(p.gq)[g] = from_f32<IO>(acc.x);
+    reinterpret_cast<IO*>(p.gk)[g] = from_f32<IO>(acc.y);
+    reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(acc.z);
+    reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(acc.w);
   }
 }
 
@@ -397,28 +482,29 @@ cudaError_t launch_bwd_typed(const BwdParams& bp, dim3 grid, int threads, size_t
     if (e == cudaSuccess) e = cudaFuncSetAttribute(bw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  const size_t BHTdk = (size_t)grid.x * bp.T * DK;
+  if (bp.ncb > 1 && BHTdk > 0) {
+    const cudaError_t e = cudaMemsetAsync(bp.rowpart, 0, BHTdk * 4 * sizeof(float), s);
+    if (e != cudaSuccess) return e;
+  }
   ck<<<grid, threads, smem, s>>>(bp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   bw<<<grid, threads, smem, s>>>(bp);
   e = cudaGetLastError();
-  if (e != cudaSuccess || bp.ncb == 1) return e;
-  const size_t BHTdk = (size_t)grid.x * bp.T * DK;
-  if (BHTdk == 0) return cudaSuccess;
+  if (e != cudaSuccess || bp.ncb == 1 || BHTdk == 0) return e;
   const unsigned blocks = (unsigned)std::min<size_t>((BHTdk + 255) / 256, 4096);
   kla_bwd_finish_kernel<IO><<<blocks, 256, 0, s>>>(bp, BHTdk);
   return cudaGetLastError();
 }
 
 template <typename IO>
-cudaError_t launch_bwd_io(int dk, int cpl, const BwdParams& bp, dim3 grid, int threads, size_t smem,
-                          cudaStream_t s) {
-  switch (dk * 100 + cpl) {
-    case 1608: return launch_bwd_typed<IO, 16, 8>(bp, grid, threads, smem, s);
-    case 1616: return launch_bwd_typed<IO, 16, 16>(bp, grid, threads, smem, s);
-    case 3216: return launch_bwd_typed<IO, 32, 16>(bp, grid, threads, smem, s);
-    case 6416: return launch_bwd_typed<IO, 64, 16>(bp, grid, threads, smem, s);
-    case 12816: return launch_bwd_typed<IO, 128, 16>(bp, grid, threads, smem, s);
+cudaError_t launch_bwd_io(int dk, const BwdParams& bp, dim3 grid, int threads, size_t smem, cudaStream_t s) {
+  switch (dk) {
+    case 16: return launch_bwd_typed<IO, 16, kCpl>(bp, grid, threads, smem, s);
+    case 32: return launch_bwd_typed<IO, 32, kCpl>(bp, grid, threads, smem, s);
+    case 64: return launch_bwd_typed<IO, 64, kCpl>(bp, grid, threads, smem, s);
+    case 128: return launch_bwd_typed<IO, 128, kCpl>(bp, grid, threads, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -427,20 +513,25 @@ cudaError_t launch_bwd_io(int dk, int cpl, const BwdParams& bp, dim3 grid, int t
 
 BwdPlan backward_plan(long long bh, int T, int dk, int dv, int num_sms) {
   BwdPlan b{};
-  b.cpl = (dk == 16 && dv == 16) ? 8 : 16;
-  const int rw = dk < 32 ? dk : 32, wcols = (32 / rw) * b.cpl, nwr = dk / rw;
+  b.cpl = kCpl;
+  const int rw = dk < 32 ? dk : 32, wcols = (32 / rw) * kCpl, nwr = dk / rw;
+  constexpr int kMaxWarps = 16;  // 512 threads at the reverse kernel's register budget
+  constexpr size_t kMaxSmem = 220 * 1024;
   int cc = dv;
-  while (cc > wcols && (nwr * (cc / wcols) > 16 || BwdSmem::bytes(dk, cc) > 200 * 1024)) cc /= 2;
-  // Few heads: narrower column blocks, so that there are blocks for every SM.
-  while (cc > wcols && bh * (dv / cc) < num_sms) cc /= 2;
+  while (cc > wcols &&
+         (nwr * (cc / wcols) > kMaxWarps || BwdSmem::bytes(dk, cc, 32 * nwr * (cc / wcols)) > kMaxSmem))
+    cc /= 2;
+  // Few heads: narrower column blocks, so that at least half the SMs get a
+  // block (a block of up to 16 warps keeps an SM busy on its own).
+  while (cc > wcols && 2 * bh * (dv / cc) < num_sms) cc /= 2;
   b.cc = cc;
   b.threads = 32 * nwr * (cc / wcols);
   b.ncb = dv / cc;
   b.nchunks = (T + kChunk - 1) / kChunk;
   const long long elems = bh * dk * dv;
   b.ckpt_bytes = (size_t)(b.nchunks + 1) * 2 * (size_t)elems * sizeof(float);
-  b.rowpart_bytes = b.ncb > 1 ? (size_t)b.ncb * 4 * (size_t)bh * T * dk * sizeof(float) : 0;
-  b.smem = BwdSmem::bytes(dk, cc);
+  b.rowpart_bytes = b.ncb > 1 ? (size_t)4 * (size_t)bh * T * dk * sizeof(float) : 0;
+  b.smem = BwdSmem::bytes(dk, cc, b.threads);
   return b;
 }
 
@@ -458,8 +549,8 @@ cudaError_t launch_backward(const BackwardArgs& f, const BwdPlan& b, void* works
   bp.T = f.T; bp.dk = f.dk; bp.dv = f.dv; bp.cc = b.cc; bp.ncb = b.ncb; bp.nchunks = b.nchunks;
   bp.elems = bh * f.dk * f.dv;
   const dim3 grid((unsigned)bh, (unsigned)b.ncb);
-  return f.io == IO_BF16 ? launch_bwd_io<__nv_bfloat16>(f.dk, b.cpl, bp, grid, b.threads, b.smem, s)
-                         : launch_bwd_io<float>(f.dk, b.cpl, bp, grid, b.threads, b.smem, s);
+  return f.io == IO_BF16 ? launch_bwd_io<__nv_bfloat16>(f.dk, bp, grid, b.threads, b.smem, s)
+                         : launch_bwd_io<float>(f.dk, bp, grid, b.threads, b.smem, s);
 }
 
 }  // namespace kla
