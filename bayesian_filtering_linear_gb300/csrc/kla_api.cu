@@ -384,9 +384,18 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
   const kla::BwdPlan b = kla::backward_plan(bh, T, dk, dv, sms);
   if (!workspace || ws_bytes < b.ckpt_bytes + b.rowpart_bytes) return KLA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KLA_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T > 0) {  // forward scan storing its state every 16 tokens (no y)
+    const kla_options seq{KLA_SEQUENTIAL, 0, 0};
+    Plan fp{};
+    if ((st = make_plan(B, H, T, dk, dv, io, &seq, sms, &fp)) != KLA_OK) return st;
+    kla::ForwardArgs ff{q, k, v, lam_v, a, pbar, lam0, eta0, nullptr, nullptr, nullptr, B, H, T, dk, dv, (int)io};
+    if (kla::launch_forward(ff, fp, nullptr, s, reinterpret_cast<float*>(workspace)) != cudaSuccess)
+      return KLA_ERR_CUDA;
+  }
   kla::BackwardArgs f{q,  k,  v,  lam_v, a,     pbar, lam0, eta0, gy, glamT, getaT, gq, gk, ga,
                       gpbar, gv, glam_v, glam0, geta0, B, H, T, dk, dv, (int)io};
-  const cudaError_t e = kla::launch_backward(f, b, workspace, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = kla::launch_backward(f, b, workspace, s);
   return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 

@@ -19,9 +19,9 @@
 // dλ0 = −(P̄ + μ̄η0)/λ0², dη0 = μ̄/λ0 (P0 = 1/λ0, μ0 = η0/λ0).
 //
 // GPU plan (three kernels, all on the caller's stream):
-//  1. kla_bwd_checkpoint_kernel runs the forward once and stores the state
-//     (P, μ) of every element at the start of every chunk of kChunk tokens,
-//     and at the end, into the workspace.
+//  1. The forward scan kernel (sequential plan, no y) stores the scaled state
+//     (P̃ = K·P, μ) of every element before every 16-token tile and at the
+//     end into the workspace (kla_scan.cu).
 //  2. kla_bwd_kernel walks the chunks from last to first, each in sub-chunks
 //     of kSub tokens from its end: it re-runs the forward from the chunk's
 //     checkpoint to the sub-chunk, keeps the states before the sub-chunk's
@@ -50,6 +50,7 @@ namespace {
 constexpr int kChunk = 16;  // tokens per checkpoint interval and per staged tile
 constexpr int kCpl = 8;     // columns per lane
 constexpr int kSub = 4;     // tokens per reverse sub-chunk (states kept in shared memory)
+static_assert(kChunk == kScanTile, "the forward scan checkpoints once per tile");
 
 struct BwdParams {
   const void *q, *k, *v, *lam_v, *a, *pbar;
@@ -127,31 +128,7 @@ __device__ void stage_chunk(const BwdParams& p, const BwdSmem& s, long long bh, 
   }
 }
 
-// One forward token for a lane's CPL elements of row i (staged token t).
-template <int DK, int CPL>
-__device__ __forceinline__ void forward_token(const BwdSmem& s, int cc, int t, int i, int jl, float (&P)[CPL],
-                                              float (&M)[CPL]) {
-  const float at = s.a[t * DK + i], pt = s.p[t * DK + i], kt = s.k[t * DK + i];
-  const float a2 = at * at, k2 = kt * kt;
-#pragma unroll
-  for (int u4 = 0; u4 < CPL; u4 += 4) {
-    const float4 L4 = *reinterpret_cast<const float4*>(s.L + t * cc + jl + u4);
-    const float4 v4 = *reinterpret_cast<const float4*>(s.v + t * cc + jl + u4);
-    const float Ls[4] = {L4.x, L4.y, L4.z, L4.w}, vs[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int u = u4 + x;
-      const float Pp = fmaf(a2, P[u], pt);
-      const float w = rcp_approx(fmaf(k2 * Ls[x], Pp, 1.0f));
-      const float b = kt * (Ls[x] * vs[x]);
-      const float uu = fmaf(Pp, b, at * M[u]);
-      P[u] = w * Pp;
-      M[u] = w * uu;
-    }
-  }
-}
-
-// Lane geometry shared by the two sequence kernels.
+// Lane geometry of the reverse kernel.
 template <int DK, int CPL>
 struct BwdLane {
   int lane, i, jl;
@@ -166,59 +143,6 @@ struct BwdLane {
     e0 = (size_t)bh * DK * p.dv + (size_t)i * p.dv + jb + jl;
   }
 };
-
-template <int CPL>
-__device__ __forceinline__ void store_state(float* dst, size_t e0, long long elems, const float (&P)[CPL],
-                                            const float (&M)[CPL]) {
-#pragma unroll
-  for (int u = 0; u < CPL; u += 4) {
-    *reinterpret_cast<float4*>(dst + e0 + u) = make_float4(P[u], P[u + 1], P[u + 2], P[u + 3]);
-    *reinterpret_cast<float4*>(dst + elems + e0 + u) = make_float4(M[u], M[u + 1], M[u + 2], M[u + 3]);
-  }
-}
-
-template <int CPL>
-__device__ __forceinline__ void load_state(const float* src, size_t e0, long long elems, float (&P)[CPL],
-                                           float (&M)[CPL]) {
-#pragma unroll
-  for (int u = 0; u < CPL; u += 4) {
-    const float4 p4 = *reinterpret_cast<const float4*>(src + e0 + u);
-    const float4 m4 = *reinterpret_cast<const float4*>(src + elems + e0 + u);
-    P[u] = p4.x; P[u + 1] = p4.y; P[u + 2] = p4.z; P[u + 3] = p4.w;
-    M[u] = m4.x; M[u + 1] = m4.y; M[u + 2] = m4.z; M[u + 3] = m4.w;
-  }
-}
-
-// Pass 1: the forward, storing (P, μ) at every chunk start and at the end.
-template <typename IO, int DK, int CPL>
-__global__ void __launch_bounds__(512) kla_bwd_checkpoint_kernel(const BwdParams p) {
-  extern __shared__ __align__(16) float bwd_smem[];
-  const BwdSmem s(bwd_smem, DK, p.cc);
-  const long long bh = blockIdx.x;
-  const int jb = blockIdx.y * p.cc;
-  const BwdLane<DK, CPL> ln(p, bh, jb);
-  float P[CPL], M[CPL];
-#pragma unroll
-  for (int u = 0; u < CPL; ++u) {
-    if (p.lam0) {
-      P[u] = 1.0f / p.lam0[ln.e0 + u];
-      M[u] = p.eta0[ln.e0 + u] * P[u];
-    } else {
-      P[u] = 1.0f;
-      M[u] = 0.0f;
-    }
-  }
-  for (int c = 0; c < p.nchunks; ++c) {
-    store_state<CPL>(p.ckpt + (size_t)c * 2 * p.elems, ln.e0, p.elems, P, M);
-    const int t0 = c * kChunk, tl = min(kChunk, p.T - t0);
-    __syncthreads();  // the previous chunk's staged inputs are no longer read
-    stage_chunk<IO>(p, s, bh, jb, t0, tl, false);
-    __syncthreads();
-#pragma unroll 1
-    for (int t = 0; t < tl; ++t) forward_token<DK, CPL>(s, p.cc, t, ln.i, ln.jl, P, M);
-  }
-  store_state<CPL>(p.ckpt + (size_t)p.nchunks * 2 * p.elems, ln.e0, p.elems, P, M);
-}
 
 // Butterfly reduce-scatter of NV per-lane values over the RW lanes of a
 // column group (lanes differing in their low log2(RW) bits). While a lane
@@ -303,11 +227,43 @@ __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
     }
   };
 
+  // The checkpoints hold the forward scan's scaled variance P̃ = K·P with
+  // K = k² + 2^-40 of the token before (1 at the start).
+  auto inv_scale = [&](int t) -> f2 {
+    float K = 1.0f;
+    if (t > 0) {
+      const float kp = ld<IO>(p.k, ((size_t)bh * p.T + t - 1) * DK + i);
+      K = fmaf(kp, kp, kK2Floor);
+    }
+    const float r = 1.0f / K;
+    return f2_make(r, r);
+  };
+  auto load_state = [&](int idx, f2 rK, f2 (&P)[NP], f2 (&M)[NP]) {
+    load_pairs(p.ckpt + (size_t)idx * 2 * p.elems, P, M);
+#pragma unroll
+    for (int u = 0; u < NP; ++u) P[u] = f2_mul(P[u], rK);
+  };
+
   // terminal adjoints from dλ_T, dη_T through λ_T = 1/P_T, η_T = μ_T/P_T
   f2 Pb[NP], Mb[NP];
   {
     f2 PT[NP], MT[NP];
-    load_pairs(p.ckpt + (size_t)p.nchunks * 2 * p.elems, PT, MT);
+    if (p.nchunks > 0) {
+      load_state(p.nchunks, inv_scale(p.T), PT, MT);
+    } else {  // empty sequence: the final state is the initial one
+#pragma unroll
+      for (int u = 0; u < NP; ++u) {
+        float pv[2], mv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const size_t e = ln.e0 + 2 * u + h;
+          pv[h] = p.lam0 ? 1.0f / p.lam0[e] : 1.0f;
+          mv[h] = p.eta0 ? p.eta0[e] * pv[h] : 0.0f;
+        }
+        PT[u] = f2_make(pv[0], pv[1]);
+        MT[u] = f2_make(mv[0], mv[1]);
+      }
+    }
 #pragma unroll
     for (int u = 0; u < NP; ++u) {
       float pbv[2], mbv[2];
@@ -331,11 +287,11 @@ __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
     stage_chunk<IO>(p, s, bh, jb, t0, tl, true);
     for (int x = threadIdx.x; x < kChunk * (4 * DK + 2 * p.cc); x += blockDim.x) s.racc[x] = 0.0f;
     __syncthreads();
-    const float* ck = p.ckpt + (size_t)c * 2 * p.elems;
+    const f2 rK = inv_scale(t0);
     for (int sb = (tl - 1) / kSub; sb >= 0; --sb) {
       const int ts = sb * kSub;
       f2 P[NP], M[NP];
-      load_pairs(ck, P, M);
+      load_state(c, rK, P, M);
 #pragma unroll 1
       for (int t = 0; t < ts; ++t) fwd(t, P, M);
       f2* st = reinterpret_cast<f2*>(s.st) + threadIdx.x;
@@ -475,11 +431,9 @@ __global__ void kla_bwd_finish_kernel(const BwdParams p, size_t BHTdk) {
 
 template <typename IO, int DK, int CPL>
 cudaError_t launch_bwd_typed(const BwdParams& bp, dim3 grid, int threads, size_t smem, cudaStream_t s) {
-  auto ck = kla_bwd_checkpoint_kernel<IO, DK, CPL>;
   auto bw = kla_bwd_kernel<IO, DK, CPL>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(bw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = cudaFuncSetAttribute(bw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   const size_t BHTdk = (size_t)grid.x * bp.T * DK;
@@ -487,11 +441,8 @@ cudaError_t launch_bwd_typed(const BwdParams& bp, dim3 grid, int threads, size_t
     const cudaError_t e = cudaMemsetAsync(bp.rowpart, 0, BHTdk * 4 * sizeof(float), s);
     if (e != cudaSuccess) return e;
   }
-  ck<<<grid, threads, smem, s>>>(bp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   bw<<<grid, threads, smem, s>>>(bp);
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || bp.ncb == 1 || BHTdk == 0) return e;
   const unsigned blocks = (unsigned)std::min<size_t>((BHTdk + 255) / 256, 4096);
   kla_bwd_finish_kernel<IO><<<blocks, 256, 0, s>>>(bp, BHTdk);

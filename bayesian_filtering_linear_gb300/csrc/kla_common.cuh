@@ -67,8 +67,10 @@ struct KernelParams {
   const float *lam0, *eta0;
   const float* starts;  // [S][2][elems] chunk-start (P, μ), or nullptr
   float* maps;          // compose output [S-1][7][elems]
-  void* y;
+  void* y;              // nullptr: y is not stored (checkpoint pass of the backward)
   float *lamT, *etaT;
+  float* ckpt;          // scan only, or nullptr: [T/16 + 1][2][elems] scaled states (P̃, μ)
+                        // at every 16-token tile start and at the end
   int T, dv, chunk_len, cc, log2cc;
   long long elems;  // B·H·dk·dv
 };

@@ -47,7 +47,10 @@ size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 //   starts [S][2][B·H·dk·dv]    chunk-start (P, μ)
 size_t chunk_workspace_bytes(long long elems, int num_chunks);
 
-cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s);
+cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s,
+                           float* ckpt = nullptr);
+// The scan stores its checkpoints every kScanTile tokens.
+constexpr int kScanTile = 16;
 cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cudaStream_t s);
 cudaError_t launch_carry(const ForwardArgs& f, const Plan& p, const float* maps, float* starts,
                          cudaStream_t s);

@@ -221,8 +221,9 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
       if (n + 2 < ntiles) stage_raw<IO, DK, TC>(p, smem + L.raw(b), bh, jb, t_begin + (n + 2) * TC, tile_len(n + 2), ptid, pn);
       cp_async_commit();
       named_sync(kBarEmpty0 + b, nall);  // the scan of tile n is done with coef/pj[b] and ypart[b]
-      store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
-                                    ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
+      if (p.y)
+        store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
+                                      ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
       if (n + 2 < ntiles) {
         cp_async_wait<0>();
         named_sync(kBarProducers, pn);
@@ -259,9 +260,25 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
       Mu[r][c] = f2_make(M2[0], M2[1]);
     }
   }
+  // Checkpoints for the backward pass (sequential plan only): the scaled
+  // state (P̃ = K_{t-1}·P, μ) before every tile and after the last token.
+  auto checkpoint = [&](int idx) {
+    float* ck = p.ckpt + (size_t)idx * 2 * p.elems;
+#pragma unroll
+    for (int r = 0; r < NPR; ++r)
+#pragma unroll
+      for (int c = 0; c < CL; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const size_t e = (size_t)bh * E + (size_t)(i0 + 2 * r + h) * p.dv + jb + cl0 + (c ^ swz);
+          ck[e] = h ? f2_hi(Pt[r][c]) : f2_lo(Pt[r][c]);
+          ck[p.elems + e] = h ? f2_hi(Mu[r][c]) : f2_lo(Mu[r][c]);
+        }
+  };
   for (int n = 0; n < ntiles; ++n) {
     const int b = n & 1;
     const int tl = tile_len(n);
+    if (p.ckpt) checkpoint(n);
     named_sync(kBarFull0 + b, nall);  // coefficients of tile n are ready
     // ---- the scan over tile n ------------------------------------------------
     {
@@ -375,6 +392,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
     named_arrive(kBarEmpty0 + b, nall);
   }
 
+  if (p.ckpt) checkpoint(ntiles);
   // ---- final state of the last chunk: λ_T = K_last / P̃, η_T = μ λ_T ---------
   if (z == (int)gridDim.z - 1 && p.lamT) {
     const float* klast = reinterpret_cast<const float*>(smem + L.kprev(ntiles & 1));
@@ -463,9 +481,12 @@ size_t forward_smem_bytes(int dk, int rl, int io, int cc, int /*tile*/) {
   return io == IO_BF16 ? scan_smem_io<__nv_bfloat16>(dk, rl, cc) : scan_smem_io<float>(dk, rl, cc);
 }
 
-cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s) {
+static_assert(kTile == kScanTile, "checkpoints are taken once per tile");
+
+cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s, float* ckpt) {
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
+  kp.ckpt = ckpt;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
   const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, p.rows_per_lane) + kProducerWarps);
   const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile);
