@@ -1,7 +1,7 @@
 """Benchmark of the KLA scan (one JSON line).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kla|reference]
-                    [--workload headline|medium|long|tiny|decode]
+                    [--workload headline|medium|long|tiny|decode] [--pass forward|backward]
 
 By default a step is one kla_forward over the headline workload — B=8, H=16,
 T=4096, d_k=d_v=64, bf16 inputs/outputs, fp32 state — with inputs resident
@@ -14,6 +14,9 @@ d64 fp32 per step, state from a 1024-token prefix; HBM-bound). Under
 torchrun every rank runs its own independent batch (weak scaling; no
 collective on the data path) and rank 0 reports the whole-job throughput over
 the slowest rank's time.
+
+``--pass backward`` times kla_backward instead (gradients of every input for a
+random dL/dy and dL/dλ_T, dL/dη_T) on the same forward workloads.
 
 ``--impl reference`` times the fp64 CPU oracle (the stand-in reference arm,
 on this host's cores) on a bounded sample of the same workload.
@@ -47,6 +50,9 @@ DESCRIPTIONS = {
     "decode": "decode kla_step B256 H16 dk64 dv64 fp32, state from a 1024-token kla_forward prefix",
 }
 FLOPS_PER_ELEMENT_STEP = 13  # algorithmic count of the printed recursion
+# Backward: the checkpointing forward (13) plus the adjoint step as written in
+# kla_backward.cu with the forward quantities it needs recomputed (48).
+BWD_FLOPS_PER_ELEMENT_STEP = 13 + 48
 L2_FLUSH_BYTES = 256 << 20   # written between steps when a workload's inputs fit in L2
 TRAFFIC_FILES = {"headline": os.path.join(ROOT, "profiles", "traffic_headline.json")}
 KERNEL_SOURCES = [os.path.join(ROOT, "bayesian_filtering_linear_gb300", "csrc", f)
@@ -282,6 +288,8 @@ def run_kla(args, world, rank, local):
     names = ("q", "k", "v", "lam_v", "a", "pbar", "lam0", "eta0")
     if wname == "decode":
         return run_kla_decode(args, world, rank, local, w, x, stream)
+    if args.pass_ == "backward":
+        return run_kla_backward(args, world, rank, local, w, x, stream)
 
     plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io)
     ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev) if plan["workspace_bytes"] else None
@@ -443,6 +451,99 @@ def run_kla_decode(args, world, rank, local, w, x, stream):
     }), flush=True)
 
 
+def run_kla_backward(args, world, rank, local, w, x, stream):
+    """One kla_backward per step: gradients of every input for a fixed random
+    dL/dy and dL/dλ_T, dL/dη_T, inputs resident in HBM."""
+    import torch
+    from bayesian_filtering_linear_gb300 import kla
+    dev = x["q"].device
+    g = torch.Generator(device=dev)
+    g.manual_seed(7 + rank)
+    gy = torch.randn(w.B, w.H, w.T, w.dv, generator=g, device=dev).to(x["q"].dtype)
+    gl = torch.randn(w.B, w.H, w.dk, w.dv, generator=g, device=dev)
+    ge = torch.randn(w.B, w.H, w.dk, w.dv, generator=g, device=dev)
+    ws = torch.empty(max(16, kla.LIB.kla_backward_workspace_size(w.B, w.H, w.T, w.dk, w.dv)), dtype=torch.uint8,
+                     device=dev)
+    names = ("q", "k", "v", "lam_v", "a", "pbar", "lam0", "eta0")
+
+    def step():
+        kla.backward(*(x[n] for n in names), gy=gy, glamT=gl, getaT=ge, workspace=ws, stream=stream)
+
+    total_ms, per_launch_ms, clocks = timed_steps(step, args, world, local, stream)
+    ms_per_step = total_ms / args.steps
+    tokens = w.B * w.H * w.T
+    value = tokens * world / (ms_per_step * 1e-3)
+
+    host = {n: x[n].cpu().pin_memory() for n in names}
+    host_up = {"gy": gy.cpu().pin_memory(), "gl": gl.cpu().pin_memory(), "ge": ge.cpu().pin_memory()}
+    devb = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in list(host.items()) + list(host_up.items())}
+    sample = kla.backward(*(x[n] for n in names), gy=gy, glamT=gl, getaT=ge, workspace=ws, stream=stream)
+    out_h = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in sample.items()}
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_up.values()))
+    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+
+    def e2e_step():
+        for n, t in list(host.items()) + list(host_up.items()):
+            devb[n].copy_(t, non_blocking=True)
+        out = kla.backward(*(devb[n] for n in names), gy=devb["gy"], glamT=devb["gl"], getaT=devb["ge"],
+                           workspace=ws, stream=stream)
+        for n, t in out.items():
+            out_h[n].copy_(t, non_blocking=True)
+
+    e2e_ms = e2e_timing(e2e_step, args, world, stream)
+    if rank != 0:
+        return
+    ckpt_bytes = (-(-w.T // 16) + 1) * 2 * w.B * w.H * w.dk * w.dv * 4
+    peaks = measured_peaks()
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_tflops = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12
+    flops = BWD_FLOPS_PER_ELEMENT_STEP * tokens * w.dk * w.dv
+    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    cpu_value, cpu_desc = cpu_oracle_backward_sample(w, os.cpu_count() or 1)
+    print(json.dumps({
+        "metric": METRICS[w.name].replace("KLA scan tokens/s", "KLA backward tokens/s"), "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[w.name] + "; backward pass", "B": w.B, "H": w.H, "T": w.T, "dk": w.dk,
+                   "dv": w.dv, "io": w.io, "workspace_bytes": ws.numel(),
+                   "l2": "inputs larger than L2; no flush", "parallelism": f"{world} independent batches"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tflops, "traffic": None,
+                     "kernel": "kla_backward (checkpointing scan + kla_bwd_kernel)", "kernel_ms": per_launch_ms,
+                     "peak_basis": f"{nsm} SMs x 128 fp32 lanes x 2 flop x {sm_mhz:.0f} MHz (max SM clock)",
+                     "flops_per_launch": flops},
+        "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
+        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        # checkpointing scan + reverse kernel, + the row-sum pass when the
+        # workspace holds more than the checkpoints (columns split over blocks)
+        "gpu_launches": (2 + int(ws.numel() > ckpt_bytes)) * args.steps,
+        "clocks": clocks.summary(),
+    }), flush=True)
+
+
+def cpu_oracle_backward_sample(w, nthreads: int) -> tuple[float, dict]:
+    """The fp64 oracle's backward, as it stands, on 16 heads of the recipe
+    (up to 1024 tokens). Returns (tokens/s, description)."""
+    import numpy as np
+    import oracle
+    from bayesian_filtering_linear_gb300.inputs import make_inputs
+    heads, tokens = min(16, w.B * w.H), min(w.T, 1024)
+    x = make_inputs(1, heads, tokens, w.dk, w.dv, io=w.io, seed=w.seed, a_logit_mean=w.a_logit_mean)
+    gy = np.random.default_rng(0).standard_normal((1, heads, tokens, w.dv)).astype(np.float32)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.backward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"], gy,
+                    nthreads=nthreads, want_scales=False)
+    dt = time.perf_counter() - t0
+    used = min(nthreads, heads)
+    return heads * tokens / dt, {"kind": "oracle", "cores": used,
+                                 "sample": f"{heads} heads x {tokens} tokens of the {w.name} recipe, fp64 C++ "
+                                           f"reverse-mode loop, {used} threads"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,6 +551,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("kla", "reference"), default="kla")
     ap.add_argument("--workload", choices=tuple(METRICS), default="headline")
+    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward")
     args = ap.parse_args(argv)
     world, rank, local = dist_info()
     if world > 1:
