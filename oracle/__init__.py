@@ -56,7 +56,7 @@ def build(force: bool = False, mutant: int = 0) -> str:
 def _declare(lib):
     fp = ctypes.c_void_p
     lib.kla_oracle_forward_f64.restype = ctypes.c_longlong
-    lib.kla_oracle_forward_f64.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 5 + [ctypes.c_int]
+    lib.kla_oracle_forward_f64.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 6 + [ctypes.c_int]
     lib.kla_oracle_forward_f32.restype = ctypes.c_longlong
     lib.kla_oracle_forward_f32.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 3 + [ctypes.c_int]
     lib.kla_oracle_forward_f64in.restype = ctypes.c_longlong
@@ -102,7 +102,7 @@ def _ptr(a):
 
 
 def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, precision: str = "f64",
-            nthreads: int | None = None, heads=None, want_scales: bool = True,
+            nthreads: int | None = None, heads=None, want_scales: bool = True, want_var: bool = False,
             _mutant: int = 0) -> dict:
     """Run the oracle over every head (or the flat head indices in ``heads``).
 
@@ -112,6 +112,8 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, precision: str = "
     arrays have that leading shape.
 
     Returns a dict with ``y [B,H,T,dv]``, ``lamT``, ``etaT`` ``[B,H,dk,dv]``,
+    (fp64, with ``want_var``) ``y_var [B,H,T,dv]`` = Σ_i q_i² P (all terms ≥ 0,
+    so it is its own condition scale),
     (fp64 only) the condition scales ``y_scale`` and ``eta_scale``, and
     ``violations`` — the count of invariant violations (0 expected).
     """
@@ -147,11 +149,14 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, precision: str = "
     if precision == "f64":
         ys = np.empty((B, H, T, dv), np.float64) if want_scales else None
         es = np.empty((B, H, dk, dv), np.float64) if want_scales else None
+        yv = np.empty((B, H, T, dv), np.float64) if want_var else None
         nv = lib.kla_oracle_forward_f64(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0),
                                         B, H, T, dk, dv, _ptr(y), _ptr(lamT), _ptr(etaT),
-                                        _ptr(ys), _ptr(es), int(nthreads))
+                                        _ptr(ys), _ptr(es), _ptr(yv), int(nthreads))
         if want_scales:
             out["y_scale"], out["eta_scale"] = ys, es
+        if want_var:
+            out["y_var"] = yv
     elif precision == "f32":
         nv = lib.kla_oracle_forward_f32(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0),
                                         B, H, T, dk, dv, _ptr(y), _ptr(lamT), _ptr(etaT),

@@ -19,6 +19,10 @@
 //     P      = 1 / (1/P_pred + k_{t,i}² · Λ^v_{t,j})          (observation of
 //     μ      = P · (μ_pred/P_pred + k_{t,i} · Λ^v_{t,j} · v_{t,j})   v_{t,j} through k_{t,i})
 //     y[t,j] += q_{t,i} · μ            (summed over i in increasing order)
+//     y_var[t,j] += q_{t,i}² · P       (optional: the readout's variance under
+//                                       the posterior, the layer's explicit
+//                                       belief uncertainty, Belangrijkste
+//                                       Bijdragen item 3)
 //
 // and at the end λ_T = 1/P, η_T = μ/P (information form). The readout uses the
 // posterior that already includes token t.
@@ -61,6 +65,7 @@ struct Args {
   const In *q, *k, *v, *lam_v, *a, *pbar, *lam0, *eta0;
   int B, H, T, dk, dv;
   R *y, *lamT, *etaT, *y_scale, *eta_scale;
+  R* y_var = nullptr;  // Σ_i q_i² P (the readout's variance), or NULL
 };
 
 template <typename R, typename In>
@@ -76,11 +81,11 @@ long long run_head(const Args<R, In>& g, long long bh) {
     muabs[e] = std::fabs(mu[e]);
   }
   long long violations = 0;
-  std::vector<R> yacc(dv), ysc(dv);
+  std::vector<R> yacc(dv), ysc(dv), yvar(dv);
   for (int t = 0; t < T; ++t) {
     const size_t ri = ((size_t)bh * T + t) * dk;  // row of the per-i inputs
     const size_t rj = ((size_t)bh * T + t) * dv;  // row of the per-j inputs
-    for (int j = 0; j < dv; ++j) { yacc[j] = 0; ysc[j] = 0; }
+    for (int j = 0; j < dv; ++j) { yacc[j] = 0; ysc[j] = 0; yvar[j] = 0; }
     for (int i = 0; i < dk; ++i) {
       const R ai = g.a[ri + i], pi = g.pbar[ri + i], ki = g.k[ri + i], qi = g.q[ri + i];
       for (int j = 0; j < dv; ++j) {
@@ -102,6 +107,7 @@ long long run_head(const Args<R, In>& g, long long bh) {
         P[e] = Pn;
         mu[e] = mun;
         yacc[j] += qi * readout;
+        yvar[j] += qi * qi * (KLA_ORACLE_MUTANT == 10 ? Ppred : Pn);  // 10: prior variance read out
         ysc[j] += std::fabs(qi) * muabs[e];
         const R lam = (R)1 / Pn;
         if (!(lam > 0)) ++violations;
@@ -114,6 +120,7 @@ long long run_head(const Args<R, In>& g, long long bh) {
     for (int j = 0; j < dv; ++j) {
       if (g.y) g.y[rj + j] = yacc[j];
       if (g.y_scale) g.y_scale[rj + j] = ysc[j];
+      if (g.y_var) g.y_var[rj + j] = yvar[j];
     }
   }
   for (size_t e = 0; e < E; ++e) {
@@ -314,10 +321,10 @@ long long kla_oracle_forward_f64(const float* q, const float* k, const float* v,
                                  const float* lam0, const float* eta0,
                                  int B, int H, int T, int dk, int dv,
                                  double* y, double* lamT, double* etaT,
-                                 double* y_scale, double* eta_scale, int nthreads) {
+                                 double* y_scale, double* eta_scale, double* y_var, int nthreads) {
   if (!q || !k || !v || !lam_v || !a || !pbar || B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
     return -1;
-  Args<double> g{q, k, v, lam_v, a, pbar, lam0, eta0, B, H, T, dk, dv, y, lamT, etaT, y_scale, eta_scale};
+  Args<double> g{q, k, v, lam_v, a, pbar, lam0, eta0, B, H, T, dk, dv, y, lamT, etaT, y_scale, eta_scale, y_var};
   return run_all<double>(g, nthreads);
 }
 
