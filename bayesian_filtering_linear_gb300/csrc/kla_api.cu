@@ -222,6 +222,68 @@ void fill_info(const Plan& p, kla_plan_info* out) {
   out->rows_per_lane = p.rows_per_lane;
 }
 
+
+// kla_forward, and with y_var the variance readout of kla_forward_uncertainty.
+kla_status forward_impl(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                       const void* pbar, const float* lam0, const float* eta0, void* y, float* lamT,
+                       float* etaT, int B, int H, int T, int dk, int dv, kla_dtype io, void* workspace,
+                       size_t ws_bytes, const kla_options* opt, void* stream, void* y_var) {
+  // ---- validation: no CUDA call before it passes ---------------------------
+  kla_status st = check_shape(B, H, T, dk, dv);
+  if (st != KLA_OK) return st;
+  if ((st = check_options(opt, dk)) != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  const long long tokens = bh * T;
+  if ((lam0 == nullptr) != (eta0 == nullptr)) return KLA_ERR_INVALID_ARG;
+  if ((lamT == nullptr) != (etaT == nullptr)) return KLA_ERR_INVALID_ARG;
+  if (tokens > 0 && (!q || !k || !v || !lam_v || !a || !pbar || !y)) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, y_var};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  const size_t state_bytes = (size_t)bh * dk * dv * sizeof(float);
+  if (overlaps_partially(lamT, lam0, state_bytes) || overlaps_partially(etaT, eta0, state_bytes) ||
+      overlaps_partially(lamT, eta0, state_bytes) || overlaps_partially(etaT, lam0, state_bytes) ||
+      (lamT && lamT == (const float*)eta0) || (etaT && etaT == (const float*)lam0))
+    return KLA_ERR_INVALID_ARG;
+  if (lamT && overlaps_partially(lamT, etaT, state_bytes)) return KLA_ERR_INVALID_ARG;
+  if (lamT && lamT == etaT) return KLA_ERR_INVALID_ARG;
+  if (y_var && (y_var == y || overlaps_partially(y_var, y, (size_t)tokens * dv * (io == KLA_BF16 ? 2 : 4))))
+    return KLA_ERR_INVALID_ARG;
+  if (bh == 0) return KLA_OK;
+
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  Plan p{};
+  if ((st = make_plan(B, H, T, dk, dv, io, opt, sms, &p)) != KLA_OK) return st;
+  if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return KLA_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return KLA_ERR_MISALIGNED;
+
+  kla::ForwardArgs f{q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, (int)io};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // The variance readout (when asked for) runs before the main pass, which
+  // may overwrite λ0/η0 in place.
+  kla::ForwardArgs fv = f;
+  fv.y = y_var;
+  fv.lamT = fv.etaT = nullptr;
+  if (T == 0) {
+    e = kla::launch_init_state(f, s);
+  } else if (p.strategy == KLA_SEQUENTIAL) {
+    e = y_var ? kla::launch_forward(fv, p, nullptr, s, nullptr, true) : cudaSuccess;
+    if (e == cudaSuccess) e = kla::launch_forward(f, p, nullptr, s);
+  } else {
+    const long long elems = bh * dk * dv;
+    float* maps = reinterpret_cast<float*>(workspace);
+    float* starts = maps + (size_t)7 * (p.num_chunks - 1) * elems;
+    e = kla::launch_compose(f, p, maps, s);
+    if (e == cudaSuccess) e = kla::launch_carry(f, p, maps, starts, s);
+    if (e == cudaSuccess && y_var) e = kla::launch_forward(fv, p, starts, s, nullptr, true);
+    if (e == cudaSuccess) e = kla::launch_forward(f, p, starts, s);
+  }
+  return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -280,51 +342,17 @@ kla_status kla_forward(const void* q, const void* k, const void* v, const void* 
                        const void* pbar, const float* lam0, const float* eta0, void* y, float* lamT,
                        float* etaT, int B, int H, int T, int dk, int dv, kla_dtype io, void* workspace,
                        size_t ws_bytes, const kla_options* opt, void* stream) {
-  // ---- validation: no CUDA call before it passes ---------------------------
-  kla_status st = check_shape(B, H, T, dk, dv);
-  if (st != KLA_OK) return st;
-  if ((st = check_options(opt, dk)) != KLA_OK) return st;
-  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
-  const long long bh = (long long)B * H;
-  const long long tokens = bh * T;
-  if ((lam0 == nullptr) != (eta0 == nullptr)) return KLA_ERR_INVALID_ARG;
-  if ((lamT == nullptr) != (etaT == nullptr)) return KLA_ERR_INVALID_ARG;
-  if (tokens > 0 && (!q || !k || !v || !lam_v || !a || !pbar || !y)) return KLA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT};
-  for (const void* ptr : ptrs)
-    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
-  const size_t state_bytes = (size_t)bh * dk * dv * sizeof(float);
-  if (overlaps_partially(lamT, lam0, state_bytes) || overlaps_partially(etaT, eta0, state_bytes) ||
-      overlaps_partially(lamT, eta0, state_bytes) || overlaps_partially(etaT, lam0, state_bytes) ||
-      (lamT && lamT == (const float*)eta0) || (etaT && etaT == (const float*)lam0))
-    return KLA_ERR_INVALID_ARG;
-  if (lamT && overlaps_partially(lamT, etaT, state_bytes)) return KLA_ERR_INVALID_ARG;
-  if (lamT && lamT == etaT) return KLA_ERR_INVALID_ARG;
-  if (bh == 0) return KLA_OK;
+  return forward_impl(q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, io, workspace,
+                      ws_bytes, opt, stream, nullptr);
+}
 
-  int sms = 0;
-  if ((st = device_sms(&sms)) != KLA_OK) return st;
-  Plan p{};
-  if ((st = make_plan(B, H, T, dk, dv, io, opt, sms, &p)) != KLA_OK) return st;
-  if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return KLA_ERR_WORKSPACE;
-  if (workspace && !aligned16(workspace)) return KLA_ERR_MISALIGNED;
-
-  kla::ForwardArgs f{q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, (int)io};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (T == 0) {
-    e = kla::launch_init_state(f, s);
-  } else if (p.strategy == KLA_SEQUENTIAL) {
-    e = kla::launch_forward(f, p, nullptr, s);
-  } else {
-    const long long elems = bh * dk * dv;
-    float* maps = reinterpret_cast<float*>(workspace);
-    float* starts = maps + (size_t)7 * (p.num_chunks - 1) * elems;
-    e = kla::launch_compose(f, p, maps, s);
-    if (e == cudaSuccess) e = kla::launch_carry(f, p, maps, starts, s);
-    if (e == cudaSuccess) e = kla::launch_forward(f, p, starts, s);
-  }
-  return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+kla_status kla_forward_uncertainty(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                                   const void* pbar, const float* lam0, const float* eta0, void* y, void* y_var,
+                                   float* lamT, float* etaT, int B, int H, int T, int dk, int dv, kla_dtype io,
+                                   void* workspace, size_t ws_bytes, const kla_options* opt, void* stream) {
+  if ((long long)B * H * T > 0 && !y_var) return KLA_ERR_INVALID_ARG;
+  return forward_impl(q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, io, workspace,
+                      ws_bytes, opt, stream, y_var);
 }
 
 kla_status kla_step(const void* q, const void* k, const void* v, const void* lam_v, const void* a,

@@ -47,8 +47,10 @@ size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 //   starts [S][2][B·H·dk·dv]    chunk-start (P, μ)
 size_t chunk_workspace_bytes(long long elems, int num_chunks);
 
+// ckpt: also store the backward's checkpoints; variance: read out
+// y_var = Σ_i q_i² P_t (into f.y) instead of y, skipping the mean.
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s,
-                           float* ckpt = nullptr);
+                           float* ckpt = nullptr, bool variance = false);
 // The scan stores its checkpoints every kScanTile tokens.
 constexpr int kScanTile = 16;
 cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cudaStream_t s);

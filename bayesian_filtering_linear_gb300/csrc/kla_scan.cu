@@ -84,9 +84,10 @@ struct ScanLayout {
 };
 
 // Per-(t, i) row coefficients of a staged tile, four rows per thread:
-// coef[t][0..4][i] = (A, B, 1/a, k/K, q). kp_cur holds K of the row before
-// the tile (1 at a chunk start); K of the tile's last row goes to kp_nxt.
-template <typename IO, int DK, int TC>
+// coef[t][0..4][i] = (A, B, 1/a, k/K, q), or with VAR (the variance readout)
+// the last one is q²/K. kp_cur holds K of the row before the tile (1 at a
+// chunk start); K of the tile's last row goes to kp_nxt.
+template <typename IO, int DK, int TC, bool VAR = false>
 __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float* coef, const float* kp_cur,
                                                  float* kp_nxt, int tl, int tid, int nthr) {
   using R = RawTile<IO, DK, TC>;
@@ -108,7 +109,8 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
     }
     const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
     const float pv[4] = {p4.x, p4.y, p4.z, p4.w}, kpv[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
-    float A[4], B[4], AI[4], KI[4], Kt[4];
+    const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+    float A[4], B[4], AI[4], KI[4], Kt[4], QV[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const float at = fmaxf(av[u], kAMin);
@@ -118,14 +120,16 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
       AI[u] = (Kt[u] * kpv[u]) * r;             // 1/a
       A[u] = aK * (aK * r);                     // K_t a / K_{t-1}
       B[u] = (Kt[u] * pv[u]) * AI[u];           // K_t p̄ / a
-      KI[u] = kv[u] * (at * kpv[u] * r);        // k / K_t
+      const float rK = at * kpv[u] * r;         // 1 / K_t
+      KI[u] = kv[u] * rK;                       // k / K_t
+      QV[u] = VAR ? qv[u] * qv[u] * rK : qv[u];  // q²/K_t (variance readout) or q
     }
     float* ct = coef + t * 5 * DK + i;
     *reinterpret_cast<float4*>(ct + 0 * DK) = make_float4(A[0], A[1], A[2], A[3]);
     *reinterpret_cast<float4*>(ct + 1 * DK) = make_float4(B[0], B[1], B[2], B[3]);
     *reinterpret_cast<float4*>(ct + 2 * DK) = make_float4(AI[0], AI[1], AI[2], AI[3]);
     *reinterpret_cast<float4*>(ct + 3 * DK) = make_float4(KI[0], KI[1], KI[2], KI[3]);
-    *reinterpret_cast<float4*>(ct + 4 * DK) = q4;
+    *reinterpret_cast<float4*>(ct + 4 * DK) = make_float4(QV[0], QV[1], QV[2], QV[3]);
     if (t == tl - 1) *reinterpret_cast<float4*>(kp_nxt + i) = make_float4(Kt[0], Kt[1], Kt[2], Kt[3]);
   }
 }
@@ -155,7 +159,9 @@ __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, in
   }
 }
 
-template <typename IO, int DK, int RL, int TC>
+// VAR: the variance readout y_var[t, j] = Σ_i q_i² P_t[i, j] instead of y (the
+// mean recursion is skipped; y points at y_var).
+template <typename IO, int DK, int RL, int TC, bool VAR = false>
 __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_kernel(const KernelParams p) {
   using G = Geo<DK, RL>;
   constexpr int NPR = RL / 2;  // row pairs per lane
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
     for (int i = ptid; i < DK; i += pn) kp0[i] = 1.0f;
     auto build = [&](int m) {  // coefficients of tile m into buffer m % 2
       const int bm = m & 1;
-      row_coefficients<IO, DK, TC>(smem + L.raw(bm), reinterpret_cast<float*>(smem + L.coef(bm)),
+      row_coefficients<IO, DK, TC, VAR>(smem + L.raw(bm), reinterpret_cast<float*>(smem + L.coef(bm)),
                                    reinterpret_cast<const float*>(smem + L.kprev(bm)),
                                    reinterpret_cast<float*>(smem + L.kprev(bm ^ 1)), tile_len(m), ptid, pn);
       column_terms<IO, DK, TC>(smem + L.raw(bm), reinterpret_cast<float4*>(smem + L.pj(bm)), p.cc, tile_len(m),
@@ -334,10 +340,14 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
             const f2 d = f2_fma(s, L2[c], AI[r]);
             const f2 w = f2_rcp(d);
             Pt[r][c] = f2_mul(s, w);
-            const f2 g = f2_mul(s, V2[c]);
-            const f2 m = f2_fma(g, KI[r], Mu[r][c]);
-            Mu[r][c] = f2_mul(m, w);
-            y2 = f2_fma(Q[r], Mu[r][c], y2);
+            if constexpr (VAR) {
+              y2 = f2_fma(Q[r], Pt[r][c], y2);  // (q²/K)·P̃ = q²·P
+            } else {
+              const f2 g = f2_mul(s, V2[c]);
+              const f2 m = f2_fma(g, KI[r], Mu[r][c]);
+              Mu[r][c] = f2_mul(m, w);
+              y2 = f2_fma(Q[r], Mu[r][c], y2);
+            }
           }
           yc[c] = f2_lo(y2) + f2_hi(y2);
         }
@@ -462,18 +472,24 @@ size_t scan_smem_io(int dk, int rl, int cc) {
     default: return 0;
   }
 }
-template <typename IO>
-cudaError_t scan_dispatch(int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
-                          const KernelParams& kp) {
+template <typename IO, bool VAR>
+cudaError_t scan_dispatch_v(int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                            const KernelParams& kp) {
   switch (dk * 16 + rl) {
-    case 16 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 16, 4, kTile>, grid, threads, smem, s, kp);
-    case 32 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 32, 4, kTile>, grid, threads, smem, s, kp);
-    case 64 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 64, 4, kTile>, grid, threads, smem, s, kp);
-    case 64 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 64, 8, kTile>, grid, threads, smem, s, kp);
-    case 128 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 128, 4, kTile>, grid, threads, smem, s, kp);
-    case 128 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 128, 8, kTile>, grid, threads, smem, s, kp);
+    case 16 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 16, 4, kTile, VAR>, grid, threads, smem, s, kp);
+    case 32 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 32, 4, kTile, VAR>, grid, threads, smem, s, kp);
+    case 64 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 64, 4, kTile, VAR>, grid, threads, smem, s, kp);
+    case 64 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 64, 8, kTile, VAR>, grid, threads, smem, s, kp);
+    case 128 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 128, 4, kTile, VAR>, grid, threads, smem, s, kp);
+    case 128 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 128, 8, kTile, VAR>, grid, threads, smem, s, kp);
     default: return cudaErrorInvalidValue;
   }
+}
+template <typename IO>
+cudaError_t scan_dispatch(int dk, int rl, bool var, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                          const KernelParams& kp) {
+  return var ? scan_dispatch_v<IO, true>(dk, rl, grid, threads, smem, s, kp)
+             : scan_dispatch_v<IO, false>(dk, rl, grid, threads, smem, s, kp);
 }
 }  // namespace
 
@@ -483,15 +499,16 @@ size_t forward_smem_bytes(int dk, int rl, int io, int cc, int /*tile*/) {
 
 static_assert(kTile == kScanTile, "checkpoints are taken once per tile");
 
-cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s, float* ckpt) {
+cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s, float* ckpt,
+                           bool variance) {
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
   kp.ckpt = ckpt;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
   const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, p.rows_per_lane) + kProducerWarps);
   const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile);
-  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, p.rows_per_lane, grid, threads, smem, s, kp)
-                         : scan_dispatch<float>(f.dk, p.rows_per_lane, grid, threads, smem, s, kp);
+  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, p.rows_per_lane, variance, grid, threads, smem, s, kp)
+                         : scan_dispatch<float>(f.dk, p.rows_per_lane, variance, grid, threads, smem, s, kp);
 }
 
 }  // namespace kla

@@ -24,7 +24,7 @@ _IO = {torch.float32: F32, torch.bfloat16: BF16}
 # Every function the header declares, for the export check.
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
            "kla_status_string", "kla_version", "kla_forward_chunked_noalloc", "kla_backward_workspace_size",
-           "kla_backward")
+           "kla_backward", "kla_forward_uncertainty")
 
 
 class Options(ctypes.Structure):
@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH):
     lib.kla_forward.argtypes = [vp] * 11 + [i] * 6 + [vp, sz, ctypes.POINTER(Options), vp]
     lib.kla_step.restype = i
     lib.kla_step.argtypes = [vp] * 9 + [i] * 5 + [vp]
+    lib.kla_forward_uncertainty.restype = i
+    lib.kla_forward_uncertainty.argtypes = [vp] * 12 + [i] * 6 + [vp, sz, ctypes.POINTER(Options), vp]
     lib.kla_backward_workspace_size.restype = sz
     lib.kla_backward_workspace_size.argtypes = [i] * 5
     lib.kla_backward.restype = i
@@ -130,9 +132,11 @@ def _need(t, name, dtype, shape, device):
 
 def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None, etaT=None,
             strategy: str | int = "auto", chunk_len: int = 0, workspace=None, stream=None,
-            final_state: bool = True, rows_per_lane: int = 0):
+            final_state: bool = True, rows_per_lane: int = 0, uncertainty: bool = False, y_var=None):
     """Whole-sequence KLA scan. Returns ``(y, lamT, etaT)`` (the last two are
-    None when ``final_state`` is False and none were given)."""
+    None when ``final_state`` is False and none were given); with
+    ``uncertainty`` (or a ``y_var`` buffer) also the variance readout
+    ``y_var[t, j] = Σ_i q_i² / λ_{t,i,j}`` as a fourth element."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -163,6 +167,17 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
             nbytes = int(info.workspace_bytes)
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        if uncertainty or y_var is not None:
+            if y_var is None:
+                y_var = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+            else:
+                _need(y_var, "y_var", dt, (B, H, T, dv), dev)
+            st = LIB.kla_forward_uncertainty(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam0),
+                                             _ptr(eta0), _ptr(y), _ptr(y_var), _ptr(lamT), _ptr(etaT), B, H, T, dk,
+                                             dv, _IO[dt], _ptr(workspace), ws_bytes, ctypes.byref(opt),
+                                             _stream(stream))
+            _check(st, "kla_forward_uncertainty")
+            return y, lamT, etaT, y_var
         st = LIB.kla_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam0), _ptr(eta0),
                              _ptr(y), _ptr(lamT), _ptr(etaT), B, H, T, dk, dv, _IO[dt],
                              _ptr(workspace), ws_bytes, ctypes.byref(opt), _stream(stream))

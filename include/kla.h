@@ -115,6 +115,22 @@ kla_status kla_forward(const void* q, const void* k, const void* v, const void* 
                        int B, int H, int T, int dk, int dv, kla_dtype io,
                        void* workspace, size_t ws_bytes, const kla_options* opt, void* stream);
 
+/* kla_forward plus the belief uncertainty of every readout: the variance of
+ * y under the filter's posterior, y_var[t,j] = Σ_i q_{t,i}² P_{t,i,j} with
+ * P = 1/λ (each element's posterior variance after token t). The summary
+ * states that the layer carries an explicit belief-state uncertainty
+ * (Belangrijkste Bijdragen item 3; "Expliciete Onzekerheid" under the
+ * results); this readout exposes it per token. Arguments as for kla_forward, plus
+ *   y_var [B,H,T,dv] in `io` (output; required unless B·H·T = 0; must not
+ *   overlap y). It costs one more scan pass without the mean (about 0.7×
+ *   the forward); it runs before the main pass, so in-place λ0/η0 → λ_T/η_T
+ *   updates stay correct. */
+kla_status kla_forward_uncertainty(const void* q, const void* k, const void* v, const void* lam_v,
+                                   const void* a, const void* pbar, const float* lam0, const float* eta0,
+                                   void* y, void* y_var, float* lamT, float* etaT,
+                                   int B, int H, int T, int dk, int dv, kla_dtype io,
+                                   void* workspace, size_t ws_bytes, const kla_options* opt, void* stream);
+
 /* One recurrent decode step, identical in meaning to kla_forward with T = 1
  * and the state updated in place (same summary, same sections).
  *   q, k, a, pbar [B,H,dk] and v, lam_v [B,H,dv] in `io` (one token)

@@ -205,3 +205,14 @@ def test_backward_without_a_device_reports_cuda_error():
     assert L.kla_backward_workspace_size(1, 1, 8, 16, 16) == ctypes.c_size_t(-1).value
     assert L.kla_backward_workspace_size(0, 4, 8, 16, 16) == 0
     assert L.kla_backward_workspace_size(1, 1, 8, 20, 16) == ctypes.c_size_t(-1).value
+
+
+def test_forward_uncertainty_validation_before_any_cuda_call():
+    def fu(y_var=P, y=ctypes.c_void_p(0x30000), **kw):
+        g = lambda n: kw.get(n, P)
+        return L.kla_forward_uncertainty(g("q"), g("k"), g("v"), g("lam_v"), g("a"), g("pbar"), None, None, y,
+                                         y_var, None, None, 1, 1, 8, 16, 16, kla.F32, None, 0, None, None)
+    assert fu(y_var=None) == kla.ERR_INVALID_ARG
+    assert fu(y_var=ctypes.c_void_p(0x30000)) == kla.ERR_INVALID_ARG        # same buffer as y
+    assert fu(y_var=ctypes.c_void_p(0x30000 + 64)) == kla.ERR_INVALID_ARG   # overlaps y (8x16 fp32 = 512 B)
+    assert fu(y_var=MIS) == kla.ERR_MISALIGNED
