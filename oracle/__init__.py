@@ -60,7 +60,7 @@ def _declare(lib):
     lib.kla_oracle_forward_f32.restype = ctypes.c_longlong
     lib.kla_oracle_forward_f32.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 3 + [ctypes.c_int]
     lib.kla_oracle_forward_f64in.restype = ctypes.c_longlong
-    lib.kla_oracle_forward_f64in.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 3 + [ctypes.c_int]
+    lib.kla_oracle_forward_f64in.argtypes = [fp] * 8 + [ctypes.c_int] * 5 + [fp] * 5 + [ctypes.c_int]
     for name in ("kla_oracle_backward_f64", "kla_oracle_backward_f64in"):
         f = getattr(lib, name)
         f.restype = ctypes.c_longlong
@@ -191,20 +191,27 @@ def _shapes(arrs):
 
 
 def forward64(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, nthreads: int | None = None,
-              _mutant: int = 0) -> dict:
+              want_scales: bool = False, _mutant: int = 0) -> dict:
     """The fp64 loop of :func:`forward` on fp64 inputs (no rounding of the
-    inputs to float32). Returns ``y``, ``lamT``, ``etaT``."""
+    inputs to float32). Returns ``y``, ``lamT``, ``etaT`` (and with
+    ``want_scales`` the condition scales ``y_scale``, ``eta_scale``)."""
     arrs = [_f64(x) for x in (q, k, v, lam_v, a, pbar)]
     l0, e0 = _f64(lam0), _f64(eta0)
     B, H, T, dk, dv = _shapes(arrs)
     y = np.empty((B, H, T, dv))
     lamT = np.empty((B, H, dk, dv))
     etaT = np.empty((B, H, dk, dv))
+    ys = np.empty((B, H, T, dv)) if want_scales else None
+    es = np.empty((B, H, dk, dv)) if want_scales else None
     nv = _load(_mutant).kla_oracle_forward_f64in(*[_ptr(x) for x in arrs], _ptr(l0), _ptr(e0), B, H, T, dk, dv,
-                                                 _ptr(y), _ptr(lamT), _ptr(etaT), int(nthreads or os.cpu_count() or 1))
+                                                 _ptr(y), _ptr(lamT), _ptr(etaT), _ptr(ys), _ptr(es),
+                                                 int(nthreads or os.cpu_count() or 1))
     if nv < 0:
         raise ValueError("oracle rejected its arguments")
-    return {"y": y, "lamT": lamT, "etaT": etaT}
+    out = {"y": y, "lamT": lamT, "etaT": etaT}
+    if want_scales:
+        out["y_scale"], out["eta_scale"] = ys, es
+    return out
 
 
 GRAD_NAMES = ("dq", "dk", "da", "dpbar", "dv", "dlam_v", "dlam0", "deta0")

@@ -345,10 +345,11 @@ long long kla_oracle_forward_f64in(const double* q, const double* k, const doubl
                                    const double* lam_v, const double* a, const double* pbar,
                                    const double* lam0, const double* eta0,
                                    int B, int H, int T, int dk, int dv,
-                                   double* y, double* lamT, double* etaT, int nthreads) {
+                                   double* y, double* lamT, double* etaT, double* y_scale, double* eta_scale,
+                                   int nthreads) {
   if (!q || !k || !v || !lam_v || !a || !pbar || B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0)
     return -1;
-  Args<double, double> g{q, k, v, lam_v, a, pbar, lam0, eta0, B, H, T, dk, dv, y, lamT, etaT, nullptr, nullptr};
+  Args<double, double> g{q, k, v, lam_v, a, pbar, lam0, eta0, B, H, T, dk, dv, y, lamT, etaT, y_scale, eta_scale};
   return run_all<double, double>(g, nthreads);
 }
 
