@@ -37,8 +37,13 @@ kla_status check_shape(int B, int H, int T, int dk, int dv) {
 }
 
 // Options for a head of dk rows (dk already checked).
+bool valid_gates(int g) {
+  return (g & ~15) == 0 && !((g & KLA_GATE_PBAR_SOFTPLUS) && (g & KLA_GATE_PBAR_OU));
+}
+
 kla_status check_options(const kla_options* opt, int dk) {
   if (!opt) return KLA_OK;
+  if (!valid_gates(opt->gates)) return KLA_ERR_INVALID_ARG;
   if (opt->strategy < KLA_AUTO || opt->strategy > KLA_CHUNKED) return KLA_ERR_INVALID_ARG;
   if (opt->chunk_len < 0 || opt->chunk_len % kChunkAlign != 0) return KLA_ERR_INVALID_ARG;
   if (opt->rows_per_lane != 0) {  // must be a geometry the scan kernel is built for
@@ -259,7 +264,8 @@ kla_status forward_impl(const void* q, const void* k, const void* v, const void*
   if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return KLA_ERR_WORKSPACE;
   if (workspace && !aligned16(workspace)) return KLA_ERR_MISALIGNED;
 
-  kla::ForwardArgs f{q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, (int)io};
+  kla::ForwardArgs f{q, k, v, lam_v, a, pbar, lam0, eta0, y, lamT, etaT, B, H, T, dk, dv, (int)io,
+                     opt ? opt->gates : 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   // The variance readout (when asked for) runs before the main pass, which
@@ -355,12 +361,13 @@ kla_status kla_forward_uncertainty(const void* q, const void* k, const void* v, 
                       ws_bytes, opt, stream, y_var);
 }
 
-kla_status kla_step(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
-                    const void* pbar, float* lam, float* eta, void* y, int B, int H, int dk, int dv, kla_dtype io,
-                    void* stream) {
+kla_status kla_step_gated(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                          const void* pbar, float* lam, float* eta, void* y, int B, int H, int dk, int dv,
+                          kla_dtype io, int gates, void* stream) {
   kla_status st = check_shape(B, H, 1, dk, dv);
   if (st != KLA_OK) return st;
   if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  if (!valid_gates(gates)) return KLA_ERR_INVALID_ARG;
   const long long bh = (long long)B * H;
   if (bh > 0 && (!q || !k || !v || !lam_v || !a || !pbar || !lam || !eta || !y)) return KLA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, lam_v, a, pbar, lam, eta, y};
@@ -369,9 +376,15 @@ kla_status kla_step(const void* q, const void* k, const void* v, const void* lam
   const size_t state_bytes = (size_t)bh * dk * dv * sizeof(float);
   if (lam && (lam == eta || overlaps_partially(lam, eta, state_bytes))) return KLA_ERR_INVALID_ARG;
   if (bh == 0) return KLA_OK;
-  kla::StepArgs sa{q, k, v, lam_v, a, pbar, lam, eta, y, B, H, dk, dv, (int)io};
+  kla::StepArgs sa{q, k, v, lam_v, a, pbar, lam, eta, y, B, H, dk, dv, (int)io, gates};
   const cudaError_t e = kla::launch_step(sa, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_step(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                    const void* pbar, float* lam, float* eta, void* y, int B, int H, int dk, int dv, kla_dtype io,
+                    void* stream) {
+  return kla_step_gated(q, k, v, lam_v, a, pbar, lam, eta, y, B, H, dk, dv, io, 0, stream);
 }
 
 size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv) {
@@ -388,11 +401,12 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
                         const void* pbar, const float* lam0, const float* eta0, const void* gy,
                         const float* glamT, const float* getaT, void* gq, void* gk, void* gv, void* glam_v,
                         void* ga, void* gpbar, float* glam0, float* geta0, int B, int H, int T, int dk, int dv,
-                        kla_dtype io, void* workspace, size_t ws_bytes, void* stream) {
+                        kla_dtype io, int gates, void* workspace, size_t ws_bytes, void* stream) {
   // ---- validation: no CUDA call before it passes ---------------------------
   kla_status st = check_shape(B, H, T, dk, dv);
   if (st != KLA_OK) return st;
   if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  if (!valid_gates(gates)) return KLA_ERR_INVALID_ARG;
   const long long bh = (long long)B * H;
   const long long tokens = bh * T;
   if ((lam0 == nullptr) != (eta0 == nullptr)) return KLA_ERR_INVALID_ARG;
@@ -414,15 +428,16 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
   if (!aligned16(workspace)) return KLA_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T > 0) {  // forward scan storing its state every 16 tokens (no y)
-    const kla_options seq{KLA_SEQUENTIAL, 0, 0};
+    const kla_options seq{KLA_SEQUENTIAL, 0, 0, gates};
     Plan fp{};
     if ((st = make_plan(B, H, T, dk, dv, io, &seq, sms, &fp)) != KLA_OK) return st;
-    kla::ForwardArgs ff{q, k, v, lam_v, a, pbar, lam0, eta0, nullptr, nullptr, nullptr, B, H, T, dk, dv, (int)io};
+    kla::ForwardArgs ff{q, k, v, lam_v, a, pbar, lam0, eta0, nullptr, nullptr, nullptr, B, H, T, dk, dv, (int)io,
+                        gates};
     if (kla::launch_forward(ff, fp, nullptr, s, reinterpret_cast<float*>(workspace)) != cudaSuccess)
       return KLA_ERR_CUDA;
   }
   kla::BackwardArgs f{q,  k,  v,  lam_v, a,     pbar, lam0, eta0, gy, glamT, getaT, gq, gk, ga,
-                      gpbar, gv, glam_v, glam0, geta0, B, H, T, dk, dv, (int)io};
+                      gpbar, gv, glam_v, glam0, geta0, B, H, T, dk, dv, (int)io, gates};
   const cudaError_t e = kla::launch_backward(f, b, workspace, s);
   return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }

@@ -62,6 +62,7 @@ struct BwdParams {
   float* ckpt;     // [nchunks + 1][2][elems]: (P, μ) at each chunk start, then at T
   float* rowpart;  // [B·H·T·d_k][4] fp32 per-row sums (dq, dk, da, dp̄) when ncb > 1, else null
   int T, dk, dv, cc, ncb, nchunks;
+  int gates;        // kla_gate bits: a, p̄, Λ^v inputs are pre-activations
   long long elems;  // B·H·d_k·d_v
 };
 
@@ -115,14 +116,15 @@ __device__ void stage_chunk(const BwdParams& p, const BwdSmem& s, long long bh, 
   for (int x = threadIdx.x; x < tl * p.dk; x += nthr) {
     s.q[x] = ld<IO>(p.q, rbase + x);
     s.k[x] = ld<IO>(p.k, rbase + x);
-    s.a[x] = ld<IO>(p.a, rbase + x);
-    s.p[x] = ld<IO>(p.pbar, rbase + x);
+    const float xa = ld<IO>(p.a, rbase + x);
+    s.a[x] = gate_a(xa, p.gates);
+    s.p[x] = gate_pbar(ld<IO>(p.pbar, rbase + x), xa, p.gates);
   }
   for (int x = threadIdx.x; x < tl * p.cc; x += nthr) {
     const int t = x / p.cc, j = x - t * p.cc;
     const size_t g = ((size_t)bh * p.T + t0 + t) * p.dv + jb + j;
     s.v[x] = ld<IO>(p.v, g);
-    s.L[x] = ld<IO>(p.lam_v, g);
+    s.L[x] = gate_lamv(ld<IO>(p.lam_v, g), p.gates);
     s.Lv[x] = s.L[x] * s.v[x];
     s.dy[x] = (with_dy && p.dy) ? ld<IO>(p.dy, g) : 0.0f;
   }
@@ -384,10 +386,12 @@ __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
       const size_t g = ((size_t)bh * p.T + t0 + t) * DK + r;
       const float* acc = s.racc + t * 4 * DK + r;
       if (p.ncb == 1) {
+        float gxa = acc[2 * DK], gxp = acc[3 * DK];
+        if (p.gates) gate_chain_row(acc[2 * DK], acc[3 * DK], ld<IO>(p.a, g), ld<IO>(p.pbar, g), p.gates, gxa, gxp);
         reinterpret_cast<IO*>(p.gq)[g] = from_f32<IO>(acc[0]);
         reinterpret_cast<IO*>(p.gk)[g] = from_f32<IO>(acc[DK]);
-        reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(acc[2 * DK]);
-        reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(acc[3 * DK]);
+        reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(gxa);
+        reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(gxp);
       } else {  // other column blocks add to the same rows: accumulate in fp32
         atomicAdd(reinterpret_cast<float4*>(p.rowpart) + g, make_float4(acc[0], acc[DK], acc[2 * DK], acc[3 * DK]));
       }
@@ -396,7 +400,8 @@ __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
       const int t = x / p.cc, j = x - t * p.cc;
       const size_t g = ((size_t)bh * p.T + t0 + t) * p.dv + jb + j;
       const float sz = s.cacc[(t * 2 + 1) * p.cc + j];  // Σ_i k b̄
-      reinterpret_cast<IO*>(p.glam_v)[g] = from_f32<IO>(fmaf(s.v[t * p.cc + j], sz, s.cacc[(t * 2) * p.cc + j]));
+      const float gL = fmaf(s.v[t * p.cc + j], sz, s.cacc[(t * 2) * p.cc + j]);
+      reinterpret_cast<IO*>(p.glam_v)[g] = from_f32<IO>(p.gates ? gate_chain_lamv(gL, ld<IO>(p.lam_v, g), p.gates) : gL);
       reinterpret_cast<IO*>(p.gv)[g] = from_f32<IO>(s.L[t * p.cc + j] * sz);
     }
   }
@@ -422,10 +427,12 @@ template <typename IO>
 __global__ void kla_bwd_finish_kernel(const BwdParams p, size_t BHTdk) {
   for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < BHTdk; g += (size_t)gridDim.x * blockDim.x) {
     const float4 acc = reinterpret_cast<const float4*>(p.rowpart)[g];
+    float gxa = acc.z, gxp = acc.w;
+    if (p.gates) gate_chain_row(acc.z, acc.w, ld<IO>(p.a, g), ld<IO>(p.pbar, g), p.gates, gxa, gxp);
     reinterpret_cast<IO*>(p.gq)[g] = from_f32<IO>(acc.x);
     reinterpret_cast<IO*>(p.gk)[g] = from_f32<IO>(acc.y);
-    reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(acc.z);
-    reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(acc.w);
+    reinterpret_cast<IO*>(p.ga)[g] = from_f32<IO>(gxa);
+    reinterpret_cast<IO*>(p.gpbar)[g] = from_f32<IO>(gxp);
   }
 }
 
@@ -499,6 +506,7 @@ cudaError_t launch_backward(const BackwardArgs& f, const BwdPlan& b, void* works
   bp.rowpart = b.ncb > 1 ? reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + b.ckpt_bytes) : nullptr;
   bp.T = f.T; bp.dk = f.dk; bp.dv = f.dv; bp.cc = b.cc; bp.ncb = b.ncb; bp.nchunks = b.nchunks;
   bp.elems = bh * f.dk * f.dv;
+  bp.gates = f.gates;
   const dim3 grid((unsigned)bh, (unsigned)b.ncb);
   return f.io == IO_BF16 ? launch_bwd_io<__nv_bfloat16>(f.dk, bp, grid, b.threads, b.smem, s)
                          : launch_bwd_io<float>(f.dk, bp, grid, b.threads, b.smem, s);

@@ -72,6 +72,7 @@ struct KernelParams {
   float* ckpt;          // scan only, or nullptr: [T/16 + 1][2][elems] scaled states (P̃, μ)
                         // at every 16-token tile start and at the end
   int T, dv, chunk_len, cc, log2cc;
+  int gates;        // kla_gate bits
   long long elems;  // B·H·dk·dv
 };
 
@@ -135,12 +136,13 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 // entries (no bank conflicts); the duplicated pairs let one packed
 // instruction serve two rows.
 template <typename IO, int DK, int TC>
-__device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl, int tid, int nthr) {
+__device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl, int tid, int nthr,
+                                             int gates) {
   using R = RawTile<IO, DK, TC>;
   const IO* rv = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes());
   const IO* rL = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes() + R::col_bytes(cc));
   for (int g = tid; g < tl * cc; g += nthr) {
-    const float L = to_f32<IO>(rL[g]);
+    const float L = gate_lamv(to_f32<IO>(rL[g]), gates);
     const float Lv = L * to_f32<IO>(rv[g]);
     pj[g] = make_float4(L, L, Lv, Lv);
   }
@@ -157,6 +159,7 @@ inline KernelParams make_params(const ForwardArgs& f, const Plan& p) {
   while ((1 << l2) < p.cols_per_block) ++l2;
   kp.log2cc = l2;
   kp.elems = (long long)f.B * f.H * f.dk * f.dv;
+  kp.gates = f.gates;
   return kp;
 }
 

@@ -94,15 +94,16 @@ __global__ void __launch_bounds__(kMaxThreads) kla_compose_kernel(const KernelPa
       for (int idx = tid; idx < tl * DK; idx += blockDim.x) {
         const int t = idx / DK, i = idx % DK;
         const float kt = to_f32<IO>(rk[idx]);
-        const float at = fmaxf(to_f32<IO>(ra[idx]), kAMin);
+        const float xa = to_f32<IO>(ra[idx]);
+        const float at = fmaxf(gate_a(xa, p.gates), kAMin);
         float* ct = coef + t * 5 * DK + i;
-        ct[0 * DK] = at * at;                      // a²
-        ct[1 * DK] = to_f32<IO>(rp[idx]);          // p̄
+        ct[0 * DK] = at * at;                                       // a²
+        ct[1 * DK] = gate_pbar(to_f32<IO>(rp[idx]), xa, p.gates);  // p̄
         ct[2 * DK] = fmaf(kt, kt, kK2Floor);       // k² (floored as in the scan)
         ct[3 * DK] = kt;                           // k
         ct[4 * DK] = at;                           // a
       }
-      column_terms<IO, DK, TC>(buf, pj, p.cc, tl, tid, blockDim.x);
+      column_terms<IO, DK, TC>(buf, pj, p.cc, tl, tid, blockDim.x, p.gates);
     }
     __syncthreads();
 

@@ -102,4 +102,48 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+
+// ---- gate activations (kla_options.gates) -----------------------------------
+// With a gate bit set the corresponding input holds a pre-activation:
+//   Λ^v = softplus(x), a = sigmoid(x), p̄ = softplus(x), or the OU-tied
+//   p̄ = softplus(x)·(1 − a²) (an exactly discretised OU process with
+//   stationary variance softplus(x) and decay a).
+constexpr int kGateLamV = 1, kGateA = 2, kGatePbarSoftplus = 4, kGatePbarOU = 8;
+
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float gate_lamv(float x, int gates) { return (gates & kGateLamV) ? softplus_f(x) : x; }
+__device__ __forceinline__ float gate_a(float x, int gates) { return (gates & kGateA) ? sigmoid_f(x) : x; }
+// p̄ from its input xp and the decay's input xa (both as given to the kernel).
+__device__ __forceinline__ float gate_pbar(float xp, float xa, int gates) {
+  if (gates & kGatePbarOU) {
+    // 1 − a² = (1 − a)(1 + a), with 1 − a = sigmoid(−x) when a = sigmoid(x)
+    const float one_minus_a = (gates & kGateA) ? sigmoid_f(-xa) : 1.0f - xa;
+    const float a = (gates & kGateA) ? sigmoid_f(xa) : xa;
+    return softplus_f(xp) * (one_minus_a * (1.0f + a));
+  }
+  return (gates & kGatePbarSoftplus) ? softplus_f(xp) : xp;
+}
+
+
+// Gradients with respect to the pre-activations, from the gradients ga, gp
+// with respect to a and p̄ (per row) ...
+__device__ __forceinline__ void gate_chain_row(float ga, float gp, float xa, float xp, int gates, float& gxa,
+                                               float& gxp) {
+  const float a = (gates & kGateA) ? sigmoid_f(xa) : xa;
+  if (gates & kGatePbarOU) {  // p̄ = S(1 − a²), S = softplus(xp)
+    const float one_minus_a = (gates & kGateA) ? sigmoid_f(-xa) : 1.0f - xa;
+    gxp = gp * (one_minus_a * (1.0f + a)) * sigmoid_f(xp);
+    ga = fmaf(gp * softplus_f(xp), -2.0f * a, ga);
+  } else {
+    gxp = (gates & kGatePbarSoftplus) ? gp * sigmoid_f(xp) : gp;
+  }
+  gxa = (gates & kGateA) ? ga * (a * sigmoid_f(-xa)) : ga;  // σ' = σ(x)σ(−x)
+}
+// ... and from the gradient with respect to Λ^v (per column).
+__device__ __forceinline__ float gate_chain_lamv(float gL, float xL, int gates) {
+  return (gates & kGateLamV) ? gL * sigmoid_f(xL) : gL;
+}
+
 }  // namespace kla

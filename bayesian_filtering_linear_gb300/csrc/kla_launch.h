@@ -15,7 +15,8 @@ struct ForwardArgs {
   void* y;
   float *lamT, *etaT;
   int B, H, T, dk, dv;
-  int io;  // IoType
+  int io;     // IoType
+  int gates;  // kla_gate bits: Λ^v, a, p̄ given as pre-activations
 };
 
 // Launch geometry shared by the planner and the launchers.
@@ -69,6 +70,7 @@ struct BackwardArgs {
   float *dlam0, *deta0;                        // [B,H,dk,dv] fp32, or null
   int B, H, T, dk, dv;
   int io;
+  int gates;
 };
 struct BwdPlan {
   int cc, cpl, threads, ncb, nchunks;
@@ -83,6 +85,7 @@ struct StepArgs {
   void* y;
   int B, H, dk, dv;
   int io;
+  int gates;
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 

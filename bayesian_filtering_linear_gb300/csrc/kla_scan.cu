@@ -89,7 +89,7 @@ struct ScanLayout {
 // chunk start); K of the tile's last row goes to kp_nxt.
 template <typename IO, int DK, int TC, bool VAR = false>
 __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float* coef, const float* kp_cur,
-                                                 float* kp_nxt, int tl, int tid, int nthr) {
+                                                 float* kp_nxt, int tl, int tid, int nthr, int gates) {
   using R = RawTile<IO, DK, TC>;
   const IO* rq = reinterpret_cast<const IO*>(raw);
   const IO* rk = reinterpret_cast<const IO*>(raw + R::row_bytes());
@@ -113,13 +113,14 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
     float A[4], B[4], AI[4], KI[4], Kt[4], QV[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float at = fmaxf(av[u], kAMin);
+      const float at = fmaxf(gate_a(av[u], gates), kAMin);
+      const float pbu = gate_pbar(pv[u], av[u], gates);
       Kt[u] = fmaf(kv[u], kv[u], kK2Floor);
       const float aK = at * Kt[u];
       const float r = rcp_approx(aK * kpv[u]);  // 1 / (a K_t K_{t-1})
       AI[u] = (Kt[u] * kpv[u]) * r;             // 1/a
       A[u] = aK * (aK * r);                     // K_t a / K_{t-1}
-      B[u] = (Kt[u] * pv[u]) * AI[u];           // K_t p̄ / a
+      B[u] = (Kt[u] * pbu) * AI[u];             // K_t p̄ / a
       const float rK = at * kpv[u] * r;         // 1 / K_t
       KI[u] = kv[u] * rK;                       // k / K_t
       QV[u] = VAR ? qv[u] * qv[u] * rK : qv[u];  // q²/K_t (variance readout) or q
@@ -203,9 +204,10 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
       const int bm = m & 1;
       row_coefficients<IO, DK, TC, VAR>(smem + L.raw(bm), reinterpret_cast<float*>(smem + L.coef(bm)),
                                    reinterpret_cast<const float*>(smem + L.kprev(bm)),
-                                   reinterpret_cast<float*>(smem + L.kprev(bm ^ 1)), tile_len(m), ptid, pn);
+                                   reinterpret_cast<float*>(smem + L.kprev(bm ^ 1)), tile_len(m), ptid, pn,
+                                   p.gates);
       column_terms<IO, DK, TC>(smem + L.raw(bm), reinterpret_cast<float4*>(smem + L.pj(bm)), p.cc, tile_len(m),
-                               ptid, pn);
+                               ptid, pn, p.gates);
     };
     stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, tile_len(0), ptid, pn);
     cp_async_commit();

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(1024) kla_step_kernel(const StepArgs a) {
   float Lc[4], Bv[4], y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    Lc[c] = to_f32<IO>(lv[j0 + c]);
+    Lc[c] = gate_lamv(to_f32<IO>(lv[j0 + c]), a.gates);
     Bv[c] = Lc[c] * to_f32<IO>(vv[j0 + c]);
   }
   float* lam = a.lam + (size_t)bh * dk * dv;
@@ -53,8 +53,9 @@ __global__ void __launch_bounds__(1024) kla_step_kernel(const StepArgs a) {
   for (int rr = 0; rr < kRowsPerThread; ++rr) {
     const int i = r0 + rr;
     const float ki = to_f32<IO>(kv[i]);
-    const float ai = fmaxf(to_f32<IO>(av[i]), kAMin);
-    const float pi = to_f32<IO>(pv[i]);
+    const float xa = to_f32<IO>(av[i]);
+    const float ai = fmaxf(gate_a(xa, a.gates), kAMin);
+    const float pi = gate_pbar(to_f32<IO>(pv[i]), xa, a.gates);
     const float qi = to_f32<IO>(qv[i]);
     const float K = fmaf(ki, ki, kK2Floor);
     const float a2 = ai * ai;

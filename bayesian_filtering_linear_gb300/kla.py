@@ -24,11 +24,12 @@ _IO = {torch.float32: F32, torch.bfloat16: BF16}
 # Every function the header declares, for the export check.
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
            "kla_status_string", "kla_version", "kla_forward_chunked_noalloc", "kla_backward_workspace_size",
-           "kla_backward", "kla_forward_uncertainty")
+           "kla_backward", "kla_forward_uncertainty", "kla_step_gated")
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("rows_per_lane", ctypes.c_int)]
+    _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("rows_per_lane", ctypes.c_int),
+                ("gates", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -63,7 +64,9 @@ def load_library(path: str = LIB_PATH):
     lib.kla_backward_workspace_size.restype = sz
     lib.kla_backward_workspace_size.argtypes = [i] * 5
     lib.kla_backward.restype = i
-    lib.kla_backward.argtypes = [vp] * 19 + [i] * 6 + [vp, sz, vp]
+    lib.kla_backward.argtypes = [vp] * 19 + [i] * 7 + [vp, sz, vp]
+    lib.kla_step_gated.restype = i
+    lib.kla_step_gated.argtypes = [vp] * 9 + [i] * 6 + [vp]
     return lib
 
 
@@ -85,9 +88,13 @@ def status_string(status: int) -> str:
     return LIB.kla_status_string(status).decode()
 
 
-def options(strategy: str | int = "auto", chunk_len: int = 0, rows_per_lane: int = 0) -> Options:
+# kla_gate bits: the corresponding input holds a pre-activation
+GATE_LAMV_SOFTPLUS, GATE_A_SIGMOID, GATE_PBAR_SOFTPLUS, GATE_PBAR_OU = 1, 2, 4, 8
+
+
+def options(strategy: str | int = "auto", chunk_len: int = 0, rows_per_lane: int = 0, gates: int = 0) -> Options:
     s = _STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
-    return Options(s, int(chunk_len), int(rows_per_lane))
+    return Options(s, int(chunk_len), int(rows_per_lane), int(gates))
 
 
 def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strategy: str | int = "auto",
@@ -132,11 +139,13 @@ def _need(t, name, dtype, shape, device):
 
 def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None, etaT=None,
             strategy: str | int = "auto", chunk_len: int = 0, workspace=None, stream=None,
-            final_state: bool = True, rows_per_lane: int = 0, uncertainty: bool = False, y_var=None):
+            final_state: bool = True, rows_per_lane: int = 0, uncertainty: bool = False, y_var=None,
+            gates: int = 0):
     """Whole-sequence KLA scan. Returns ``(y, lamT, etaT)`` (the last two are
     None when ``final_state`` is False and none were given); with
     ``uncertainty`` (or a ``y_var`` buffer) also the variance readout
-    ``y_var[t, j] = Σ_i q_i² / λ_{t,i,j}`` as a fourth element."""
+    ``y_var[t, j] = Σ_i q_i² / λ_{t,i,j}`` as a fourth element. ``gates``: kla_gate
+    bits (GATE_*), the corresponding inputs being pre-activations."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -159,7 +168,7 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
     if final_state and lamT is None:
         lamT = torch.empty(st_shape, dtype=torch.float32, device=dev)
         etaT = torch.empty(st_shape, dtype=torch.float32, device=dev)
-    opt = options(strategy, chunk_len, rows_per_lane)
+    opt = options(strategy, chunk_len, rows_per_lane, gates)
     with torch.cuda.device(dev):
         if workspace is None:
             info = PlanInfo()
@@ -185,7 +194,7 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
     return y, lamT, etaT
 
 
-def step(q, k, v, lam_v, a, pbar, lam, eta, *, y=None, stream=None):
+def step(q, k, v, lam_v, a, pbar, lam, eta, *, y=None, stream=None, gates: int = 0):
     """One decode step: q, k, a, pbar ``[B,H,dk]``, v, lam_v ``[B,H,dv]``;
     updates the fp32 state (lam, eta) ``[B,H,dk,dv]`` in place; returns y."""
     B, H, dk = q.shape
@@ -203,14 +212,14 @@ def step(q, k, v, lam_v, a, pbar, lam, eta, *, y=None, stream=None):
     else:
         _need(y, "y", dt, (B, H, dv), dev)
     with torch.cuda.device(dev):
-        st = LIB.kla_step(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam), _ptr(eta),
-                          _ptr(y), B, H, dk, dv, _IO[dt], _stream(stream))
+        st = LIB.kla_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam), _ptr(eta),
+                                _ptr(y), B, H, dk, dv, _IO[dt], int(gates), _stream(stream))
     _check(st, "kla_step")
     return y
 
 
 def backward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, gy=None, glamT=None, getaT=None,
-             state_grads: bool = True, workspace=None, stream=None):
+             state_grads: bool = True, workspace=None, stream=None, gates: int = 0):
     """Gradients of a scalar loss through :func:`forward`, given ``gy`` = dL/dy
     ``[B,H,T,dv]`` (I/O dtype) and optionally ``glamT``, ``getaT`` = dL/dλ_T,
     dL/dη_T (fp32 ``[B,H,dk,dv]``). Returns a dict with ``gq, gk, ga, gpbar``
@@ -247,7 +256,7 @@ def backward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, gy=None, glamT=No
         st = LIB.kla_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam0), _ptr(eta0),
                               _ptr(gy), _ptr(glamT), _ptr(getaT), _ptr(out["gq"]), _ptr(out["gk"]), _ptr(out["gv"]),
                               _ptr(out["glam_v"]), _ptr(out["ga"]), _ptr(out["gpbar"]), _ptr(out.get("glam0")),
-                              _ptr(out.get("geta0")), B, H, T, dk, dv, _IO[dt], _ptr(workspace), ws_bytes,
-                              _stream(stream))
+                              _ptr(out.get("geta0")), B, H, T, dk, dv, _IO[dt], int(gates), _ptr(workspace),
+                              ws_bytes, _stream(stream))
     _check(st, "kla_backward")
     return out

@@ -68,11 +68,31 @@ typedef enum kla_dtype { KLA_F32 = 0, KLA_BF16 = 1 } kla_dtype;
  * (compose per-chunk maps, carry them across chunks, re-run each chunk). */
 typedef enum kla_strategy { KLA_AUTO = 0, KLA_SEQUENTIAL = 1, KLA_CHUNKED = 2 } kla_strategy;
 
+/* Gate activations fused into the scan (the elementwise part of the layer's
+ * parameterisation; Methodologie §1 of the summary: OU decay a in (0, 1),
+ * process noise p̄ > 0, value precision Λ^v > 0). With a bit set, the
+ * corresponding input holds a pre-activation x and the kernels use
+ *   KLA_GATE_LAMV_SOFTPLUS: Λ^v = softplus(x) = log(1 + e^x)
+ *   KLA_GATE_A_SIGMOID:     a = sigmoid(x) = 1 / (1 + e^-x)
+ *   KLA_GATE_PBAR_SOFTPLUS: p̄ = softplus(x)
+ *   KLA_GATE_PBAR_OU:       p̄ = softplus(x)·(1 − a²) — the exactly discretised
+ *                           OU process with stationary variance softplus(x)
+ * (at most one of the two p̄ bits). Gradients from kla_backward are then
+ * with respect to the pre-activations. */
+typedef enum kla_gate {
+  KLA_GATE_LAMV_SOFTPLUS = 1,
+  KLA_GATE_A_SIGMOID = 2,
+  KLA_GATE_PBAR_SOFTPLUS = 4,
+  KLA_GATE_PBAR_OU = 8
+} kla_gate;
+
 typedef struct kla_options {
   int strategy;      /* kla_strategy */
   int chunk_len;     /* tokens per chunk for KLA_CHUNKED; 0 = automatic; multiple of 32 */
   int rows_per_lane; /* scan-kernel rows per lane: 0 = automatic, else 4 or 8 (8 needs d_k >= 64);
                         another value is INVALID_ARG. Results do not depend on it. */
+  int gates;         /* kla_gate bits (0 = inputs are a, p̄, Λ^v themselves); unknown bits or both
+                        p̄ bits are INVALID_ARG */
 } kla_options;
 
 /* The launch plan kla_forward would use for this shape on the current device. */
@@ -140,6 +160,11 @@ kla_status kla_step(const void* q, const void* k, const void* v, const void* lam
                     const void* a, const void* pbar, float* lam, float* eta, void* y,
                     int B, int H, int dk, int dv, kla_dtype io, void* stream);
 
+/* kla_step with gate activations (kla_gate bits, as in kla_options.gates). */
+kla_status kla_step_gated(const void* q, const void* k, const void* v, const void* lam_v,
+                          const void* a, const void* pbar, float* lam, float* eta, void* y,
+                          int B, int H, int dk, int dv, kla_dtype io, int gates, void* stream);
+
 /* kla_forward on the chunk-parallel path, for callers that cannot allocate
  * device memory. (Library-side addition: the summary has no counterpart.)
  * Callers that run inside an allocator or memory-pool callback, in a loop
@@ -179,6 +204,9 @@ kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void*
  *     kla_backward_workspace_size() bytes (required when B·H > 0; else
  *     KLA_ERR_WORKSPACE): the forward state every 16 tokens plus, when a
  *     head's columns are split over several blocks, per-row partial sums.
+ *   gates: kla_gate bits as in kla_options.gates (the forward that produced
+ *     L must have used the same); ga, gpbar, glam_v are then gradients with
+ *     respect to the pre-activations.
  *   Outputs must not overlap inputs or each other. Pointers 16-byte aligned
  *   (else MISALIGNED); shape rules and errors as for kla_forward. The order
  *   of the per-row and per-column sums across warps is not fixed, so the
@@ -189,7 +217,7 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
                         const void* gy, const float* glamT, const float* getaT,
                         void* gq, void* gk, void* gv, void* glam_v, void* ga, void* gpbar,
                         float* glam0, float* geta0, int B, int H, int T, int dk, int dv,
-                        kla_dtype io, void* workspace, size_t ws_bytes, void* stream);
+                        kla_dtype io, int gates, void* workspace, size_t ws_bytes, void* stream);
 
 /* Static, human-readable name of a status code. */
 const char* kla_status_string(kla_status s);

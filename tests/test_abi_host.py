@@ -175,12 +175,12 @@ def test_planner_rows_per_lane_choice():
 
 
 def bwd(B=1, H=1, T=8, dk=16, dv=16, io=kla.F32, ptrs=None, lam0=None, eta0=None, glam0=None, geta0=None,
-        ws=None, ws_bytes=0):
+        ws=None, ws_bytes=0, gates=0):
     ptrs = ptrs or {}
     g = lambda n: ptrs.get(n, P)
     return L.kla_backward(g("q"), g("k"), g("v"), g("lam_v"), g("a"), g("pbar"), lam0, eta0, ptrs.get("gy"),
                           ptrs.get("glamT"), ptrs.get("getaT"), g("gq"), g("gk"), g("gv"), g("glam_v"), g("ga"),
-                          g("gpbar"), glam0, geta0, B, H, T, dk, dv, io, ws, ws_bytes, None)
+                          g("gpbar"), glam0, geta0, B, H, T, dk, dv, io, gates, ws, ws_bytes, None)
 
 
 def test_backward_validation_before_any_cuda_call():
@@ -194,6 +194,8 @@ def test_backward_validation_before_any_cuda_call():
     for name in ("gq", "gy", "glamT", "v"):
         assert bwd(ptrs={name: MIS}) == kla.ERR_MISALIGNED, name
     assert bwd(glam0=P, geta0=P) == kla.ERR_INVALID_ARG       # the two outputs alias
+    assert bwd(gates=16) == kla.ERR_INVALID_ARG               # unknown gate bit
+    assert bwd(gates=kla.GATE_PBAR_SOFTPLUS | kla.GATE_PBAR_OU) == kla.ERR_INVALID_ARG
     # nothing to do: OK without touching CUDA
     assert bwd(B=0, ptrs={n: None for n in ("q", "k", "v", "lam_v", "a", "pbar", "gq", "gk", "gv", "glam_v",
                                               "ga", "gpbar")}) == kla.OK
@@ -216,3 +218,10 @@ def test_forward_uncertainty_validation_before_any_cuda_call():
     assert fu(y_var=ctypes.c_void_p(0x30000)) == kla.ERR_INVALID_ARG        # same buffer as y
     assert fu(y_var=ctypes.c_void_p(0x30000 + 64)) == kla.ERR_INVALID_ARG   # overlaps y (8x16 fp32 = 512 B)
     assert fu(y_var=MIS) == kla.ERR_MISALIGNED
+
+
+def test_gate_bits_are_validated_before_any_cuda_call():
+    for g in (16, 32, kla.GATE_PBAR_SOFTPLUS | kla.GATE_PBAR_OU):
+        assert fwd(opt=ctypes.byref(kla.Options(kla.AUTO, 0, 0, g))) == kla.ERR_INVALID_ARG
+        assert L.kla_step_gated(P, P, P, P, P, P, P, ctypes.c_void_p(0x50000), P, 1, 1, 16, 16, kla.F32, g,
+                                None) == kla.ERR_INVALID_ARG
