@@ -191,3 +191,20 @@ def test_decode_steps_match_forward_and_oracle():
     ref = run_oracle(x, heads=heads)
     e = errors(torch.cat([y_full[:, :, :P], y_steps], dim=2), lam, eta, ref, heads=heads)
     assert_close(e, 1e-4, "decode vs oracle")
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 20, 64, 32, "bf16"), (1, 2, 12, 128, 16, "bf16"), (3, 1, 9, 16, 128, "f32"),
+                                   (1, 1, 15, 32, 64, "f32")], ids=lambda s: "x".join(map(str, s)))
+def test_decode_steps_every_head_size_match_oracle(shape):
+    """kla_step token by token from the initial state equals the oracle's scan."""
+    B, H, T, dk, dv, io = shape
+    x = make_inputs(B, H, T, dk, dv, io=io, seed=900 + T, random_state=True)
+    ref = run_oracle(x)
+    xd = to_dev(x)
+    lam, eta = xd["lam0"].clone(), xd["eta0"].clone()
+    ys = []
+    for t in range(T):
+        tok = {n: xd[n][:, :, t].contiguous() for n in ("q", "k", "v", "lam_v", "a", "pbar")}
+        ys.append(kla.step(tok["q"], tok["k"], tok["v"], tok["lam_v"], tok["a"], tok["pbar"], lam, eta))
+    torch.cuda.synchronize()
+    assert_close(errors(torch.stack(ys, dim=2), lam, eta, ref), TOL[IO[io]], f"step {shape}")
