@@ -7,6 +7,10 @@
 
 namespace kla {
 
+// Build-time geometry knobs (defaults are the measured best on GB300):
+// columns per lane, scanning threads per block, rows per lane of the
+// composition kernel at d_k = 64, and lane-exchange rounds of the readout
+// (-1: one round per halving of the columns a lane holds).
 #ifndef KLA_CL
 #define KLA_CL 2
 #endif
@@ -16,16 +20,12 @@ namespace kla {
 #ifndef KLA_RL64
 #define KLA_RL64 8
 #endif
-#ifndef KLA_UNROLL
-#define KLA_UNROLL 2
-#endif
 #ifndef KLA_XR
 #define KLA_XR -1
 #endif
 
 constexpr int CL = KLA_CL;             // d_v columns per lane (2 or 4)
-constexpr int kMaxThreads = KLA_MAXT;  // per block (256 leaves up to 255 registers per thread)
-constexpr int kUnroll = KLA_UNROLL;    // token-loop unroll factor of the scan
+constexpr int kMaxThreads = KLA_MAXT;  // scanning threads per block (256 leaves up to 168 registers each)
 constexpr int kProducerWarps = 4;      // scan: warps that stage tiles, build coefficients and store y
 
 // Named barriers (ids 1..15; 0 is __syncthreads). bar.arrive counts this
