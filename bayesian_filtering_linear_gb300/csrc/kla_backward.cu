@@ -82,6 +82,7 @@ struct BwdGeo {
 // accesses are contiguous).
 struct BwdSmem {
   float *q, *k, *a, *p, *v, *L, *Lv, *dy, *racc, *cacc, *st;
+  unsigned char* raw;  // the next chunk's inputs as loaded (I/O dtype), filled by cp.async
   __device__ BwdSmem(float* base, int dk, int cc) {
     q = base;
     k = q + kChunk * dk;
@@ -94,10 +95,11 @@ struct BwdSmem {
     racc = dy + kChunk * cc;
     cacc = racc + kChunk * 4 * dk;
     st = cacc + kChunk * 2 * cc;
+    raw = reinterpret_cast<unsigned char*>(st + kSub * 2 * kCpl * (int)blockDim.x);
   }
   __host__ __device__ static size_t bytes(int dk, int cc, int threads) {
     return sizeof(float) * ((size_t)kChunk * (4 * dk + 4 * cc) + (size_t)kChunk * 4 * dk + (size_t)kChunk * 2 * cc +
-                            (size_t)kSub * 2 * kCpl * threads);
+                            (size_t)kSub * 2 * kCpl * threads + (size_t)kChunk * (4 * dk + 3 * cc));
   }
 };
 
@@ -106,28 +108,52 @@ __device__ __forceinline__ float ld(const void* base, size_t idx) {
   return to_f32<IO>(reinterpret_cast<const IO*>(base)[idx]);
 }
 
-// Stage tokens [t0, t0 + tl) of the block's inputs as fp32 (rows padded with
-// zeros past tl are never read).
+// Queue 16-byte asynchronous copies of tokens [t0, t0 + tl) of the block's
+// inputs (q, k, a, p̄ rows; v, Λ^v, dy columns) into s.raw, as stored.
 template <typename IO>
-__device__ void stage_chunk(const BwdParams& p, const BwdSmem& s, long long bh, int jb, int t0, int tl,
-                            bool with_dy) {
+__device__ void issue_raw(const BwdParams& p, const BwdSmem& s, long long bh, int jb, int t0, int tl) {
   const int nthr = blockDim.x;
-  const size_t rbase = ((size_t)bh * p.T + t0) * p.dk;
+  const size_t rowb = (size_t)kChunk * p.dk * sizeof(IO), colb = (size_t)kChunk * p.cc * sizeof(IO);
+  const int rchunks = (int)((size_t)tl * p.dk * sizeof(IO) / 16);
+  const size_t rsrc = ((size_t)bh * p.T + t0) * p.dk * sizeof(IO);
+  const void* rows[4] = {p.q, p.k, p.a, p.pbar};
+#pragma unroll
+  for (int arr = 0; arr < 4; ++arr)
+    for (int c = threadIdx.x; c < rchunks; c += nthr)
+      cp_async16(s.raw + arr * rowb + (size_t)c * 16, static_cast<const char*>(rows[arr]) + rsrc + (size_t)c * 16);
+  const int cpr = (int)(p.cc * sizeof(IO) / 16);  // 16-byte pieces per token row
+  const size_t csrc = (((size_t)bh * p.T + t0) * p.dv + jb) * sizeof(IO), cstride = (size_t)p.dv * sizeof(IO);
+  const void* cols[3] = {p.v, p.lam_v, p.dy};
+  for (int arr = 0; arr < (p.dy ? 3 : 2); ++arr)
+    for (int c = threadIdx.x; c < tl * cpr; c += nthr) {
+      const int t = c / cpr, piece = c - t * cpr;
+      cp_async16(s.raw + 4 * rowb + arr * colb + (size_t)c * 16,
+                 static_cast<const char*>(cols[arr]) + csrc + t * cstride + (size_t)piece * 16);
+    }
+}
+
+// Widen the staged chunk to fp32 (gates applied, Λ^v·v formed) and clear the
+// chunk's sum accumulators.
+template <typename IO>
+__device__ void convert_raw(const BwdParams& p, const BwdSmem& s, int tl) {
+  const int nthr = blockDim.x;
+  const IO* r = reinterpret_cast<const IO*>(s.raw);
+  const IO *rq = r, *rk = r + kChunk * p.dk, *ra = rk + kChunk * p.dk, *rp = ra + kChunk * p.dk;
+  const IO *rv = rp + kChunk * p.dk, *rL = rv + kChunk * p.cc, *rg = rL + kChunk * p.cc;
   for (int x = threadIdx.x; x < tl * p.dk; x += nthr) {
-    s.q[x] = ld<IO>(p.q, rbase + x);
-    s.k[x] = ld<IO>(p.k, rbase + x);
-    const float xa = ld<IO>(p.a, rbase + x);
+    s.q[x] = to_f32<IO>(rq[x]);
+    s.k[x] = to_f32<IO>(rk[x]);
+    const float xa = to_f32<IO>(ra[x]);
     s.a[x] = gate_a(xa, p.gates);
-    s.p[x] = gate_pbar(ld<IO>(p.pbar, rbase + x), xa, p.gates);
+    s.p[x] = gate_pbar(to_f32<IO>(rp[x]), xa, p.gates);
   }
   for (int x = threadIdx.x; x < tl * p.cc; x += nthr) {
-    const int t = x / p.cc, j = x - t * p.cc;
-    const size_t g = ((size_t)bh * p.T + t0 + t) * p.dv + jb + j;
-    s.v[x] = ld<IO>(p.v, g);
-    s.L[x] = gate_lamv(ld<IO>(p.lam_v, g), p.gates);
+    s.v[x] = to_f32<IO>(rv[x]);
+    s.L[x] = gate_lamv(to_f32<IO>(rL[x]), p.gates);
     s.Lv[x] = s.L[x] * s.v[x];
-    s.dy[x] = (with_dy && p.dy) ? ld<IO>(p.dy, g) : 0.0f;
+    s.dy[x] = p.dy ? to_f32<IO>(rg[x]) : 0.0f;
   }
+  for (int x = threadIdx.x; x < kChunk * (4 * p.dk + 2 * p.cc); x += nthr) s.racc[x] = 0.0f;
 }
 
 // Lane geometry of the reverse kernel.
@@ -283,12 +309,17 @@ __global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
     }
   }
 
+  auto chunk_len = [&](int c) { return min(kChunk, p.T - c * kChunk); };
+  if (p.nchunks > 0) issue_raw<IO>(p, s, bh, jb, (p.nchunks - 1) * kChunk, chunk_len(p.nchunks - 1));
+  cp_async_commit();
   for (int c = p.nchunks - 1; c >= 0; --c) {
-    const int t0 = c * kChunk, tl = min(kChunk, p.T - t0);
-    __syncthreads();  // the previous chunk's staged inputs and sums are no longer read
-    stage_chunk<IO>(p, s, bh, jb, t0, tl, true);
-    for (int x = threadIdx.x; x < kChunk * (4 * DK + 2 * p.cc); x += blockDim.x) s.racc[x] = 0.0f;
-    __syncthreads();
+    const int t0 = c * kChunk, tl = chunk_len(c);
+    cp_async_wait<0>();
+    __syncthreads();  // chunk c's inputs have landed; the previous chunk's staged data is no longer read
+    convert_raw<IO>(p, s, tl);
+    __syncthreads();  // staged; the raw buffer is free for the next chunk
+    if (c > 0) issue_raw<IO>(p, s, bh, jb, t0 - kChunk, kChunk);
+    cp_async_commit();
     const f2 rK = inv_scale(t0);
     for (int sb = (tl - 1) / kSub; sb >= 0; --sb) {
       const int ts = sb * kSub;
