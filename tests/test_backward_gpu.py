@@ -139,3 +139,14 @@ def test_backward_headline_workload_sampled_heads():
     check(out, ref, "bf16", "headline", heads=heads)
     for n in GRADS:
         assert torch.isfinite(out[n].float()).all(), n
+
+
+def test_backward_long_workload_sampled_head():
+    """B1 H16 T65536 d128 bf16 at full size (columns split over blocks, the
+    row-sum pass) against the oracle on one head."""
+    x = make_workload("long")
+    B, H, T, dk, dv = 1, 16, 65536, 128, 128
+    gy, gl, ge = upstream(B, H, T, dk, dv, "bf16", seed=8)
+    heads = [5]
+    out, ref = run_both(x, "bf16", gy, gl, ge, heads=heads)
+    check(out, ref, "bf16", "long", heads=heads)
