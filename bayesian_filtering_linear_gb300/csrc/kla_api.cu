@@ -268,24 +268,32 @@ kla_status forward_impl(const void* q, const void* k, const void* v, const void*
                      opt ? opt->gates : 0};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  // The variance readout (when asked for) runs before the main pass, which
-  // may overwrite λ0/η0 in place.
+  // The variance readout (when asked for) is fused into the scan (mode 2)
+  // when that kernel's shared memory fits; otherwise it is a separate pass
+  // without the mean (mode 1), run before the main pass, which may
+  // overwrite λ0/η0 in place.
+  const bool fused = y_var && kla::forward_smem_bytes(dk, p.rows_per_lane, io, p.cols_per_block, p.tile, 2) <=
+                                  kMaxSmem;
+  f.y_var = fused ? y_var : nullptr;
   kla::ForwardArgs fv = f;
   fv.y = y_var;
+  fv.y_var = nullptr;
   fv.lamT = fv.etaT = nullptr;
+  const int main_mode = fused ? 2 : 0;
+  const bool var_pass = y_var && !fused;
   if (T == 0) {
     e = kla::launch_init_state(f, s);
   } else if (p.strategy == KLA_SEQUENTIAL) {
-    e = y_var ? kla::launch_forward(fv, p, nullptr, s, nullptr, true) : cudaSuccess;
-    if (e == cudaSuccess) e = kla::launch_forward(f, p, nullptr, s);
+    e = var_pass ? kla::launch_forward(fv, p, nullptr, s, nullptr, 1) : cudaSuccess;
+    if (e == cudaSuccess) e = kla::launch_forward(f, p, nullptr, s, nullptr, main_mode);
   } else {
     const long long elems = bh * dk * dv;
     float* maps = reinterpret_cast<float*>(workspace);
     float* starts = maps + (size_t)7 * (p.num_chunks - 1) * elems;
     e = kla::launch_compose(f, p, maps, s);
     if (e == cudaSuccess) e = kla::launch_carry(f, p, maps, starts, s);
-    if (e == cudaSuccess && y_var) e = kla::launch_forward(fv, p, starts, s, nullptr, true);
-    if (e == cudaSuccess) e = kla::launch_forward(f, p, starts, s);
+    if (e == cudaSuccess && var_pass) e = kla::launch_forward(fv, p, starts, s, nullptr, 1);
+    if (e == cudaSuccess) e = kla::launch_forward(f, p, starts, s, nullptr, main_mode);
   }
   return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }

@@ -68,6 +68,7 @@ struct KernelParams {
   const float* starts;  // [S][2][elems] chunk-start (P, μ), or nullptr
   float* maps;          // compose output [S-1][7][elems]
   void* y;              // nullptr: y is not stored (checkpoint pass of the backward)
+  void* y_var;          // the variance readout when the scan computes both readouts
   float *lamT, *etaT;
   float* ckpt;          // scan only, or nullptr: [T/16 + 1][2][elems] scaled states (P̃, μ)
                         // at every 16-token tile start and at the end
@@ -135,14 +136,14 @@ __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
 // (t, j) per thread so that consecutive threads store consecutive 16-byte
 // entries (no bank conflicts); the duplicated pairs let one packed
 // instruction serve two rows.
-template <typename IO, int DK, int TC>
+template <typename IO, int DK, int TC, bool GATED = true>
 __device__ __forceinline__ void column_terms(const unsigned char* raw, float4* pj, int cc, int tl, int tid, int nthr,
                                              int gates) {
   using R = RawTile<IO, DK, TC>;
   const IO* rv = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes());
   const IO* rL = reinterpret_cast<const IO*>(raw + 4 * R::row_bytes() + R::col_bytes(cc));
   for (int g = tid; g < tl * cc; g += nthr) {
-    const float L = gate_lamv(to_f32<IO>(rL[g]), gates);
+    const float L = GATED ? gate_lamv(to_f32<IO>(rL[g]), gates) : to_f32<IO>(rL[g]);
     const float Lv = L * to_f32<IO>(rv[g]);
     pj[g] = make_float4(L, L, Lv, Lv);
   }
@@ -153,7 +154,7 @@ inline KernelParams make_params(const ForwardArgs& f, const Plan& p) {
   KernelParams kp{};
   kp.q = f.q; kp.k = f.k; kp.v = f.v; kp.lam_v = f.lam_v; kp.a = f.a; kp.pbar = f.pbar;
   kp.lam0 = f.lam0; kp.eta0 = f.eta0;
-  kp.y = f.y; kp.lamT = f.lamT; kp.etaT = f.etaT;
+  kp.y = f.y; kp.y_var = f.y_var; kp.lamT = f.lamT; kp.etaT = f.etaT;
   kp.T = f.T; kp.dv = f.dv; kp.chunk_len = p.chunk_len; kp.cc = p.cols_per_block;
   int l2 = 0;
   while ((1 << l2) < p.cols_per_block) ++l2;

@@ -8,6 +8,8 @@
 // are Möbius maps that compose associatively, and the information-mean
 // updates are affine, so a long sequence can be cut into chunks whose maps
 // are built independently and then combined.
+#include <type_traits>
+
 #include "kla_common.cuh"
 #include "kla_launch.h"
 
@@ -91,19 +93,27 @@ __global__ void __launch_bounds__(kMaxThreads) kla_compose_kernel(const KernelPa
       const IO* rk = reinterpret_cast<const IO*>(buf) + TC * DK;
       const IO* ra = rk + TC * DK;
       const IO* rp = ra + TC * DK;
-      for (int idx = tid; idx < tl * DK; idx += blockDim.x) {
-        const int t = idx / DK, i = idx % DK;
-        const float kt = to_f32<IO>(rk[idx]);
-        const float xa = to_f32<IO>(ra[idx]);
-        const float at = fmaxf(gate_a(xa, p.gates), kAMin);
-        float* ct = coef + t * 5 * DK + i;
-        ct[0 * DK] = at * at;                                       // a²
-        ct[1 * DK] = gate_pbar(to_f32<IO>(rp[idx]), xa, p.gates);  // p̄
-        ct[2 * DK] = fmaf(kt, kt, kK2Floor);       // k² (floored as in the scan)
-        ct[3 * DK] = kt;                           // k
-        ct[4 * DK] = at;                           // a
-      }
-      column_terms<IO, DK, TC>(buf, pj, p.cc, tl, tid, blockDim.x, p.gates);
+      // (the gate activations are a separate instantiation: no extra work
+      // without them)
+      auto coefficients = [&](auto gated) {
+        constexpr bool GT = decltype(gated)::value;
+        for (int idx = tid; idx < tl * DK; idx += blockDim.x) {
+          const int t = idx / DK, i = idx % DK;
+          const float kt = to_f32<IO>(rk[idx]);
+          const float xa = to_f32<IO>(ra[idx]);
+          const float at = fmaxf(GT ? gate_a(xa, p.gates) : xa, kAMin);
+          const float xp = to_f32<IO>(rp[idx]);
+          float* ct = coef + t * 5 * DK + i;
+          ct[0 * DK] = at * at;                                 // a²
+          ct[1 * DK] = GT ? gate_pbar(xp, xa, p.gates) : xp;   // p̄
+          ct[2 * DK] = fmaf(kt, kt, kK2Floor);                 // k² (floored as in the scan)
+          ct[3 * DK] = kt;                                      // k
+          ct[4 * DK] = at;                                      // a
+        }
+        column_terms<IO, DK, TC, GT>(buf, pj, p.cc, tl, tid, blockDim.x, p.gates);
+      };
+      if (p.gates) coefficients(std::true_type{});
+      else coefficients(std::false_type{});
     }
     __syncthreads();
 

@@ -15,8 +15,9 @@ struct ForwardArgs {
   void* y;
   float *lamT, *etaT;
   int B, H, T, dk, dv;
-  int io;     // IoType
-  int gates;  // kla_gate bits: Λ^v, a, p̄ given as pre-activations
+  int io;      // IoType
+  int gates;   // kla_gate bits: Λ^v, a, p̄ given as pre-activations
+  void* y_var; // variance readout [B,H,T,dv] (scan mode 2), or null
 };
 
 // Launch geometry shared by the planner and the launchers.
@@ -40,7 +41,7 @@ int tile_for(int dk, int io);
 int warp_cols(int dk, int rl);  // columns covered by one warp
 int max_threads();              // largest number of scanning threads in a block
 int producer_warps();           // extra warps per scan block that feed the scanning warps
-size_t forward_smem_bytes(int dk, int rl, int io, int cc, int tile);
+size_t forward_smem_bytes(int dk, int rl, int io, int cc, int tile, int mode = 0);
 size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 
 // Workspace layout for the chunked path (fp32 elements):
@@ -48,10 +49,11 @@ size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 //   starts [S][2][B·H·dk·dv]    chunk-start (P, μ)
 size_t chunk_workspace_bytes(long long elems, int num_chunks);
 
-// ckpt: also store the backward's checkpoints; variance: read out
-// y_var = Σ_i q_i² P_t (into f.y) instead of y, skipping the mean.
+// ckpt: also store the backward's checkpoints. mode 0: y; 1: the variance
+// readout y_var = Σ_i q_i² P_t into f.y instead of y (no mean); 2: both, y
+// into f.y and y_var into f.y_var.
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s,
-                           float* ckpt = nullptr, bool variance = false);
+                           float* ckpt = nullptr, int mode = 0);
 // The scan stores its checkpoints every kScanTile tokens.
 constexpr int kScanTile = 16;
 cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cudaStream_t s);

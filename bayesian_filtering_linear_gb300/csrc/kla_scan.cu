@@ -50,6 +50,8 @@
 // (A, B, 1/a, k/K, q) are computed once per (t, i) and serve all CC columns;
 // the per-column terms (Λ^v, Λ^v v) once per (t, j) for all d_k rows.
 // ---------------------------------------------------------------------------
+#include <type_traits>
+
 #include "kla_common.cuh"
 #include "kla_launch.h"
 
@@ -64,17 +66,19 @@ constexpr int kBarEmpty0 = 3;     // 3, 4: the scan is done with buffer 0 / 1
 constexpr int kBarProducers = 5;  // producer warps only (staged raw tile visible)
 
 // Byte offsets of the double-buffered shared-memory regions of one block.
-template <typename IO, int DK, int TC, int NP>
+template <typename IO, int DK, int TC, int NP, int NC = 5, int NOUT = 1>
 struct ScanLayout {
   int cc;
+  // NC per-row coefficients per token; NOUT readouts (y, and y_var with both).
   __host__ __device__ explicit ScanLayout(int cc_) : cc(cc_) {}
   __host__ __device__ size_t raw_bytes() const { return RawTile<IO, DK, TC>::bytes(cc); }
-  __host__ __device__ size_t coef_bytes() const { return (size_t)TC * 5 * DK * sizeof(float); }
+  __host__ __device__ size_t coef_bytes() const { return (size_t)TC * NC * DK * sizeof(float); }
   __host__ __device__ size_t pj_bytes() const { return (size_t)TC * cc * sizeof(float4); }
   // Partial sums, token-major per (partial, column): [NP][cc][TC + 4] (the
   // padding keeps 128-bit stores of four tokens free of bank conflicts).
   static constexpr int TCP = TC + 4;
-  __host__ __device__ size_t ypart_bytes() const { return (size_t)cc * NP * TCP * sizeof(float); }
+  __host__ __device__ size_t ypart_out() const { return (size_t)cc * NP * TCP; }  // floats per readout
+  __host__ __device__ size_t ypart_bytes() const { return NOUT * ypart_out() * sizeof(float); }
   __host__ __device__ size_t raw(int b) const { return b * raw_bytes(); }
   __host__ __device__ size_t coef(int b) const { return 2 * raw_bytes() + b * coef_bytes(); }
   __host__ __device__ size_t pj(int b) const { return coef(2) + b * pj_bytes(); }
@@ -84,10 +88,11 @@ struct ScanLayout {
 };
 
 // Per-(t, i) row coefficients of a staged tile, four rows per thread:
-// coef[t][0..4][i] = (A, B, 1/a, k/K, q), or with VAR (the variance readout)
-// the last one is q²/K. kp_cur holds K of the row before the tile (1 at a
-// chunk start); K of the tile's last row goes to kp_nxt.
-template <typename IO, int DK, int TC, bool VAR = false>
+// coef[t][0..4][i] = (A, B, 1/a, k/K, q); MODE 1 (variance readout only) has
+// q²/K in place of q, MODE 2 (both readouts) adds q²/K as coef[t][5][i].
+// kp_cur holds K of the row before the tile (1 at a chunk start); K of the
+// tile's last row goes to kp_nxt.
+template <typename IO, int DK, int TC, int MODE = 0, bool GATED = false>
 __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float* coef, const float* kp_cur,
                                                  float* kp_nxt, int tl, int tid, int nthr, int gates) {
   using R = RawTile<IO, DK, TC>;
@@ -113,8 +118,8 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
     float A[4], B[4], AI[4], KI[4], Kt[4], QV[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float at = fmaxf(gate_a(av[u], gates), kAMin);
-      const float pbu = gate_pbar(pv[u], av[u], gates);
+      const float at = fmaxf(GATED ? gate_a(av[u], gates) : av[u], kAMin);
+      const float pbu = GATED ? gate_pbar(pv[u], av[u], gates) : pv[u];
       Kt[u] = fmaf(kv[u], kv[u], kK2Floor);
       const float aK = at * Kt[u];
       const float r = rcp_approx(aK * kpv[u]);  // 1 / (a K_t K_{t-1})
@@ -123,14 +128,19 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
       B[u] = (Kt[u] * pbu) * AI[u];             // K_t p̄ / a
       const float rK = at * kpv[u] * r;         // 1 / K_t
       KI[u] = kv[u] * rK;                       // k / K_t
-      QV[u] = VAR ? qv[u] * qv[u] * rK : qv[u];  // q²/K_t (variance readout) or q
+      QV[u] = qv[u] * qv[u] * rK;               // q²/K_t (variance readout)
     }
-    float* ct = coef + t * 5 * DK + i;
+    constexpr int NC = MODE == 2 ? 6 : 5;
+    float* ct = coef + t * NC * DK + i;
     *reinterpret_cast<float4*>(ct + 0 * DK) = make_float4(A[0], A[1], A[2], A[3]);
     *reinterpret_cast<float4*>(ct + 1 * DK) = make_float4(B[0], B[1], B[2], B[3]);
     *reinterpret_cast<float4*>(ct + 2 * DK) = make_float4(AI[0], AI[1], AI[2], AI[3]);
     *reinterpret_cast<float4*>(ct + 3 * DK) = make_float4(KI[0], KI[1], KI[2], KI[3]);
-    *reinterpret_cast<float4*>(ct + 4 * DK) = make_float4(QV[0], QV[1], QV[2], QV[3]);
+    if (MODE == 1)
+      *reinterpret_cast<float4*>(ct + 4 * DK) = make_float4(QV[0], QV[1], QV[2], QV[3]);
+    else
+      *reinterpret_cast<float4*>(ct + 4 * DK) = q4;
+    if (MODE == 2) *reinterpret_cast<float4*>(ct + 5 * DK) = make_float4(QV[0], QV[1], QV[2], QV[3]);
     if (t == tl - 1) *reinterpret_cast<float4*>(kp_nxt + i) = make_float4(Kt[0], Kt[1], Kt[2], Kt[3]);
   }
 }
@@ -160,14 +170,17 @@ __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, in
   }
 }
 
-// VAR: the variance readout y_var[t, j] = Σ_i q_i² P_t[i, j] instead of y (the
-// mean recursion is skipped; y points at y_var).
-template <typename IO, int DK, int RL, int TC, bool VAR = false>
+// MODE 0: y. MODE 1: the variance readout y_var[t, j] = Σ_i q_i² P_t[i, j]
+// instead of y (the mean recursion is skipped; y points at y_var). MODE 2:
+// both, y into p.y and y_var into p.y_var.
+template <typename IO, int DK, int RL, int TC, int MODE = 0>
 __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_kernel(const KernelParams p) {
   using G = Geo<DK, RL>;
   constexpr int NPR = RL / 2;  // row pairs per lane
+  constexpr bool VAR = MODE == 1;
+  constexpr int NC = MODE == 2 ? 6 : 5, NOUT = MODE == 2 ? 2 : 1;
   extern __shared__ __align__(16) unsigned char smem[];
-  const ScanLayout<IO, DK, TC, G::NP> L(p.cc);
+  const ScanLayout<IO, DK, TC, G::NP, NC, NOUT> L(p.cc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Warps [0, ncons) scan; the last kProducerWarps warps stage raw tiles,
@@ -193,6 +206,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
   for (int r = 0; r < G::XR; ++r) swz |= ((li >> r) & 1) << (kLogCL - 1 - r);
   const size_t E = (size_t)DK * p.dv;
   IO* ybase = reinterpret_cast<IO*>(p.y) + ((size_t)bh * p.T) * p.dv + jb;
+  IO* yvbase = reinterpret_cast<IO*>(p.y_var) + ((size_t)bh * p.T) * p.dv + jb;
   auto tile_len = [&](int n) { return min(TC, t_end - (t_begin + n * TC)); };
 
   if (warp >= ncons) {
@@ -200,14 +214,21 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
     const int ptid = tid - 32 * ncons, pn = 32 * kProducerWarps;
     float* kp0 = reinterpret_cast<float*>(smem + L.kprev(0));
     for (int i = ptid; i < DK; i += pn) kp0[i] = 1.0f;
-    auto build = [&](int m) {  // coefficients of tile m into buffer m % 2
+    // coefficients of tile m into buffer m % 2; the gate activations are a
+    // separate instantiation so that ungated producers carry no extra work
+    auto build_tile = [&](auto gated, int m) {
+      constexpr bool GT = decltype(gated)::value;
       const int bm = m & 1;
-      row_coefficients<IO, DK, TC, VAR>(smem + L.raw(bm), reinterpret_cast<float*>(smem + L.coef(bm)),
-                                   reinterpret_cast<const float*>(smem + L.kprev(bm)),
-                                   reinterpret_cast<float*>(smem + L.kprev(bm ^ 1)), tile_len(m), ptid, pn,
-                                   p.gates);
-      column_terms<IO, DK, TC>(smem + L.raw(bm), reinterpret_cast<float4*>(smem + L.pj(bm)), p.cc, tile_len(m),
-                               ptid, pn, p.gates);
+      row_coefficients<IO, DK, TC, MODE, GT>(smem + L.raw(bm), reinterpret_cast<float*>(smem + L.coef(bm)),
+                                             reinterpret_cast<const float*>(smem + L.kprev(bm)),
+                                             reinterpret_cast<float*>(smem + L.kprev(bm ^ 1)), tile_len(m), ptid, pn,
+                                             p.gates);
+      column_terms<IO, DK, TC, GT>(smem + L.raw(bm), reinterpret_cast<float4*>(smem + L.pj(bm)), p.cc,
+                                   tile_len(m), ptid, pn, p.gates);
+    };
+    auto build = [&](int m) {
+      if (p.gates) build_tile(std::true_type{}, m);
+      else build_tile(std::false_type{}, m);
     };
     stage_raw<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, tile_len(0), ptid, pn);
     cp_async_commit();
@@ -232,6 +253,9 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
       if (p.y)
         store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
                                       ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
+      if (MODE == 2)
+        store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)) + L.ypart_out(),
+                                      yvbase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
       if (n + 2 < ntiles) {
         cp_async_wait<0>();
         named_sync(kBarProducers, pn);
@@ -297,22 +321,31 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
       // partial sums each time; after XR rounds a lane holds registers
       // 0..VALS-1, the sums over 2^XR row groups of columns cl0 + (u ^ swz)
       // (with VALS = 1: column cl0 + swz).
+      // Readout o (0: y or, in MODE 1, y_var; 1: y_var in MODE 2) goes to
+      // ypart + o·ypart_out().
       float* __restrict__ ydst = ypart + ((size_t)(li >> G::XR) * p.cc + cl0 + swz) * L.TCP;
+      constexpr int NV = NOUT * G::VALS;  // partial sums a lane stores per token
       auto exchange = [&](const float* yc, float* ex) {
-        float v[CL];
 #pragma unroll
-        for (int c = 0; c < CL; ++c) v[c] = yc[c];
+        for (int o = 0; o < NOUT; ++o) {
+          float v[CL];
 #pragma unroll
-        for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) {
+          for (int c = 0; c < CL; ++c) v[c] = yc[o * CL + c];
 #pragma unroll
-          for (int u = 0; u < nv / 2; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u + nv / 2], G::LANES_J << r);
+          for (int r = 0, nv = CL; r < G::XR; ++r, nv /= 2) {
+#pragma unroll
+            for (int u = 0; u < nv / 2; ++u) v[u] += __shfl_xor_sync(0xffffffffu, v[u + nv / 2], G::LANES_J << r);
+          }
+#pragma unroll
+          for (int u = 0; u < G::VALS; ++u) ex[o * G::VALS + u] = v[u];
         }
-#pragma unroll
-        for (int u = 0; u < G::VALS; ++u) ex[u] = v[u];
       };
-      f2 A[NPR], Bc[NPR], AI[NPR], KI[NPR], Q[NPR], L2[CL], V2[CL];
+      auto slot = [&](int v) -> float* {  // destination of stored value v
+        return ydst + (size_t)(v / G::VALS) * L.ypart_out() + (size_t)(v % G::VALS) * L.TCP;
+      };
+      f2 A[NPR], Bc[NPR], AI[NPR], KI[NPR], Q[NPR], QV[NPR], L2[CL], V2[CL];
       auto load_coef = [&](int t) {
-        const float* ct = coef + t * 5 * DK;
+        const float* ct = coef + t * NC * DK;
 #pragma unroll
         for (int m = 0; m < NPR / 2; ++m) {
           const ulonglong2 a4 = *reinterpret_cast<const ulonglong2*>(ct + 0 * DK + 4 * m);
@@ -325,6 +358,10 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
           AI[2 * m] = i4.x; AI[2 * m + 1] = i4.y;
           KI[2 * m] = k4.x; KI[2 * m + 1] = k4.y;
           Q[2 * m] = q4.x;  Q[2 * m + 1] = q4.y;
+          if constexpr (MODE == 2) {
+            const ulonglong2 v4 = *reinterpret_cast<const ulonglong2*>(ct + 5 * DK + 4 * m);
+            QV[2 * m] = v4.x; QV[2 * m + 1] = v4.y;
+          }
         }
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
@@ -332,10 +369,11 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
           L2[c] = lv.x; V2[c] = lv.y;
         }
       };
+      // yc[c]: readout 0 of column register c; yc[CL + c]: readout 1 (MODE 2)
       auto compute = [&](float* yc) {
 #pragma unroll
         for (int c = 0; c < CL; ++c) {
-          f2 y2 = f2_make(0.0f, 0.0f);
+          f2 y2 = f2_make(0.0f, 0.0f), yv2 = f2_make(0.0f, 0.0f);
 #pragma unroll
           for (int r = 0; r < NPR; ++r) {
             const f2 s = f2_fma(A[r], Pt[r][c], Bc[r]);
@@ -349,9 +387,11 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
               const f2 m = f2_fma(g, KI[r], Mu[r][c]);
               Mu[r][c] = f2_mul(m, w);
               y2 = f2_fma(Q[r], Mu[r][c], y2);
+              if constexpr (MODE == 2) yv2 = f2_fma(QV[r], Pt[r][c], yv2);
             }
           }
           yc[c] = f2_lo(y2) + f2_hi(y2);
+          if constexpr (MODE == 2) yc[CL + c] = f2_lo(yv2) + f2_hi(yv2);
         }
       };
       if (tl == TC) {
@@ -360,10 +400,10 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
         // 128-bit store per value, so no store waits on a fresh result.
         // (Unrolled by two batches so that pb/cur are renamed, not copied: a
         // register move would cost a slot on the busy FMA pipe.)
-        float pb[4][CL];
+        float pb[4][NOUT * CL];
 #pragma unroll 2
         for (int t4 = 0; t4 < TC; t4 += 4) {
-          float cur[4][CL], ex[4][G::VALS];
+          float cur[4][NOUT * CL], ex[4][NV];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             load_coef(t4 + u);
@@ -372,31 +412,29 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
           }
           if (t4 > 0) {
 #pragma unroll
-            for (int v = 0; v < G::VALS; ++v)
-              *reinterpret_cast<float4*>(ydst + (size_t)v * L.TCP + t4 - 4) =
-                  make_float4(ex[0][v], ex[1][v], ex[2][v], ex[3][v]);
+            for (int v = 0; v < NV; ++v)
+              *reinterpret_cast<float4*>(slot(v) + t4 - 4) = make_float4(ex[0][v], ex[1][v], ex[2][v], ex[3][v]);
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int c = 0; c < CL; ++c) pb[u][c] = cur[u][c];
+            for (int c = 0; c < NOUT * CL; ++c) pb[u][c] = cur[u][c];
         }
-        float ex[4][G::VALS];
+        float ex[4][NV];
 #pragma unroll
         for (int u = 0; u < 4; ++u) exchange(pb[u], ex[u]);
 #pragma unroll
-        for (int v = 0; v < G::VALS; ++v)
-          *reinterpret_cast<float4*>(ydst + (size_t)v * L.TCP + TC - 4) =
-              make_float4(ex[0][v], ex[1][v], ex[2][v], ex[3][v]);
+        for (int v = 0; v < NV; ++v)
+          *reinterpret_cast<float4*>(slot(v) + TC - 4) = make_float4(ex[0][v], ex[1][v], ex[2][v], ex[3][v]);
       } else {
         // Ragged last tile: one token at a time.
         for (int t = 0; t < tl; ++t) {
-          float yc[CL], ex[G::VALS];
+          float yc[NOUT * CL], ex[NV];
           load_coef(t);
           compute(yc);
           exchange(yc, ex);
 #pragma unroll
-          for (int v = 0; v < G::VALS; ++v) ydst[(size_t)v * L.TCP + t] = ex[v];
+          for (int v = 0; v < NV; ++v) slot(v)[t] = ex[v];
         }
       }
     }
@@ -459,58 +497,62 @@ int warp_cols(int dk, int rl) { return (32 / (dk / rl)) * CL; }
 
 namespace {
 template <typename IO, int DK, int RL>
-size_t scan_smem(int cc) {
-  return ScanLayout<IO, DK, kTile, Geo<DK, RL>::NP>(cc).total();
+size_t scan_smem(int cc, int mode) {
+  using G = Geo<DK, RL>;
+  return mode == 2 ? ScanLayout<IO, DK, kTile, G::NP, 6, 2>(cc).total() : ScanLayout<IO, DK, kTile, G::NP>(cc).total();
 }
 template <typename IO>
-size_t scan_smem_io(int dk, int rl, int cc) {
+size_t scan_smem_io(int dk, int rl, int cc, int mode) {
   switch (dk * 16 + rl) {
-    case 16 * 16 + 4: return scan_smem<IO, 16, 4>(cc);
-    case 32 * 16 + 4: return scan_smem<IO, 32, 4>(cc);
-    case 64 * 16 + 4: return scan_smem<IO, 64, 4>(cc);
-    case 64 * 16 + 8: return scan_smem<IO, 64, 8>(cc);
-    case 128 * 16 + 4: return scan_smem<IO, 128, 4>(cc);
-    case 128 * 16 + 8: return scan_smem<IO, 128, 8>(cc);
+    case 16 * 16 + 4: return scan_smem<IO, 16, 4>(cc, mode);
+    case 32 * 16 + 4: return scan_smem<IO, 32, 4>(cc, mode);
+    case 64 * 16 + 4: return scan_smem<IO, 64, 4>(cc, mode);
+    case 64 * 16 + 8: return scan_smem<IO, 64, 8>(cc, mode);
+    case 128 * 16 + 4: return scan_smem<IO, 128, 4>(cc, mode);
+    case 128 * 16 + 8: return scan_smem<IO, 128, 8>(cc, mode);
     default: return 0;
   }
 }
-template <typename IO, bool VAR>
-cudaError_t scan_dispatch_v(int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
+template <typename IO, int MODE>
+cudaError_t scan_dispatch_m(int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
                             const KernelParams& kp) {
   switch (dk * 16 + rl) {
-    case 16 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 16, 4, kTile, VAR>, grid, threads, smem, s, kp);
-    case 32 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 32, 4, kTile, VAR>, grid, threads, smem, s, kp);
-    case 64 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 64, 4, kTile, VAR>, grid, threads, smem, s, kp);
-    case 64 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 64, 8, kTile, VAR>, grid, threads, smem, s, kp);
-    case 128 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 128, 4, kTile, VAR>, grid, threads, smem, s, kp);
-    case 128 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 128, 8, kTile, VAR>, grid, threads, smem, s, kp);
+    case 16 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 16, 4, kTile, MODE>, grid, threads, smem, s, kp);
+    case 32 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 32, 4, kTile, MODE>, grid, threads, smem, s, kp);
+    case 64 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 64, 4, kTile, MODE>, grid, threads, smem, s, kp);
+    case 64 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 64, 8, kTile, MODE>, grid, threads, smem, s, kp);
+    case 128 * 16 + 4: return launch_kernel(kla_scan_kernel<IO, 128, 4, kTile, MODE>, grid, threads, smem, s, kp);
+    case 128 * 16 + 8: return launch_kernel(kla_scan_kernel<IO, 128, 8, kTile, MODE>, grid, threads, smem, s, kp);
     default: return cudaErrorInvalidValue;
   }
 }
 template <typename IO>
-cudaError_t scan_dispatch(int dk, int rl, bool var, dim3 grid, int threads, size_t smem, cudaStream_t s,
+cudaError_t scan_dispatch(int dk, int rl, int mode, dim3 grid, int threads, size_t smem, cudaStream_t s,
                           const KernelParams& kp) {
-  return var ? scan_dispatch_v<IO, true>(dk, rl, grid, threads, smem, s, kp)
-             : scan_dispatch_v<IO, false>(dk, rl, grid, threads, smem, s, kp);
+  switch (mode) {
+    case 0: return scan_dispatch_m<IO, 0>(dk, rl, grid, threads, smem, s, kp);
+    case 1: return scan_dispatch_m<IO, 1>(dk, rl, grid, threads, smem, s, kp);
+    default: return scan_dispatch_m<IO, 2>(dk, rl, grid, threads, smem, s, kp);
+  }
 }
 }  // namespace
 
-size_t forward_smem_bytes(int dk, int rl, int io, int cc, int /*tile*/) {
-  return io == IO_BF16 ? scan_smem_io<__nv_bfloat16>(dk, rl, cc) : scan_smem_io<float>(dk, rl, cc);
+size_t forward_smem_bytes(int dk, int rl, int io, int cc, int /*tile*/, int mode) {
+  return io == IO_BF16 ? scan_smem_io<__nv_bfloat16>(dk, rl, cc, mode) : scan_smem_io<float>(dk, rl, cc, mode);
 }
 
 static_assert(kTile == kScanTile, "checkpoints are taken once per tile");
 
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s, float* ckpt,
-                           bool variance) {
+                           int mode) {
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
   kp.ckpt = ckpt;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
   const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, p.rows_per_lane) + kProducerWarps);
-  const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile);
-  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, p.rows_per_lane, variance, grid, threads, smem, s, kp)
-                         : scan_dispatch<float>(f.dk, p.rows_per_lane, variance, grid, threads, smem, s, kp);
+  const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile, mode);
+  return f.io == IO_BF16 ? scan_dispatch<__nv_bfloat16>(f.dk, p.rows_per_lane, mode, grid, threads, smem, s, kp)
+                         : scan_dispatch<float>(f.dk, p.rows_per_lane, mode, grid, threads, smem, s, kp);
 }
 
 }  // namespace kla

@@ -24,7 +24,7 @@ namespace {
 
 constexpr int kRowsPerThread = 4;
 
-template <typename IO>
+template <typename IO, bool GATED>
 __global__ void __launch_bounds__(1024) kla_step_kernel(const StepArgs a) {
   extern __shared__ __align__(16) float ysm[];  // [row groups][dv] partial sums
   const int dk = a.dk, dv = a.dv;
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(1024) kla_step_kernel(const StepArgs a) {
   float Lc[4], Bv[4], y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    Lc[c] = gate_lamv(to_f32<IO>(lv[j0 + c]), a.gates);
+    Lc[c] = GATED ? gate_lamv(to_f32<IO>(lv[j0 + c]), a.gates) : to_f32<IO>(lv[j0 + c]);
     Bv[c] = Lc[c] * to_f32<IO>(vv[j0 + c]);
   }
   float* lam = a.lam + (size_t)bh * dk * dv;
@@ -54,8 +54,8 @@ __global__ void __launch_bounds__(1024) kla_step_kernel(const StepArgs a) {
     const int i = r0 + rr;
     const float ki = to_f32<IO>(kv[i]);
     const float xa = to_f32<IO>(av[i]);
-    const float ai = fmaxf(gate_a(xa, a.gates), kAMin);
-    const float pi = gate_pbar(to_f32<IO>(pv[i]), xa, a.gates);
+    const float ai = fmaxf(GATED ? gate_a(xa, a.gates) : xa, kAMin);
+    const float pi = GATED ? gate_pbar(to_f32<IO>(pv[i]), xa, a.gates) : to_f32<IO>(pv[i]);
     const float qi = to_f32<IO>(qv[i]);
     const float K = fmaf(ki, ki, kK2Floor);
     const float a2 = ai * ai;
@@ -93,10 +93,13 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
   if (heads == 0) return cudaSuccess;
   const int threads = (a.dv / 4) * (a.dk / kRowsPerThread);
   const size_t smem = (size_t)(a.dk / kRowsPerThread) * a.dv * sizeof(float);
+  // gate activations are a separate instantiation (no extra work without them)
   if (a.io == IO_BF16) {
-    kla_step_kernel<__nv_bfloat16><<<(unsigned)heads, threads, smem, s>>>(a);
+    if (a.gates) kla_step_kernel<__nv_bfloat16, true><<<(unsigned)heads, threads, smem, s>>>(a);
+    else kla_step_kernel<__nv_bfloat16, false><<<(unsigned)heads, threads, smem, s>>>(a);
   } else {
-    kla_step_kernel<float><<<(unsigned)heads, threads, smem, s>>>(a);
+    if (a.gates) kla_step_kernel<float, true><<<(unsigned)heads, threads, smem, s>>>(a);
+    else kla_step_kernel<float, false><<<(unsigned)heads, threads, smem, s>>>(a);
   }
   return cudaGetLastError();
 }
