@@ -405,6 +405,24 @@ size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv) {
   return b.ckpt_bytes + b.rowpart_bytes;
 }
 
+kla_status kla_backward_plan_for_sms(int B, int H, int T, int dk, int dv, int num_sms,
+                                     kla_backward_plan_info* out) {
+  if (!out) return KLA_ERR_INVALID_ARG;
+  const kla_status st = check_shape(B, H, T, dk, dv);
+  if (st != KLA_OK) return st;
+  if (num_sms < 1) return KLA_ERR_INVALID_ARG;
+  *out = kla_backward_plan_info{};
+  const long long bh = (long long)B * H;
+  if (bh == 0) return KLA_OK;
+  const kla::BwdPlan b = kla::backward_plan(bh, T, dk, dv, num_sms);
+  out->cols_per_block = b.cc;
+  out->cols_per_lane = b.cpl;
+  out->threads = b.threads;
+  out->column_blocks = b.ncb;
+  out->workspace_bytes = b.ckpt_bytes + b.rowpart_bytes;
+  return KLA_OK;
+}
+
 kla_status kla_backward(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
                         const void* pbar, const float* lam0, const float* eta0, const void* gy,
                         const float* glamT, const float* getaT, void* gq, void* gk, void* gv, void* glam_v,

@@ -25,13 +25,15 @@
 //  2. kla_bwd_kernel walks the chunks from last to first, each in sub-chunks
 //     of kSub tokens from its end: it re-runs the forward from the chunk's
 //     checkpoint to the sub-chunk, keeps the states before the sub-chunk's
-//     tokens in registers, and runs the adjoint recursion back over them
-//     (forward work per token: about 2.5 steps, no state traffic to memory).
+//     tokens in shared memory, and runs the adjoint recursion back over them
+//     (forward work per token: 2.25 steps besides the adjoint's own, no state
+//     traffic to device memory).
 //  3. kla_bwd_finish_kernel (only when a head's columns are split over
 //     several blocks) adds the per-row partial sums of the blocks.
 //
 // Layout of a block: (head, column block of cc columns, all d_k rows). A lane
-// owns one row and kCpl = 8 consecutive columns (four fp32x2 pairs), so every
+// owns one row and CPL = 8 (or, for few heads, 4) consecutive columns (fp32x2
+// pairs), so every
 // per-row sum (dq, dk, da, dp̄) is first a sum inside the lane; a warp covers
 // RW = min(32, d_k) rows and 32/RW column groups; per-column sums (dv, dΛ^v)
 // over the warp's rows are a butterfly reduce-scatter across its lanes. Sums
@@ -48,7 +50,7 @@ namespace kla {
 namespace {
 
 constexpr int kChunk = 16;  // tokens per checkpoint interval and per staged tile
-constexpr int kCpl = 8;     // columns per lane
+constexpr int kCpl = 8;     // columns per lane (4 when a block of 8 would have few warps)
 constexpr int kSub = 4;     // tokens per reverse sub-chunk (states kept in shared memory)
 static_assert(kChunk == kScanTile, "the forward scan checkpoints once per tile");
 
@@ -78,12 +80,12 @@ struct BwdGeo {
 // [kChunk][DK] and per-column inputs v, Λ^v, Λ^v·v, dy [kChunk][cc], the
 // per-token accumulators of the row sums [kChunk][4][DK] and column sums
 // [kChunk][2][cc], and each thread's states before the tokens of the current
-// sub-chunk, [kSub][2][kCpl/2][threads] fp32x2 (thread-fastest, so a warp's
+// sub-chunk, [kSub][2][cpl/2][threads] fp32x2 (thread-fastest, so a warp's
 // accesses are contiguous).
 struct BwdSmem {
   float *q, *k, *a, *p, *v, *L, *Lv, *dy, *racc, *cacc, *st;
   unsigned char* raw;  // the next chunk's inputs as loaded (I/O dtype), filled by cp.async
-  __device__ BwdSmem(float* base, int dk, int cc) {
+  __device__ BwdSmem(float* base, int dk, int cc, int cpl) {
     q = base;
     k = q + kChunk * dk;
     a = k + kChunk * dk;
@@ -95,11 +97,11 @@ struct BwdSmem {
     racc = dy + kChunk * cc;
     cacc = racc + kChunk * 4 * dk;
     st = cacc + kChunk * 2 * cc;
-    raw = reinterpret_cast<unsigned char*>(st + kSub * 2 * kCpl * (int)blockDim.x);
+    raw = reinterpret_cast<unsigned char*>(st + kSub * 2 * cpl * (int)blockDim.x);
   }
-  __host__ __device__ static size_t bytes(int dk, int cc, int threads) {
+  __host__ __device__ static size_t bytes(int dk, int cc, int threads, int cpl) {
     return sizeof(float) * ((size_t)kChunk * (4 * dk + 4 * cc) + (size_t)kChunk * 4 * dk + (size_t)kChunk * 2 * cc +
-                            (size_t)kSub * 2 * kCpl * threads + (size_t)kChunk * (4 * dk + 3 * cc));
+                            (size_t)kSub * 2 * cpl * threads + (size_t)kChunk * (4 * dk + 3 * cc));
   }
 };
 
@@ -213,11 +215,11 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane, int& fi
 // over pairs of adjacent columns.
 
 template <typename IO, int DK, int CPL>
-__global__ void __launch_bounds__(512) kla_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
   using G = BwdGeo<DK, CPL>;
   constexpr int NP = CPL / 2;  // column pairs per lane
   extern __shared__ __align__(16) float bwd_smem[];
-  const BwdSmem s(bwd_smem, DK, p.cc);
+  const BwdSmem s(bwd_smem, DK, p.cc, CPL);
   const long long bh = blockIdx.x;
   const int jb = blockIdx.y * p.cc;
   const BwdLane<DK, CPL> ln(p, bh, jb);
@@ -488,12 +490,16 @@ cudaError_t launch_bwd_typed(const BwdParams& bp, dim3 grid, int threads, size_t
 }
 
 template <typename IO>
-cudaError_t launch_bwd_io(int dk, const BwdParams& bp, dim3 grid, int threads, size_t smem, cudaStream_t s) {
-  switch (dk) {
-    case 16: return launch_bwd_typed<IO, 16, kCpl>(bp, grid, threads, smem, s);
-    case 32: return launch_bwd_typed<IO, 32, kCpl>(bp, grid, threads, smem, s);
-    case 64: return launch_bwd_typed<IO, 64, kCpl>(bp, grid, threads, smem, s);
-    case 128: return launch_bwd_typed<IO, 128, kCpl>(bp, grid, threads, smem, s);
+cudaError_t launch_bwd_io(int dk, int cpl, const BwdParams& bp, dim3 grid, int threads, size_t smem, cudaStream_t s) {
+  switch (dk * 16 + cpl) {
+    case 16 * 16 + 8: return launch_bwd_typed<IO, 16, 8>(bp, grid, threads, smem, s);
+    case 32 * 16 + 8: return launch_bwd_typed<IO, 32, 8>(bp, grid, threads, smem, s);
+    case 64 * 16 + 8: return launch_bwd_typed<IO, 64, 8>(bp, grid, threads, smem, s);
+    case 128 * 16 + 8: return launch_bwd_typed<IO, 128, 8>(bp, grid, threads, smem, s);
+    case 16 * 16 + 4: return launch_bwd_typed<IO, 16, 4>(bp, grid, threads, smem, s);
+    case 32 * 16 + 4: return launch_bwd_typed<IO, 32, 4>(bp, grid, threads, smem, s);
+    case 64 * 16 + 4: return launch_bwd_typed<IO, 64, 4>(bp, grid, threads, smem, s);
+    case 128 * 16 + 4: return launch_bwd_typed<IO, 128, 4>(bp, grid, threads, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -501,26 +507,49 @@ cudaError_t launch_bwd_io(int dk, const BwdParams& bp, dim3 grid, int threads, s
 }  // namespace
 
 BwdPlan backward_plan(long long bh, int T, int dk, int dv, int num_sms) {
-  BwdPlan b{};
-  b.cpl = kCpl;
-  const int rw = dk < 32 ? dk : 32, wcols = (32 / rw) * kCpl, nwr = dk / rw;
   constexpr int kMaxWarps = 16;  // 512 threads at the reverse kernel's register budget
   constexpr size_t kMaxSmem = 220 * 1024;
-  int cc = dv;
-  while (cc > wcols &&
-         (nwr * (cc / wcols) > kMaxWarps || BwdSmem::bytes(dk, cc, 32 * nwr * (cc / wcols)) > kMaxSmem))
-    cc /= 2;
-  // Few heads: narrower column blocks, so that at least half the SMs get a
-  // block (a block of up to 16 warps keeps an SM busy on its own).
-  while (cc > wcols && 2 * bh * (dv / cc) < num_sms) cc /= 2;
-  b.cc = cc;
-  b.threads = 32 * nwr * (cc / wcols);
-  b.ncb = dv / cc;
+  const int rw = dk < 32 ? dk : 32, nwr = dk / rw;
+  // Column block and threads for `cpl` columns per lane.
+  auto geometry = [&](int cpl) {
+    BwdPlan b{};
+    b.cpl = cpl;
+    const int wcols = (32 / rw) * cpl;
+    int cc = dv;
+    while (cc > wcols &&
+           (nwr * (cc / wcols) > kMaxWarps || BwdSmem::bytes(dk, cc, 32 * nwr * (cc / wcols), cpl) > kMaxSmem))
+      cc /= 2;
+    // Few heads: narrower column blocks, so that at least half the SMs get a
+    // block (a block of up to 16 warps keeps an SM busy on its own).
+    while (cc > wcols && 2 * bh * (dv / cc) < num_sms) cc /= 2;
+    b.cc = cc;
+    b.threads = 32 * nwr * (cc / wcols);
+    b.smem = BwdSmem::bytes(dk, cc, b.threads, cpl);
+    return b;
+  };
+  // Warps an SM holds at once: blocks per SM (as many as there are per SM,
+  // within the shared-memory, thread and register limits) × warps per block.
+  auto resident_warps = [&](const BwdPlan& b) {
+    const long long blocks = bh * (dv / b.cc);
+    const long long per_sm = (blocks + num_sms - 1) / num_sms;
+    const long long by_smem = (long long)((228 * 1024) / (b.smem + 1024));
+    const long long by_threads = 2048 / b.threads, by_regs = 65536 / (128LL * b.threads);
+    const long long r = std::max(1LL, std::min(std::min(per_sm, by_smem), std::min(by_threads, by_regs)));
+    return r * (b.threads / 32);
+  };
+  // Eight columns per lane amortise the per-row work best; four columns
+  // double the warps of a block, which pays when eight would leave the SMs
+  // with few warps to hide latency with (few heads).
+  BwdPlan b = geometry(kCpl);
+  if (resident_warps(b) < kMaxWarps) {
+    const BwdPlan b4 = geometry(kCpl / 2);
+    if (resident_warps(b4) > resident_warps(b)) b = b4;
+  }
+  b.ncb = dv / b.cc;
   b.nchunks = (T + kChunk - 1) / kChunk;
   const long long elems = bh * dk * dv;
   b.ckpt_bytes = (size_t)(b.nchunks + 1) * 2 * (size_t)elems * sizeof(float);
   b.rowpart_bytes = b.ncb > 1 ? (size_t)4 * (size_t)bh * T * dk * sizeof(float) : 0;
-  b.smem = BwdSmem::bytes(dk, cc, b.threads);
   return b;
 }
 
@@ -539,8 +568,8 @@ cudaError_t launch_backward(const BackwardArgs& f, const BwdPlan& b, void* works
   bp.elems = bh * f.dk * f.dv;
   bp.gates = f.gates;
   const dim3 grid((unsigned)bh, (unsigned)b.ncb);
-  return f.io == IO_BF16 ? launch_bwd_io<__nv_bfloat16>(f.dk, bp, grid, b.threads, b.smem, s)
-                         : launch_bwd_io<float>(f.dk, bp, grid, b.threads, b.smem, s);
+  return f.io == IO_BF16 ? launch_bwd_io<__nv_bfloat16>(f.dk, b.cpl, bp, grid, b.threads, b.smem, s)
+                         : launch_bwd_io<float>(f.dk, b.cpl, bp, grid, b.threads, b.smem, s);
 }
 
 }  // namespace kla

@@ -70,7 +70,7 @@ struct KernelParams {
   void* y;              // nullptr: y is not stored (checkpoint pass of the backward)
   void* y_var;          // the variance readout when the scan computes both readouts
   float *lamT, *etaT;
-  float* ckpt;          // scan only, or nullptr: [T/16 + 1][2][elems] scaled states (P̃, μ)
+  float* ckpt;          // scan MODE 3 only: [T/16 + 1][2][elems] scaled states (P̃, μ)
                         // at every 16-token tile start and at the end
   int T, dv, chunk_len, cc, log2cc;
   int gates;        // kla_gate bits

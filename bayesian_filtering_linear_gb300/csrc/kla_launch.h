@@ -49,9 +49,10 @@ size_t compose_smem_bytes(int dk, int io, int cc, int tile);
 //   starts [S][2][B·H·dk·dv]    chunk-start (P, μ)
 size_t chunk_workspace_bytes(long long elems, int num_chunks);
 
-// ckpt: also store the backward's checkpoints. mode 0: y; 1: the variance
-// readout y_var = Σ_i q_i² P_t into f.y instead of y (no mean); 2: both, y
-// into f.y and y_var into f.y_var.
+// mode 0: y; 1: the variance readout y_var = Σ_i q_i² P_t into f.y instead
+// of y (no mean); 2: both, y into f.y and y_var into f.y_var. With ckpt (a
+// sequential plan only) the scan runs without a readout and stores the
+// backward's checkpoints there instead (mode is then ignored).
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s,
                            float* ckpt = nullptr, int mode = 0);
 // The scan stores its checkpoints every kScanTile tokens.

@@ -172,12 +172,14 @@ __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, in
 
 // MODE 0: y. MODE 1: the variance readout y_var[t, j] = Σ_i q_i² P_t[i, j]
 // instead of y (the mean recursion is skipped; y points at y_var). MODE 2:
-// both, y into p.y and y_var into p.y_var.
+// both, y into p.y and y_var into p.y_var. MODE 3: no readout; the state is
+// stored into p.ckpt for the backward pass.
 template <typename IO, int DK, int RL, int TC, int MODE = 0>
 __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_kernel(const KernelParams p) {
   using G = Geo<DK, RL>;
   constexpr int NPR = RL / 2;  // row pairs per lane
   constexpr bool VAR = MODE == 1;
+  constexpr bool CKPT = MODE == 3;
   constexpr int NC = MODE == 2 ? 6 : 5, NOUT = MODE == 2 ? 2 : 1;
   extern __shared__ __align__(16) unsigned char smem[];
   const ScanLayout<IO, DK, TC, G::NP, NC, NOUT> L(p.cc);
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
       if (n + 2 < ntiles) stage_raw<IO, DK, TC>(p, smem + L.raw(b), bh, jb, t_begin + (n + 2) * TC, tile_len(n + 2), ptid, pn);
       cp_async_commit();
       named_sync(kBarEmpty0 + b, nall);  // the scan of tile n is done with coef/pj[b] and ypart[b]
-      if (p.y)
+      if (!CKPT && p.y)
         store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
                                       ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
       if (MODE == 2)
@@ -310,7 +312,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
   for (int n = 0; n < ntiles; ++n) {
     const int b = n & 1;
     const int tl = tile_len(n);
-    if (p.ckpt) checkpoint(n);
+    if constexpr (CKPT) checkpoint(n);
     named_sync(kBarFull0 + b, nall);  // coefficients of tile n are ready
     // ---- the scan over tile n ------------------------------------------------
     {
@@ -357,7 +359,9 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
           Bc[2 * m] = b4.x; Bc[2 * m + 1] = b4.y;
           AI[2 * m] = i4.x; AI[2 * m + 1] = i4.y;
           KI[2 * m] = k4.x; KI[2 * m + 1] = k4.y;
-          Q[2 * m] = q4.x;  Q[2 * m + 1] = q4.y;
+          if constexpr (!CKPT) {
+            Q[2 * m] = q4.x;  Q[2 * m + 1] = q4.y;
+          }
           if constexpr (MODE == 2) {
             const ulonglong2 v4 = *reinterpret_cast<const ulonglong2*>(ct + 5 * DK + 4 * m);
             QV[2 * m] = v4.x; QV[2 * m + 1] = v4.y;
@@ -386,15 +390,30 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
               const f2 g = f2_mul(s, V2[c]);
               const f2 m = f2_fma(g, KI[r], Mu[r][c]);
               Mu[r][c] = f2_mul(m, w);
-              y2 = f2_fma(Q[r], Mu[r][c], y2);
+              if constexpr (!CKPT) y2 = f2_fma(Q[r], Mu[r][c], y2);
               if constexpr (MODE == 2) yv2 = f2_fma(QV[r], Pt[r][c], yv2);
             }
           }
-          yc[c] = f2_lo(y2) + f2_hi(y2);
+          if constexpr (!CKPT) yc[c] = f2_lo(y2) + f2_hi(y2);
           if constexpr (MODE == 2) yc[CL + c] = f2_lo(yv2) + f2_hi(yv2);
         }
       };
-      if (tl == TC) {
+      if constexpr (CKPT) {
+        // State only (full tiles unrolled so that consecutive tokens' chains
+        // overlap).
+        if (tl == TC) {
+#pragma unroll
+          for (int t = 0; t < TC; ++t) {
+            load_coef(t);
+            compute(nullptr);
+          }
+        } else {
+          for (int t = 0; t < tl; ++t) {
+            load_coef(t);
+            compute(nullptr);
+          }
+        }
+      } else if (tl == TC) {
         // Full tile: tokens in batches of four. The previous batch's partial
         // sums are exchanged while this batch computes and stored with one
         // 128-bit store per value, so no store waits on a fresh result.
@@ -442,7 +461,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
     named_arrive(kBarEmpty0 + b, nall);
   }
 
-  if (p.ckpt) checkpoint(ntiles);
+  if constexpr (CKPT) checkpoint(ntiles);
   // ---- final state of the last chunk: λ_T = K_last / P̃, η_T = μ λ_T ---------
   if (z == (int)gridDim.z - 1 && p.lamT) {
     const float* klast = reinterpret_cast<const float*>(smem + L.kprev(ntiles & 1));
@@ -532,7 +551,8 @@ cudaError_t scan_dispatch(int dk, int rl, int mode, dim3 grid, int threads, size
   switch (mode) {
     case 0: return scan_dispatch_m<IO, 0>(dk, rl, grid, threads, smem, s, kp);
     case 1: return scan_dispatch_m<IO, 1>(dk, rl, grid, threads, smem, s, kp);
-    default: return scan_dispatch_m<IO, 2>(dk, rl, grid, threads, smem, s, kp);
+    case 2: return scan_dispatch_m<IO, 2>(dk, rl, grid, threads, smem, s, kp);
+    default: return scan_dispatch_m<IO, 3>(dk, rl, grid, threads, smem, s, kp);
   }
 }
 }  // namespace
@@ -548,6 +568,7 @@ cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* sta
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
   kp.ckpt = ckpt;
+  if (ckpt) mode = 3;
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
   const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, p.rows_per_lane) + kProducerWarps);
   const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile, mode);

@@ -24,12 +24,17 @@ _IO = {torch.float32: F32, torch.bfloat16: BF16}
 # Every function the header declares, for the export check.
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
            "kla_status_string", "kla_version", "kla_forward_chunked_noalloc", "kla_backward_workspace_size",
-           "kla_backward", "kla_forward_uncertainty", "kla_step_gated")
+           "kla_backward", "kla_forward_uncertainty", "kla_step_gated", "kla_backward_plan_for_sms")
 
 
 class Options(ctypes.Structure):
     _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("rows_per_lane", ctypes.c_int),
                 ("gates", ctypes.c_int)]
+
+
+class BackwardPlanInfo(ctypes.Structure):
+    _fields_ = [("cols_per_block", ctypes.c_int), ("cols_per_lane", ctypes.c_int), ("threads", ctypes.c_int),
+                ("column_blocks", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -51,6 +56,8 @@ def load_library(path: str = LIB_PATH):
     lib.kla_version.argtypes = []
     lib.kla_plan.restype = i
     lib.kla_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Options), ctypes.POINTER(PlanInfo)]
+    lib.kla_backward_plan_for_sms.restype = i
+    lib.kla_backward_plan_for_sms.argtypes = [i, i, i, i, i, i, ctypes.POINTER(BackwardPlanInfo)]
     lib.kla_plan_for_sms.restype = i
     lib.kla_plan_for_sms.argtypes = [i, i, i, i, i, i, ctypes.POINTER(Options), i, ctypes.POINTER(PlanInfo)]
     lib.kla_forward_workspace_size.restype = sz
@@ -113,6 +120,17 @@ def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strat
             "chunk_len": info.chunk_len, "num_chunks": info.num_chunks,
             "cols_per_block": info.cols_per_block, "workspace_bytes": int(info.workspace_bytes),
             "rows_per_lane": info.rows_per_lane}
+
+
+def backward_plan(B: int, H: int, T: int, dk: int, dv: int, num_sms: int | None = None) -> dict:
+    """The launch geometry kla_backward uses on a device with ``num_sms`` SMs
+    (the current device's count when None)."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    info = BackwardPlanInfo()
+    _check(LIB.kla_backward_plan_for_sms(B, H, T, dk, dv, int(num_sms), ctypes.byref(info)), "kla_backward_plan")
+    return {"cols_per_block": info.cols_per_block, "cols_per_lane": info.cols_per_lane, "threads": info.threads,
+            "column_blocks": info.column_blocks, "workspace_bytes": int(info.workspace_bytes)}
 
 
 def _ptr(t):

@@ -212,6 +212,21 @@ kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void*
  *   of the per-row and per-column sums across warps is not fixed, so the
  *   last bits of the results can differ between runs. */
 size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv);
+
+/* Launch geometry kla_backward uses. */
+typedef struct kla_backward_plan_info {
+  int cols_per_block;     /* d_v columns of one block of the reverse kernel   */
+  int cols_per_lane;      /* 8, or 4 when eight would leave SMs with few warps */
+  int threads;            /* threads per block                                 */
+  int column_blocks;      /* d_v / cols_per_block                              */
+  size_t workspace_bytes; /* what kla_backward_workspace_size returns          */
+} kla_backward_plan_info;
+
+/* The backward plan for a device with `num_sms` SMs (host-only; no CUDA
+ * call). Errors: INVALID_ARG (out NULL, negative size, num_sms < 1),
+ * UNSUPPORTED_SHAPE. B·H = 0 gives an all-zero plan. */
+kla_status kla_backward_plan_for_sms(int B, int H, int T, int dk, int dv, int num_sms,
+                                     kla_backward_plan_info* out);
 kla_status kla_backward(const void* q, const void* k, const void* v, const void* lam_v,
                         const void* a, const void* pbar, const float* lam0, const float* eta0,
                         const void* gy, const float* glamT, const float* getaT,

@@ -209,6 +209,35 @@ def test_backward_without_a_device_reports_cuda_error():
     assert L.kla_backward_workspace_size(1, 1, 8, 20, 16) == ctypes.c_size_t(-1).value
 
 
+def test_backward_plan_geometry_on_a_152_sm_device():
+    """Eight columns per lane when the blocks fill the SMs with warps (many
+    heads), four when eight would leave few warps per SM (few heads); the
+    workspace is the 16-token checkpoints plus, with split columns, the fp32
+    per-row partial sums."""
+    bp = lambda *shape, sms=152: kla.backward_plan(*shape, num_sms=sms)
+    head = bp(8, 16, 4096, 64, 64)
+    assert (head["cols_per_lane"], head["cols_per_block"], head["threads"], head["column_blocks"]) == (8, 64, 512, 1)
+    assert head["workspace_bytes"] == (4096 // 16 + 1) * 2 * 128 * 64 * 64 * 4
+    med = bp(4, 8, 2048, 64, 64)
+    assert (med["cols_per_lane"], med["cols_per_block"], med["threads"], med["column_blocks"]) == (4, 16, 256, 4)
+    assert med["workspace_bytes"] == (2048 // 16 + 1) * 2 * 32 * 64 * 64 * 4 + 4 * 32 * 2048 * 64 * 4
+    assert bp(1, 16, 65536, 128, 128)["cols_per_lane"] == 4
+    # the shapes the GPU parity tests use for four columns per lane
+    for shape in ((8, 8, 24, 16, 64), (8, 8, 19, 32, 32), (4, 4, 40, 64, 64), (1, 16, 21, 128, 128)):
+        assert bp(*shape)["cols_per_lane"] == 4, shape
+    assert bp(1, 1, 40, 16, 16)["cols_per_lane"] == 8
+    for shape in ((8, 16, 4096, 64, 64), (4, 8, 2048, 64, 64), (3, 5, 77, 32, 128)):
+        p = bp(*shape)
+        assert p["cols_per_block"] * p["column_blocks"] == shape[4]
+        assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 512
+    assert bp(0, 4, 8, 16, 16) == {"cols_per_block": 0, "cols_per_lane": 0, "threads": 0, "column_blocks": 0,
+                                   "workspace_bytes": 0}
+    info = kla.BackwardPlanInfo()
+    assert L.kla_backward_plan_for_sms(1, 1, 8, 20, 16, 152, ctypes.byref(info)) == kla.ERR_UNSUPPORTED_SHAPE
+    assert L.kla_backward_plan_for_sms(1, 1, 8, 16, 16, 0, ctypes.byref(info)) == kla.ERR_INVALID_ARG
+    assert L.kla_backward_plan_for_sms(1, 1, 8, 16, 16, 152, None) == kla.ERR_INVALID_ARG
+
+
 def test_forward_uncertainty_validation_before_any_cuda_call():
     def fu(y_var=P, y=ctypes.c_void_p(0x30000), **kw):
         g = lambda n: kw.get(n, P)

@@ -87,6 +87,17 @@ SHAPES = [
     (1, 2, 70, 64, 16, "bf16"),
     (1, 1, 100, 128, 32, "bf16"),
     (3, 1, 17, 32, 128, "bf16"),
+    # short and ragged chunks of the 16-token checkpoint interval: one
+    # 8-token chunk, one 9-token chunk, a 14-token last chunk
+    (1, 1, 8, 16, 16, "f32"),
+    (1, 1, 9, 32, 16, "f32"),
+    (1, 2, 46, 64, 32, "f32"),
+    # enough heads that the planner gives the reverse kernel four columns per
+    # lane on a 152-SM device (checked on the host in test_abi_host.py)
+    (8, 8, 24, 16, 64, "f32"),
+    (8, 8, 19, 32, 32, "bf16"),
+    (4, 4, 40, 64, 64, "f32"),
+    (1, 16, 21, 128, 128, "bf16"),
 ]
 
 
