@@ -175,7 +175,7 @@ __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, in
 // both, y into p.y and y_var into p.y_var. MODE 3: no readout; the state is
 // stored into p.ckpt for the backward pass.
 template <typename IO, int DK, int RL, int TC, int MODE = 0>
-__global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_kernel(const KernelParams p) {
+__global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps, 1) kla_scan_kernel(const KernelParams p) {
   using G = Geo<DK, RL>;
   constexpr int NPR = RL / 2;  // row pairs per lane
   constexpr bool VAR = MODE == 1;
@@ -417,10 +417,14 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps) kla_scan_ke
         // Full tile: tokens in batches of four. The previous batch's partial
         // sums are exchanged while this batch computes and stored with one
         // 128-bit store per value, so no store waits on a fresh result.
-        // (Unrolled by two batches so that pb/cur are renamed, not copied: a
-        // register move would cost a slot on the busy FMA pipe.)
+        // (Unrolled by at least two batches so that pb/cur are renamed, not
+        // copied: a register move would cost a slot on the busy FMA pipe.
+        // With eight rows per lane the whole tile is unrolled, which turns
+        // the batch conditions and offsets into constants: 4-5% faster there,
+        // 1% slower with four rows per lane.)
+        constexpr int kBatchUnroll = RL == 8 ? TC / 4 : 2;
         float pb[4][NOUT * CL];
-#pragma unroll 2
+#pragma unroll kBatchUnroll
         for (int t4 = 0; t4 < TC; t4 += 4) {
           float cur[4][NOUT * CL], ex[4][NV];
 #pragma unroll
