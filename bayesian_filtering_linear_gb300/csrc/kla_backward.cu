@@ -123,12 +123,13 @@ __device__ void issue_raw(const BwdParams& p, const BwdSmem& s, long long bh, in
   for (int arr = 0; arr < 4; ++arr)
     for (int c = threadIdx.x; c < rchunks; c += nthr)
       cp_async16(s.raw + arr * rowb + (size_t)c * 16, static_cast<const char*>(rows[arr]) + rsrc + (size_t)c * 16);
-  const int cpr = (int)(p.cc * sizeof(IO) / 16);  // 16-byte pieces per token row
+  const int cpr = (int)(p.cc * sizeof(IO) / 16);  // 16-byte pieces per token row (a power of two)
+  const int lcpr = __ffs(cpr) - 1;
   const size_t csrc = (((size_t)bh * p.T + t0) * p.dv + jb) * sizeof(IO), cstride = (size_t)p.dv * sizeof(IO);
   const void* cols[3] = {p.v, p.lam_v, p.dy};
   for (int arr = 0; arr < (p.dy ? 3 : 2); ++arr)
     for (int c = threadIdx.x; c < tl * cpr; c += nthr) {
-      const int t = c / cpr, piece = c - t * cpr;
+      const int t = c >> lcpr, piece = c & (cpr - 1);
       cp_async16(s.raw + 4 * rowb + arr * colb + (size_t)c * 16,
                  static_cast<const char*>(cols[arr]) + csrc + t * cstride + (size_t)piece * 16);
     }
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
   const long long bh = blockIdx.x;
   const int jb = blockIdx.y * p.cc;
   const BwdLane<DK, CPL> ln(p, bh, jb);
+  const int lcc = __ffs(p.cc) - 1;  // cc is a power of two
   const int i = ln.i, jl = ln.jl;
   const f2 one2 = f2_make(1.0f, 1.0f), m1 = f2_make(-1.0f, -1.0f);
 
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
       }
     }
     for (int x = threadIdx.x; x < tl * p.cc; x += blockDim.x) {
-      const int t = x / p.cc, j = x - t * p.cc;
+      const int t = x >> lcc, j = x & (p.cc - 1);
       const size_t g = ((size_t)bh * p.T + t0 + t) * p.dv + jb + j;
       const float sz = s.cacc[(t * 2 + 1) * p.cc + j];  // Σ_i k b̄
       const float gL = fmaf(s.v[t * p.cc + j], sz, s.cacc[(t * 2) * p.cc + j]);

@@ -103,8 +103,9 @@ __device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* 
     unsigned char* d = dst + arr * R::row_bytes();
     for (int c = tid; c < chunks_i; c += nthr) cp_async16(d + (size_t)c * 16, src + (size_t)c * 16);
   }
-  const int cpr = (int)(p.cc * sizeof(IO) / 16);  // 16-byte chunks per staged row
-  const int chunks_j = tl * cpr;
+  // 16-byte chunks per staged row: cc·sizeof(IO)/16, a power of two (cc is)
+  const int lcpr = p.log2cc + (sizeof(IO) == 4 ? 2 : 1) - 4;
+  const int chunks_j = tl << lcpr;
   const size_t row_j = (size_t)p.dv * sizeof(IO);
   const size_t base_j = ((size_t)bh * p.T + t0) * row_j + (size_t)jb * sizeof(IO);
 #pragma unroll
@@ -112,7 +113,7 @@ __device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* 
     const char* src = (const char*)(arr == 0 ? p.v : p.lam_v) + base_j;
     unsigned char* d = dst + 4 * R::row_bytes() + arr * R::col_bytes(p.cc);
     for (int c = tid; c < chunks_j; c += nthr) {
-      const int row = c / cpr, col = c - row * cpr;
+      const int row = c >> lcpr, col = c & ((1 << lcpr) - 1);
       cp_async16(d + (size_t)c * 16, src + (size_t)row * row_j + (size_t)col * 16);
     }
   }

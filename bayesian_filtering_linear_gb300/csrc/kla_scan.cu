@@ -147,14 +147,15 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
 
 // Finish the d_k reduction of one tile (NP partial sums per output, layout
 // [NP][cc][TCP]) and store y rows [t0, t0 + tl) of this block's columns; a
-// thread handles one column and four tokens.
+// thread handles one column and four tokens. cc = 2^log2cc.
 template <typename IO, int NP, int TC, int TCP>
-__device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int tl, int tid, int nthr) {
+__device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, int cc, int log2cc, int tl, int tid,
+                                        int nthr) {
   // Columns vary fastest across threads: the partial-sum loads (columns
   // TCP floats apart) hit distinct banks and each y row is written by
   // consecutive threads.
   for (int g = tid; g < cc * (TC / 4); g += nthr) {
-    const int col = g % cc, t4 = 4 * (g / cc);
+    const int col = g & (cc - 1), t4 = 4 * (g >> log2cc);
     if (t4 >= tl) continue;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -254,10 +255,10 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps, 1) kla_scan
       named_sync(kBarEmpty0 + b, nall);  // the scan of tile n is done with coef/pj[b] and ypart[b]
       if (!CKPT && p.y)
         store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
-                                      ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
+                                      ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, p.log2cc, tile_len(n), ptid, pn);
       if (MODE == 2)
         store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)) + L.ypart_out(),
-                                      yvbase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, tile_len(n), ptid, pn);
+                                      yvbase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, p.log2cc, tile_len(n), ptid, pn);
       if (n + 2 < ntiles) {
         cp_async_wait<0>();
         named_sync(kBarProducers, pn);
