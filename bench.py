@@ -252,18 +252,53 @@ def timed_steps(step, args, world, local, stream, flush=None):
     return total_ms, max_over_ranks(per_launch_ms, world), clocks
 
 
-def e2e_timing(e2e_step, args, world, stream) -> float:
-    """Mean ms of an end-to-end step (host copies inside), slowest rank."""
+E2E_BUFFERS = 2
+E2E_OVERLAP = ("every step copies its own inputs in from pinned host memory and its results out; with two "
+               "buffer sets the copies run on their own streams and overlap the neighbouring steps' compute")
+
+
+def pipelined_e2e(copy_in, compute, copy_out, args, world, stream, nbuf=E2E_BUFFERS) -> float:
+    """Mean ms of an end-to-end step, slowest rank, with `nbuf` sets of device
+    buffers: step i copies its inputs into set i % nbuf on one stream,
+    computes on `stream` and copies its results out on a third stream, so the
+    copy engines work on neighbouring steps while the GPU computes. Each
+    callback gets (buffer index, stream) and must enqueue its work there."""
     import torch
+    s_in, s_out = torch.cuda.Stream(device=stream.device), torch.cuda.Stream(device=stream.device)
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    used = [False] * nbuf
+
+    def one(i):
+        b = i % nbuf
+        if used[b]:
+            s_in.wait_event(ev_comp[b])  # the last compute on set b has read its inputs
+        with torch.cuda.stream(s_in):
+            copy_in(b, s_in)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if used[b]:
+            stream.wait_event(ev_out[b])  # set b's previous results are out
+        with torch.cuda.stream(stream):
+            compute(b, stream)
+        ev_comp[b].record(stream)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            copy_out(b, s_out)
+        ev_out[b].record(s_out)
+        used[b] = True
+
     steps = max(5, min(args.steps, 50))
-    for _ in range(2):
-        e2e_step()
+    for i in range(2 * nbuf):
+        one(i)
     torch.cuda.synchronize()
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(steps):
-        e2e_step()
+    s.record(s_in)
+    for i in range(steps):
+        one(i)
+    stream.wait_event(ev_out[(steps - 1) % nbuf])
     e.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(s.elapsed_time(e) / steps, world)
@@ -317,23 +352,27 @@ def run_kla(args, world, rank, local):
     # ---- end to end through host buffers: H2D of the inputs, the call, D2H of
     # the outputs, every step, inside the timed region ------------------------
     host = {n: x[n].cpu().pin_memory() for n in names}
-    devb = {n: torch.empty_like(x[n]) for n in names}
-    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    l_h = torch.empty(lamT.shape, dtype=lamT.dtype).pin_memory()
-    e_h = torch.empty(etaT.shape, dtype=etaT.dtype).pin_memory()
+    nb = E2E_BUFFERS
+    devb = [{n: torch.empty_like(x[n]) for n in names} for _ in range(nb)]
+    outs = [(torch.empty_like(y), torch.empty_like(lamT), torch.empty_like(etaT)) for _ in range(nb)]
+    outs_h = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in o) for o in outs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in (y_h, l_h, e_h))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
 
-    def e2e_step():
+    def copy_in(b, s):
         for n in names:
-            devb[n].copy_(host[n], non_blocking=True)
-        kla.forward(devb["q"], devb["k"], devb["v"], devb["lam_v"], devb["a"], devb["pbar"], devb["lam0"],
-                    devb["eta0"], y=y, lamT=lamT, etaT=etaT, workspace=ws, stream=stream)
-        y_h.copy_(y, non_blocking=True)
-        l_h.copy_(lamT, non_blocking=True)
-        e_h.copy_(etaT, non_blocking=True)
+            devb[b][n].copy_(host[n], non_blocking=True)
 
-    e2e_ms = e2e_timing(e2e_step, args, world, stream)
+    def compute(b, s):
+        d, (yb, lb, eb) = devb[b], outs[b]
+        kla.forward(d["q"], d["k"], d["v"], d["lam_v"], d["a"], d["pbar"], d["lam0"], d["eta0"],
+                    y=yb, lamT=lb, etaT=eb, workspace=ws, stream=s)
+
+    def copy_out(b, s):
+        for t_h, t in zip(outs_h[b], outs[b]):
+            t_h.copy_(t, non_blocking=True)
+
+    e2e_ms = pipelined_e2e(copy_in, compute, copy_out, args, world, stream)
     if rank != 0:
         return
 
@@ -372,7 +411,7 @@ def run_kla(args, world, rank, local):
                      "flops_per_launch": flops},
         "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": E2E_OVERLAP},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }), flush=True)
@@ -407,22 +446,28 @@ def run_kla_decode(args, world, rank, local, w, x, stream):
     value = heads * world / (ms_per_step * 1e-3)
 
     host = [{n: t[n].cpu().pin_memory() for n in per_tok} for t in toks[:8]]
-    devb = {n: torch.empty_like(toks[0][n]) for n in per_tok}
-    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    nb = E2E_BUFFERS
+    devb = [{n: torch.empty_like(toks[0][n]) for n in per_tok} for _ in range(nb)]
+    ys = [torch.empty_like(y) for _ in range(nb)]
+    ys_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(nb)]
     h2d = sum(t.numel() * t.element_size() for t in host[0].values())
-    d2h = y_h.numel() * y_h.element_size()
+    d2h = ys_h[0].numel() * ys_h[0].element_size()
     ie = [0]
 
-    def e2e_step():
+    def copy_in(b, s):
         h = host[ie[0] % len(host)]
         ie[0] += 1
         for n in per_tok:
-            devb[n].copy_(h[n], non_blocking=True)
-        kla.step(devb["q"], devb["k"], devb["v"], devb["lam_v"], devb["a"], devb["pbar"], lam, eta, y=y,
-                 stream=stream)
-        y_h.copy_(y, non_blocking=True)
+            devb[b][n].copy_(h[n], non_blocking=True)
 
-    e2e_ms = e2e_timing(e2e_step, args, world, stream)
+    def compute(b, s):  # the state is updated in place, so steps stay in order on `stream`
+        d = devb[b]
+        kla.step(d["q"], d["k"], d["v"], d["lam_v"], d["a"], d["pbar"], lam, eta, y=ys[b], stream=s)
+
+    def copy_out(b, s):
+        ys_h[b].copy_(ys[b], non_blocking=True)
+
+    e2e_ms = pipelined_e2e(copy_in, compute, copy_out, args, world, stream)
     if rank != 0:
         return
     peaks = measured_peaks()
@@ -445,7 +490,7 @@ def run_kla_decode(args, world, rank, local, w, x, stream):
                      "bytes_per_launch": bytes_per_step},
         "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
         "e2e": {"value": heads * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": E2E_OVERLAP},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }), flush=True)
@@ -476,21 +521,30 @@ def run_kla_backward(args, world, rank, local, w, x, stream):
 
     host = {n: x[n].cpu().pin_memory() for n in names}
     host_up = {"gy": gy.cpu().pin_memory(), "gl": gl.cpu().pin_memory(), "ge": ge.cpu().pin_memory()}
-    devb = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in list(host.items()) + list(host_up.items())}
+    nb = E2E_BUFFERS
+    devb = [{n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in list(host.items()) + list(host_up.items())}
+            for _ in range(nb)]
     sample = kla.backward(*(x[n] for n in names), gy=gy, glamT=gl, getaT=ge, workspace=ws, stream=stream)
-    out_h = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in sample.items()}
+    outs_h = [{n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in sample.items()} for _ in range(nb)]
     h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_up.values()))
-    d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h[0].values())
+    results = [None] * nb
 
-    def e2e_step():
+    def copy_in(b, s):
         for n, t in list(host.items()) + list(host_up.items()):
-            devb[n].copy_(t, non_blocking=True)
-        out = kla.backward(*(devb[n] for n in names), gy=devb["gy"], glamT=devb["gl"], getaT=devb["ge"],
-                           workspace=ws, stream=stream)
-        for n, t in out.items():
-            out_h[n].copy_(t, non_blocking=True)
+            devb[b][n].copy_(t, non_blocking=True)
 
-    e2e_ms = e2e_timing(e2e_step, args, world, stream)
+    def compute(b, s):  # the gradients are allocated on `s` (the current stream here)
+        d = devb[b]
+        results[b] = kla.backward(*(d[n] for n in names), gy=d["gy"], glamT=d["gl"], getaT=d["ge"], workspace=ws,
+                                  stream=s)
+
+    def copy_out(b, s):
+        for n, t in results[b].items():
+            t.record_stream(s)  # read on the copy stream: not reused before the copy is done
+            outs_h[b][n].copy_(t, non_blocking=True)
+
+    e2e_ms = pipelined_e2e(copy_in, compute, copy_out, args, world, stream)
     if rank != 0:
         return
     ckpt_bytes = (-(-w.T // 16) + 1) * 2 * w.B * w.H * w.dk * w.dv * 4
@@ -516,7 +570,7 @@ def run_kla_backward(args, world, rank, local, w, x, stream):
                      "flops_per_launch": flops},
         "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": E2E_OVERLAP},
         # checkpointing scan + reverse kernel, + the row-sum pass when the
         # workspace holds more than the checkpoints (columns split over blocks)
         "gpu_launches": (2 + int(ws.numel() > ckpt_bytes)) * args.steps,
