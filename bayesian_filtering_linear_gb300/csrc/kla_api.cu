@@ -1,6 +1,7 @@
 // C ABI of the KLA scan library: argument validation, the launch planner and
 // the entry points declared in include/kla.h. Host code only; the kernels are
-// in kla_scan.cu (sequence scan), kla_compose.cu (chunk compose and carry),
+// in kla_scan_kernel.cuh (sequence scan; launched from kla_scan.cu),
+// kla_compose.cu (chunk compose and carry),
 // kla_noalloc.cu (the allocation-free chunked path), kla_step.cu (decode step)
 // and kla_backward.cu (backward pass).
 #include <algorithm>

@@ -21,7 +21,7 @@
 // GPU plan (three kernels, all on the caller's stream):
 //  1. The forward scan kernel (sequential plan, no y) stores the scaled state
 //     (P̃ = K·P, μ) of every element before every 16-token tile and at the
-//     end into the workspace (kla_scan.cu).
+//     end into the workspace (kla_scan_kernel.cuh).
 //  2. kla_bwd_kernel walks the chunks from last to first, each in sub-chunks
 //     of kSub tokens from its end: it re-runs the forward from the chunk's
 //     checkpoint to the sub-chunk, keeps the states before the sub-chunk's

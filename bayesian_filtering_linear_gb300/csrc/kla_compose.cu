@@ -1,7 +1,7 @@
 // Chunk-parallel path over T for sm_103a: composition of each chunk's
 // per-element map, the carry of the maps across chunks, and the state copy
 // used when T = 0. The chunks are then re-run by the scan kernel
-// (kla_scan.cu) from their carried start states.
+// (kla_scan_kernel.cuh) from their carried start states.
 //
 // Source: "Technische Samenvatting: Kalman Linear Attention (KLA)"
 // (gist.science/nl/paper/2602.10743), Methodologie §2: the precision updates

@@ -11,7 +11,7 @@ namespace kla {
 
 // k² is raised by 2^-40 before it is used as a scale, and a is floored at
 // 2^-40, so every scaled quantity in the forward recursion stays a normal
-// fp32 number (see kla_scan.cu). For |k| ≥ 2^-8 the raised k² rounds back
+// fp32 number (see kla_scan_kernel.cuh). For |k| ≥ 2^-8 the raised k² rounds back
 // to k² exactly; below that it adds 2^-40·Λ^v to the observation precision.
 constexpr float kK2Floor = 0x1p-40f;
 constexpr float kAMin = 0x1p-40f;

@@ -56,7 +56,8 @@ BWD_FLOPS_PER_ELEMENT_STEP = 13 + 48
 L2_FLUSH_BYTES = 256 << 20   # written between steps when a workload's inputs fit in L2
 TRAFFIC_FILES = {"headline": os.path.join(ROOT, "profiles", "traffic_headline.json")}
 KERNEL_SOURCES = [os.path.join(ROOT, "bayesian_filtering_linear_gb300", "csrc", f)
-                  for f in ("kla_scan.cu", "kla_common.cuh", "kla_device.cuh")]
+                  for f in ("kla_scan_kernel.cuh", "kla_scan_inst_y.cu", "kla_scan.cu", "kla_common.cuh",
+                            "kla_device.cuh")]
 
 
 def kernel_source_hash() -> str:

@@ -1,5 +1,5 @@
 """CPU model of the hand-off protocol inside kla_scan_kernel
-(bayesian_filtering_linear_gb300/csrc/kla_scan.cu).
+(bayesian_filtering_linear_gb300/csrc/kla_scan_kernel.cuh).
 
 The scan block has producer warps (stage raw tiles with cp.async, build
 coefficients, store y) and scanning warps, synchronised only by named
