@@ -48,7 +48,9 @@ def load_library(path: str = LIB_PATH):
     if not os.path.exists(path):
         raise ImportError(f"{path} is not built; run `python -m bayesian_filtering_linear_gb300.build` "
                           "(needs nvcc) — there is no fallback implementation")
-    lib = ctypes.CDLL(path)
+    # RTLD_NOW: an unresolved symbol fails here, not at the first call of the
+    # function that needs it.
+    lib = ctypes.CDLL(path, mode=os.RTLD_NOW | os.RTLD_LOCAL)
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.kla_status_string.restype = ctypes.c_char_p
     lib.kla_status_string.argtypes = [i]
