@@ -104,11 +104,12 @@ long long run_head(const Args<R, In>& g, long long bh) {
         if (KLA_ORACLE_MUTANT == 6) mun = Ppred * (mupred / Ppred + b);  // prior variance
         const R readout = (KLA_ORACLE_MUTANT == 4) ? mupred : mun;      // 4: prior mean read out
         muabs[e] = Pn * (std::fabs(ai) * muabs[e] / Ppred + std::fabs(b));
+        if (KLA_ORACLE_MUTANT == 12) muabs[e] += Pn * std::fabs(b);  // 12: |b| counted twice in the scale
         P[e] = Pn;
         mu[e] = mun;
         yacc[j] += qi * readout;
         yvar[j] += qi * qi * (KLA_ORACLE_MUTANT == 10 ? Ppred : Pn);  // 10: prior variance read out
-        ysc[j] += std::fabs(qi) * muabs[e];
+        ysc[j] += (KLA_ORACLE_MUTANT == 11 ? (R)2 : (R)1) * std::fabs(qi) * muabs[e];  // 11: |q| twice
         const R lam = (R)1 / Pn;
         if (!(lam > 0)) ++violations;
         // λ_t = λ_pred + c with λ_pred ∈ (0, 1/p̄]; allow one rounding step.
@@ -253,16 +254,17 @@ long long bwd_head(const BwdArgs<In>& g, long long bh) {
         mb += qt * gy;
         mbh += std::fabs(qt * gy);
         add(g.dq, ri, gy * mu[t + 1]);
-        add(g.sq, ri, std::fabs(gy) * muabs[t + 1]);
+        add(g.sq, ri, (KLA_ORACLE_MUTANT == 13 ? 2.0 : 1.0) * std::fabs(gy) * muabs[t + 1]);  // 13: scale doubled
         // through μ' = w u and P' = w P⁻
         const double ub = mb * w, ubh = mbh * w;
         const double wb = mb * u + Pb * Pp, wbh = mbh * uabs + Pbh * Pp;
         double Ppb = Pb * w + ub * b - wb * c * w * w;
         if (KLA_ORACLE_MUTANT == 7) Ppb = Pb * w + ub * b;  // dropped the path through w
-        const double Ppbh = Pbh * w + ubh * std::fabs(b) + wbh * c * w * w;
+        double Ppbh = Pbh * w + ubh * std::fabs(b) + wbh * c * w * w;
+        if (KLA_ORACLE_MUTANT == 14) Ppbh += Pbh * w;  // 14: the carried term counted twice in the scale
         double cb = -wb * Pp * w * w;
         if (KLA_ORACLE_MUTANT == 8) cb = wb * Pp * w * w;   // sign of ∂w/∂c
-        const double cbh = wbh * Pp * w * w;
+        const double cbh = (KLA_ORACLE_MUTANT == 15 ? 2.0 : 1.0) * wbh * Pp * w * w;  // 15: scale doubled
         const double bb = ub * Pp, bbh = ubh * Pp;
         // per-row inputs
         add(g.da, ri, ub * mu[t] + 2.0 * at * P[t] * Ppb);
