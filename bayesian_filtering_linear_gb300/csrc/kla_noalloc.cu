@@ -21,34 +21,67 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kla.h"
+#include "kla_ctx_cache.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = 32u << 20;  // 32 MiB
 
 // Device-side scratch. In host code this name is only a stand-in for the
-// symbol, not a device address: the address comes from cudaGetSymbolAddress.
+// symbol, not a device address: the address comes from cudaGetSymbolAddress,
+// once per CUDA context (each context that loads the module has its own copy).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+// Driver calls that identify the current context, taken through the runtime's
+// entry-point query so that the library does not link the driver library.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Look up (once per device, with that device current) the device address of
-// the scratch array.
+std::mutex g_mutex;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+kla::ContextAddressCache<64> g_cache;  // context ID -> scratch address
+
+bool driver_entry_points() {
+  if (g_ctx_current && g_ctx_id) return true;
+  void* f1 = nullptr;
+  void* f2 = nullptr;
+  cudaDriverEntryPointQueryResult q1{}, q2{};
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+      cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+      q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+    return false;
+  g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+  g_ctx_id = reinterpret_cast<CtxGetIdFn>(f2);
+  return true;
+}
+
+// The device address of the scratch array in the calling thread's current
+// context: looked up with cudaGetSymbolAddress on the first call in each
+// context (which, with no context current yet, also creates the device's
+// primary context), then taken from the cache.
 kla_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
+  if (!driver_entry_points()) return KLA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return KLA_ERR_CUDA;
+  void* ptr = nullptr;
+  if (!ctx) {  // nothing current yet: the lookup makes the primary context current
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return KLA_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return KLA_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  unsigned long long id = 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return KLA_ERR_CUDA;
+  if (!ptr) ptr = g_cache.find(id);
+  if (!ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return KLA_ERR_CUDA;
+  }
+  g_cache.insert(id, ptr);
+  *out = ptr;
   return KLA_OK;
 }
 

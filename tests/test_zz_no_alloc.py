@@ -5,9 +5,10 @@ chunk-parallel scan with the library's own fixed 32 MiB device scratch
 instead of a caller-provided workspace.
 
 Checked through the C ABI against kla_forward on the same inputs with the
-same chunk length, on two calls in a row (the second must not see stale
-scratch from the first), and that a call needing more than 32 MiB of scratch
-is refused before anything is launched. Kept in its own file, collected
+same chunk length, on two calls in a row with different shapes (the second
+must not see stale scratch from the first), with an explicit, the automatic
+and a one-chunk chunk length, and that a call needing more than 32 MiB of
+scratch is refused before anything is launched. Kept in its own file, collected
 last, so that a stop-at-first-failure run has already run every other test.
 """
 import ctypes
@@ -44,22 +45,38 @@ def _noalloc(x, io, chunk_len):
     return st, y, lamT, etaT
 
 
+def _compare(x, io, chunk_len):
+    B, H, T, dk = x["q"].shape
+    dv = x["v"].shape[-1]
+    y_ref, l_ref, e_ref = kla.forward(*[x[n] for n in NAMES], x["lam0"], x["eta0"], strategy="chunked",
+                                      chunk_len=chunk_len)
+    st, y, l, e = _noalloc(x, io, chunk_len)
+    torch.cuda.synchronize()
+    assert st == kla.OK, kla.status_string(st)
+    scale = y_ref.float().abs().max()
+    assert float((y.float() - y_ref.float()).abs().max() / scale) <= TOL[io]
+    assert float(((l - l_ref).abs() / l_ref).max()) <= TOL[io]
+    assert float((e - e_ref).abs().max() / e_ref.abs().max()) <= TOL[io]
+
+
+# Two calls in a row with different shapes (the second call's scratch layout
+# differs from the first's, so stale contents would show): an explicit chunk
+# length, the automatic one (0), and a sequence no longer than one chunk
+# (the plan then runs one chunk and uses no scratch).
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_noalloc_matches_kla_forward_on_two_calls(io):
-    chunk_len = 128
-    for seed in (21, 22):
-        x = {n: t.cuda() for n, t in make_inputs(2, 3, 700, 64, 32, io=io, seed=seed, random_state=True).items()}
-        need = kla.plan(2, 3, 700, 64, 32, io, strategy="chunked", chunk_len=chunk_len)
-        assert need["strategy"] == "chunked" and 0 < need["workspace_bytes"] <= 32 << 20
-        y_ref, l_ref, e_ref = kla.forward(*[x[n] for n in NAMES], x["lam0"], x["eta0"], strategy="chunked",
-                                          chunk_len=chunk_len)
-        st, y, l, e = _noalloc(x, io, chunk_len)
-        torch.cuda.synchronize()
-        assert st == kla.OK, kla.status_string(st)
-        scale = y_ref.float().abs().max()
-        assert float((y.float() - y_ref.float()).abs().max() / scale) <= TOL[io]
-        assert float(((l - l_ref).abs() / l_ref).max()) <= TOL[io]
-        assert float((e - e_ref).abs().max() / e_ref.abs().max()) <= TOL[io]
+@pytest.mark.parametrize("chunk_len,shapes", [
+    (128, [(2, 3, 700, 64, 32), (1, 5, 1000, 32, 64)]),
+    (0, [(1, 2, 900, 64, 64), (3, 1, 513, 128, 32)]),
+    (256, [(2, 2, 200, 64, 32), (1, 3, 256, 16, 16)]),
+], ids=["chunk128", "auto", "one-chunk"])
+def test_noalloc_matches_kla_forward_on_two_calls(io, chunk_len, shapes):
+    for seed, (B, H, T, dk, dv) in enumerate(shapes, start=21):
+        x = {n: t.cuda() for n, t in make_inputs(B, H, T, dk, dv, io=io, seed=seed, random_state=True).items()}
+        need = kla.plan(B, H, T, dk, dv, io, strategy="chunked", chunk_len=chunk_len)
+        assert need["workspace_bytes"] <= 32 << 20
+        if T > max(chunk_len, 32):
+            assert need["strategy"] == "chunked" and need["workspace_bytes"] > 0
+        _compare(x, io, chunk_len)
 
 
 def test_noalloc_refuses_more_than_its_scratch():
