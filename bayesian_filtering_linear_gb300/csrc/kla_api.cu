@@ -397,6 +397,78 @@ kla_status kla_step(const void* q, const void* k, const void* v, const void* lam
   return kla_step_gated(q, k, v, lam_v, a, pbar, lam, eta, y, B, H, dk, dv, io, 0, stream);
 }
 
+kla_status kla_shard_map(const void* q, const void* k, const void* v, const void* lam_v, const void* a,
+                         const void* pbar, float* map, int B, int H, int T, int dk, int dv, kla_dtype io, int gates,
+                         void* stream) {
+  // ---- validation: no CUDA call before it passes ---------------------------
+  kla_status st = check_shape(B, H, T, dk, dv);
+  if (st != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  if (!valid_gates(gates)) return KLA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  if (bh > 0 && !map) return KLA_ERR_INVALID_ARG;
+  if (bh > 0 && T > 0 && (!q || !k || !v || !lam_v || !a || !pbar)) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, lam_v, a, pbar, map};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  if (bh == 0) return KLA_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long elems = bh * dk * dv;
+  if (T == 0) return kla::launch_identity_map(map, elems, s) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  // The whole shard is one chunk of the composition kernel (grid.z = 1).
+  // Column block: the widest that still gives two blocks per SM, else the
+  // narrowest the kernel allows (more blocks for few heads).
+  const int wc = kla::warp_cols(dk, kla::rows_per_lane_for(dk));
+  const int cc_min = std::max<int>(wc, (int)(16 / io_size(io)));
+  const int cc_max = std::min(dv, kla::max_threads() / 32 * wc);
+  int cc = cc_min;
+  for (int c = cc_min; c <= cc_max; c *= 2)
+    if (bh * (dv / c) >= 2LL * sms) cc = c;
+  if (kla::compose_smem_bytes(dk, io, cc, kla::tile_for(dk, io)) > kMaxSmem) return KLA_ERR_UNSUPPORTED_SHAPE;
+  Plan p{};
+  p.strategy = KLA_CHUNKED;
+  p.chunk_len = T;
+  p.num_chunks = 2;
+  p.cols_per_block = cc;
+  p.rows_per_lane = kla::rows_per_lane_for(dk);
+  p.tile = kla::tile_for(dk, io);
+  kla::ForwardArgs f{q, k, v, lam_v, a, pbar, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T, dk, dv,
+                     (int)io, gates};
+  return kla::launch_compose(f, p, map, s) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_shard_start(const float* maps, int n_maps, const float* lam0, const float* eta0, float* lam_start,
+                           float* eta_start, int B, int H, int dk, int dv, void* stream) {
+  kla_status st = check_shape(B, H, 0, dk, dv);
+  if (st != KLA_OK) return st;
+  if (n_maps < 0) return KLA_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  if ((lam0 == nullptr) != (eta0 == nullptr)) return KLA_ERR_INVALID_ARG;
+  if (bh > 0 && (!lam_start || !eta_start || (n_maps > 0 && !maps))) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {maps, lam0, eta0, lam_start, eta_start};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  const size_t state_bytes = (size_t)bh * dk * dv * sizeof(float);
+  if (overlaps_partially(lam_start, lam0, state_bytes) || overlaps_partially(eta_start, eta0, state_bytes) ||
+      overlaps_partially(lam_start, eta0, state_bytes) || overlaps_partially(eta_start, lam0, state_bytes) ||
+      (lam_start && (lam_start == (const float*)eta0 || lam_start == eta_start)) ||
+      (eta_start && eta_start == (const float*)lam0) || overlaps_partially(lam_start, eta_start, state_bytes))
+    return KLA_ERR_INVALID_ARG;
+  if (maps && n_maps > 0) {
+    const size_t map_bytes = (size_t)n_maps * 7 * state_bytes;
+    for (const float* o : {lam_start, eta_start}) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(maps), b0 = reinterpret_cast<uintptr_t>(o);
+      if (a0 < b0 + state_bytes && b0 < a0 + map_bytes) return KLA_ERR_INVALID_ARG;
+    }
+  }
+  if (bh == 0) return KLA_OK;
+  const cudaError_t e = kla::launch_shard_start(maps, n_maps, lam0, eta0, lam_start, eta_start, bh * dk * dv,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
 size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv) {
   if (check_shape(B, H, T, dk, dv) != KLA_OK) return (size_t)-1;
   const long long bh = (long long)B * H;

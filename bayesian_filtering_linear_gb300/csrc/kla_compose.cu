@@ -223,6 +223,41 @@ __global__ void kla_init_state_kernel(const float* lam0, const float* eta0, floa
   if (etaT) etaT[e] = n;
 }
 
+// Context-parallel sharding over T: the start state of a shard from the maps
+// of the shards before it, applied in order to (λ0, η0) (or 1 and 0), in
+// information form: λ = 1/P, η = μ/P. Each thread reads its element's
+// initial state before writing, so the output may alias lam0/eta0.
+__global__ void kla_shard_start_kernel(const float* __restrict__ maps, int n_maps, const float* lam0,
+                                       const float* eta0, float* lamS, float* etaS, long long elems) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= elems) return;
+  float P = 1.0f, mu = 0.0f;
+  if (lam0) {
+    P = 1.0f / lam0[e];
+    mu = eta0[e] * P;
+  }
+  for (int z = 0; z < n_maps; ++z) {
+    const float* m = maps + (size_t)z * 7 * elems + e;
+    const float A = m[0], B = m[elems], C = m[2 * elems], D = m[3 * elems];
+    const float E = m[4 * elems], F = m[5 * elems], Gm = m[6 * elems];
+    const float nn = fmaf(A, P, B);
+    const float mm = fmaf(C, P, D);
+    const float ee = fmaf(E, P, fmaf(Gm, mu, F));
+    P = nn / mm;
+    mu = ee / mm;
+  }
+  lamS[e] = 1.0f / P;
+  etaS[e] = mu / P;
+}
+
+// The identity map (A, D, G = 1; B, C, E, F = 0): the map of an empty shard.
+__global__ void kla_identity_map_kernel(float* maps, long long elems) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= elems) return;
+#pragma unroll
+  for (int q = 0; q < 7; ++q) maps[(size_t)q * elems + e] = (q == 0 || q == 3 || q == 6) ? 1.0f : 0.0f;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -290,6 +325,27 @@ cudaError_t launch_init_state(const ForwardArgs& f, cudaStream_t s) {
   const int threads = 256;
   const unsigned blocks = (unsigned)((elems + threads - 1) / threads);
   kla_init_state_kernel<<<blocks, threads, 0, s>>>(f.lam0, f.eta0, f.lamT, f.etaT, elems);
+  return cudaGetLastError();
+}
+
+}  // namespace kla
+
+namespace kla {
+
+cudaError_t launch_shard_start(const float* maps, int n_maps, const float* lam0, const float* eta0, float* lamS,
+                               float* etaS, long long elems, cudaStream_t s) {
+  if (elems == 0) return cudaSuccess;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((elems + threads - 1) / threads);
+  kla_shard_start_kernel<<<blocks, threads, 0, s>>>(maps, n_maps, lam0, eta0, lamS, etaS, elems);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_identity_map(float* maps, long long elems, cudaStream_t s) {
+  if (elems == 0) return cudaSuccess;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((elems + threads - 1) / threads);
+  kla_identity_map_kernel<<<blocks, threads, 0, s>>>(maps, elems);
   return cudaGetLastError();
 }
 

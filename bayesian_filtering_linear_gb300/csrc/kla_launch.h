@@ -61,6 +61,12 @@ cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cud
 cudaError_t launch_carry(const ForwardArgs& f, const Plan& p, const float* maps, float* starts,
                          cudaStream_t s);
 cudaError_t launch_init_state(const ForwardArgs& f, cudaStream_t s);
+// Context-parallel sharding over T (kla_shard_map / kla_shard_start): the
+// start state (λ, η) of a shard from the maps [n_maps][7][elems] of the shards
+// before it, and the identity map (an empty shard).
+cudaError_t launch_shard_start(const float* maps, int n_maps, const float* lam0, const float* eta0, float* lamS,
+                               float* etaS, long long elems, cudaStream_t s);
+cudaError_t launch_identity_map(float* maps, long long elems, cudaStream_t s);
 
 // Backward pass (kla_backward.cu): gradients of a loss given dL/dy and
 // optionally dL/dλ_T, dL/dη_T.

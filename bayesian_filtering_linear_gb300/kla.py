@@ -24,7 +24,8 @@ _IO = {torch.float32: F32, torch.bfloat16: BF16}
 # Every function the header declares, for the export check.
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
            "kla_status_string", "kla_version", "kla_forward_chunked_noalloc", "kla_backward_workspace_size",
-           "kla_backward", "kla_forward_uncertainty", "kla_step_gated", "kla_backward_plan_for_sms")
+           "kla_backward", "kla_forward_uncertainty", "kla_step_gated", "kla_backward_plan_for_sms",
+           "kla_shard_map", "kla_shard_start")
 
 
 class Options(ctypes.Structure):
@@ -76,6 +77,10 @@ def load_library(path: str = LIB_PATH):
     lib.kla_backward.argtypes = [vp] * 19 + [i] * 7 + [vp, sz, vp]
     lib.kla_step_gated.restype = i
     lib.kla_step_gated.argtypes = [vp] * 9 + [i] * 6 + [vp]
+    lib.kla_shard_map.restype = i
+    lib.kla_shard_map.argtypes = [vp] * 7 + [i] * 7 + [vp]
+    lib.kla_shard_start.restype = i
+    lib.kla_shard_start.argtypes = [vp, i, vp, vp, vp, vp, i, i, i, i, vp]
     return lib
 
 
@@ -232,8 +237,12 @@ def step(q, k, v, lam_v, a, pbar, lam, eta, *, y=None, stream=None, gates: int =
     else:
         _need(y, "y", dt, (B, H, dv), dev)
     with torch.cuda.device(dev):
-        st = LIB.kla_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam), _ptr(eta),
-                                _ptr(y), B, H, dk, dv, _IO[dt], int(gates), _stream(stream))
+        if gates:
+            st = LIB.kla_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam),
+                                    _ptr(eta), _ptr(y), B, H, dk, dv, _IO[dt], int(gates), _stream(stream))
+        else:
+            st = LIB.kla_step(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(lam), _ptr(eta),
+                              _ptr(y), B, H, dk, dv, _IO[dt], _stream(stream))
     _check(st, "kla_step")
     return y
 
@@ -280,3 +289,82 @@ def backward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, gy=None, glamT=No
                               ws_bytes, _stream(stream))
     _check(st, "kla_backward")
     return out
+
+
+# ---- context-parallel sharding over T -----------------------------------------
+
+def shard_map(q, k, v, lam_v, a, pbar, *, gates: int = 0, out=None, stream=None):
+    """The composed map of a shard (all of its tokens), ``[7, B, H, dk, dv]``
+    fp32 (kla_shard_map): (A, B, C, D, E, F, G) take the state (P, μ) before
+    the shard to P' = (A P + B)/(C P + D), μ' = (E P + F + G μ)/(C P + D)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    if dt not in _IO:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    for name, t, last in (("q", q, dk), ("k", k, dk), ("a", a, dk), ("pbar", pbar, dk),
+                          ("v", v, dv), ("lam_v", lam_v, dv)):
+        _need(t, name, dt, (B, H, T, last), dev)
+    if out is None:
+        out = torch.empty((7, B, H, dk, dv), dtype=torch.float32, device=dev)
+    else:
+        _need(out, "out", torch.float32, (7, B, H, dk, dv), dev)
+    with torch.cuda.device(dev):
+        st = LIB.kla_shard_map(_ptr(q), _ptr(k), _ptr(v), _ptr(lam_v), _ptr(a), _ptr(pbar), _ptr(out),
+                               B, H, T, dk, dv, _IO[dt], int(gates), _stream(stream))
+    _check(st, "kla_shard_map")
+    return out
+
+
+def shard_start(maps, lam0=None, eta0=None, *, lam_out=None, eta_out=None, stream=None):
+    """Start state (λ, η) of the shard after those whose maps are stacked in
+    ``maps`` ``[n, 7, B, H, dk, dv]`` (in sequence order), from (λ0, η0) (None:
+    λ0 = 1, η0 = 0). Returns ``(lam, eta)`` fp32 ``[B, H, dk, dv]``."""
+    n, seven, B, H, dk, dv = maps.shape
+    if seven != 7:
+        raise ValueError("maps must be [n, 7, B, H, dk, dv]")
+    dev = maps.device
+    _need(maps, "maps", torch.float32, tuple(maps.shape), dev)
+    st_shape = (B, H, dk, dv)
+    for name, t in (("lam0", lam0), ("eta0", eta0), ("lam_out", lam_out), ("eta_out", eta_out)):
+        if t is not None:
+            _need(t, name, torch.float32, st_shape, dev)
+    lam_out = torch.empty(st_shape, dtype=torch.float32, device=dev) if lam_out is None else lam_out
+    eta_out = torch.empty(st_shape, dtype=torch.float32, device=dev) if eta_out is None else eta_out
+    with torch.cuda.device(dev):
+        st = LIB.kla_shard_start(_ptr(maps) if n else None, n, _ptr(lam0), _ptr(eta0), _ptr(lam_out),
+                                 _ptr(eta_out), B, H, dk, dv, _stream(stream))
+    _check(st, "kla_shard_start")
+    return lam_out, eta_out
+
+
+def exchange_maps(local_map, group=None):
+    """All-gather every rank's shard map, ``[world, 7, B, H, dk, dv]`` in rank
+    order. With the NCCL backend the device tensors are gathered in place;
+    with another backend (gloo) through host copies."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    nccl = dist.get_backend(group) == "nccl"
+    src = local_map if nccl else local_map.cpu()
+    parts = [torch.empty_like(src) for _ in range(world)]
+    dist.all_gather(parts, src.contiguous(), group=group)
+    out = torch.stack(parts)
+    return out if out.device == local_map.device else out.to(local_map.device)
+
+
+def forward_context_parallel(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, group=None, gates: int = 0,
+                             stream=None, **forward_kw):
+    """KLA forward over a sequence cut along T across the ranks of ``group``
+    (rank r holds the r-th contiguous token range of the same heads). Each
+    rank composes its shard's map (kla_shard_map), the maps are all-gathered
+    (the one exchange step), each rank applies the maps of the shards before
+    its own to (λ0, η0) (kla_shard_start) and scans its shard from that state
+    (kla_forward). Returns this rank's ``(y, lamT, etaT)``: y of its tokens and
+    the state after its shard (the last rank's is the sequence's final state).
+    λ0, η0 must be the same on every rank."""
+    import torch.distributed as dist
+    rank = dist.get_rank(group)
+    local = shard_map(q, k, v, lam_v, a, pbar, gates=gates, stream=stream)
+    maps = exchange_maps(local, group)
+    lam_s, eta_s = shard_start(maps[:rank].contiguous(), lam0, eta0, stream=stream)
+    return forward(q, k, v, lam_v, a, pbar, lam_s, eta_s, gates=gates, stream=stream, **forward_kw)

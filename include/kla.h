@@ -25,8 +25,12 @@
  * Conventions for every entry point:
  *  - All array pointers are DEVICE pointers owned by the caller; the library
  *    allocates no device memory and keeps no state beyond a per-device cache
- *    of the SM count. Work is queued on `stream` (a cudaStream_t; NULL is the
- *    legacy default stream) and the call returns without synchronising.
+ *    of the SM count. The one exception is kla_forward_chunked_noalloc: its
+ *    fixed 32 MiB scratch array lives in device memory on every GPU that
+ *    loads the library, its address is cached per CUDA context, and calls of
+ *    it that overlap on the GPU race (see its comment below). Work is queued
+ *    on `stream` (a cudaStream_t; NULL is the legacy default stream) and the
+ *    call returns without synchronising.
  *  - Layout is contiguous row-major with no strides:
  *      q, k, a, pbar : [B, H, T, d_k]     v, lam_v, y : [B, H, T, d_v]
  *      lam0, eta0, lamT, etaT : [B, H, d_k, d_v], always fp32.
@@ -41,7 +45,8 @@
  *    kernels raise a below 2^-40 to 2^-40 and add 2^-40 to k², which changes
  *    results only below fp32 resolution for |k| ≥ 2^-8; other violations
  *    give NaN/Inf and never a trap.
- *  - Entry points are thread-safe; calls on one stream are ordered.
+ *  - Entry points are thread-safe; calls on one stream are ordered (for
+ *    kla_forward_chunked_noalloc, see its comment on overlapping calls).
  */
 #ifndef KLA_H_
 #define KLA_H_
@@ -59,7 +64,9 @@ typedef enum kla_status {
   KLA_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned          */
   KLA_ERR_WORKSPACE = 4,         /* workspace missing or smaller than needed */
   KLA_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed      */
-  KLA_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up        */
+  KLA_ERR_TIMEOUT = 6            /* reserved: a bounded device-side wait gave
+                                    up. No current entry point has such a wait,
+                                    so none returns this code. */
 } kla_status;
 
 typedef enum kla_dtype { KLA_F32 = 0, KLA_BF16 = 1 } kla_dtype;
@@ -142,9 +149,12 @@ kla_status kla_forward(const void* q, const void* k, const void* v, const void* 
  * (Belangrijkste Bijdragen item 3; "Expliciete Onzekerheid" under the
  * results); this readout exposes it per token. Arguments as for kla_forward, plus
  *   y_var [B,H,T,dv] in `io` (output; required unless B·H·T = 0; must not
- *   overlap y). It costs one more scan pass without the mean (about 0.7×
- *   the forward); it runs before the main pass, so in-place λ0/η0 → λ_T/η_T
- *   updates stay correct. */
+ *   overlap y). The readout is fused into the scan: the same pass produces
+ *   y and y_var (one more multiply-add per element-step and a second
+ *   reduction over d_k). Where that kernel's shared memory would not fit
+ *   (d_k = 128 with 32-column blocks) the library instead
+ *   runs a separate pass without the mean before the main pass, so in-place
+ *   λ0/η0 → λ_T/η_T updates stay correct either way. */
 kla_status kla_forward_uncertainty(const void* q, const void* k, const void* v, const void* lam_v,
                                    const void* a, const void* pbar, const float* lam0, const float* eta0,
                                    void* y, void* y_var, float* lamT, float* etaT,
@@ -177,8 +187,12 @@ kla_status kla_step_gated(const void* q, const void* k, const void* v, const voi
  *   else a multiple of 32).
  *   Returns KLA_ERR_WORKSPACE, before launching anything, when the plan's
  *   workspace (kla_plan with strategy KLA_CHUNKED) exceeds 32 MiB.
- *   The first call on a device looks up the scratch address on that device
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   The first call in each CUDA context (the device's primary context, or a
+ *   context the caller made current) looks up the scratch address in that
+ *   context (cudaGetSymbolAddress) and caches it by context; make that first
+ *   call before any stream capture. After cudaDeviceReset the device has a new
+ *   primary context, so the next call looks the address up again: make it,
+ *   too, outside a capture.
  *   All calls on a device share the scratch: calls whose work overlaps on the
  *   GPU (different streams, unordered host threads) race; order them. */
 kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void* v, const void* lam_v,
@@ -186,6 +200,45 @@ kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void*
                                        const float* eta0, void* y, float* lamT, float* etaT,
                                        int B, int H, int T, int dk, int dv, kla_dtype io,
                                        int chunk_len, void* stream);
+
+/* Context-parallel sharding over T (Methodologie §2 of the summary: the
+ * per-token maps compose associatively, so a sequence can be cut into shards
+ * whose composed maps are exchanged). A shard is a contiguous token range of
+ * the same heads; a rank holding shard r needs only the maps of shards
+ * 0..r-1 to know its start state:
+ *   1. kla_shard_map composes the rank's own shard into one map per element;
+ *   2. the ranks exchange their maps (an all-gather, done by the caller);
+ *   3. kla_shard_start applies the maps of the earlier shards, in order, to
+ *      (λ0, η0), giving the shard's start state;
+ *   4. kla_forward runs the shard from that state (lam0/eta0 = the start).
+ * The result equals one kla_forward over the whole sequence up to fp32
+ * rounding (the same arithmetic as the KLA_CHUNKED strategy).
+ *
+ * kla_shard_map: the composed map of tokens [0, T) of the given inputs,
+ *   per element, in homogeneous coordinates P = n/m, μ = e/m (P = 1/λ,
+ *   μ = η/λ): with (A, B, C, D, E, F, G) = map[0..6], the map takes the
+ *   state (P, μ) before the shard to
+ *       P' = (A P + B) / (C P + D),   μ' = (E P + F + G μ) / (C P + D).
+ *   The seven entries are scaled by a common power of two per element (the
+ *   map is homogeneous, so the scale does not matter).
+ *   Inputs as for kla_forward; gates as kla_options.gates.
+ *   map: fp32 [7][B,H,dk,dv] (output; entry q at map + q·B·H·dk·dv).
+ *   T = 0 writes the identity map. Errors as for kla_forward. */
+kla_status kla_shard_map(const void* q, const void* k, const void* v, const void* lam_v,
+                         const void* a, const void* pbar, float* map, int B, int H, int T, int dk, int dv,
+                         kla_dtype io, int gates, void* stream);
+
+/* kla_shard_start: the start state of the shard that follows n_maps shards.
+ *   maps: fp32 [n_maps][7][B,H,dk,dv], the shards' maps in sequence order
+ *     (as kla_shard_map writes them); n_maps = 0 gives the initial state.
+ *   lam0, eta0: fp32 [B,H,dk,dv] state before the first shard (both NULL:
+ *     λ0 = 1, η0 = 0).
+ *   lam_start, eta_start: fp32 [B,H,dk,dv] outputs; they may alias lam0 /
+ *     eta0 exactly, and must not overlap maps.
+ *   Errors: INVALID_ARG (n_maps < 0, missing pointers, overlaps),
+ *   UNSUPPORTED_SHAPE, MISALIGNED, CUDA. */
+kla_status kla_shard_start(const float* maps, int n_maps, const float* lam0, const float* eta0,
+                           float* lam_start, float* eta_start, int B, int H, int dk, int dv, void* stream);
 
 /* Backward pass: gradients of a scalar loss L through kla_forward. It is the
  * exact reverse-mode derivative of the scan defined in Methodologie §1–§2 of

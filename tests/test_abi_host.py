@@ -254,3 +254,37 @@ def test_gate_bits_are_validated_before_any_cuda_call():
         assert fwd(opt=ctypes.byref(kla.Options(kla.AUTO, 0, 0, g))) == kla.ERR_INVALID_ARG
         assert L.kla_step_gated(P, P, P, P, P, P, P, ctypes.c_void_p(0x50000), P, 1, 1, 16, 16, kla.F32, g,
                                 None) == kla.ERR_INVALID_ARG
+
+
+def test_shard_entry_points_validate_before_any_cuda_call():
+    # kla_shard_map(q, k, v, lam_v, a, pbar, map, B, H, T, dk, dv, io, gates, stream)
+    m = L.kla_shard_map
+    assert m(P, P, P, P, P, P, P, 1, 1, 8, 24, 64, kla.F32, 0, None) == kla.ERR_UNSUPPORTED_SHAPE
+    assert m(P, P, P, P, P, P, P, -1, 1, 8, 64, 64, kla.F32, 0, None) == kla.ERR_INVALID_ARG
+    assert m(P, P, P, P, P, P, None, 1, 1, 8, 64, 64, kla.F32, 0, None) == kla.ERR_INVALID_ARG
+    assert m(P, None, P, P, P, P, P, 1, 1, 8, 64, 64, kla.F32, 0, None) == kla.ERR_INVALID_ARG
+    assert m(P, P, P, P, P, P, MIS, 1, 1, 8, 64, 64, kla.F32, 0, None) == kla.ERR_MISALIGNED
+    assert m(P, P, P, P, P, P, P, 1, 1, 8, 64, 64, 7, 0, None) == kla.ERR_INVALID_ARG
+    assert m(P, P, P, P, P, P, P, 1, 1, 8, 64, 64, kla.F32, 12, None) == kla.ERR_INVALID_ARG  # both p̄ gates
+    assert m(None, None, None, None, None, None, None, 0, 4, 8, 64, 64, kla.F32, 0, None) == kla.OK
+    # kla_shard_start(maps, n_maps, lam0, eta0, lam_start, eta_start, B, H, dk, dv, stream)
+    s = L.kla_shard_start
+    assert s(P, -1, None, None, P, ctypes.c_void_p(0x20000), 1, 1, 64, 64, None) == kla.ERR_INVALID_ARG
+    assert s(None, 2, None, None, P, ctypes.c_void_p(0x20000), 1, 1, 64, 64, None) == kla.ERR_INVALID_ARG
+    assert s(P, 1, P, None, ctypes.c_void_p(0x30000), ctypes.c_void_p(0x40000), 1, 1, 64, 64,
+             None) == kla.ERR_INVALID_ARG                                    # lam0 without eta0
+    assert s(P, 1, None, None, MIS, ctypes.c_void_p(0x40000), 1, 1, 64, 64, None) == kla.ERR_MISALIGNED
+    # outputs overlapping the maps (one map is 7·64·64·4 bytes from 0x10000)
+    assert s(P, 1, None, None, ctypes.c_void_p(0x10000 + 4096), ctypes.c_void_p(0x900000), 1, 1, 64, 64,
+             None) == kla.ERR_INVALID_ARG
+    assert s(P, 1, None, None, ctypes.c_void_p(0x900000), ctypes.c_void_p(0x900000), 1, 1, 64, 64,
+             None) == kla.ERR_INVALID_ARG                                    # lam_start == eta_start
+    assert s(P, 1, None, None, P, P, 1, 1, 24, 64, None) == kla.ERR_UNSUPPORTED_SHAPE
+    assert s(None, 0, None, None, None, None, 0, 3, 64, 64, None) == kla.OK  # empty batch
+
+
+def test_shard_entry_points_without_a_device_report_cuda_error():
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    a, b = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    assert L.kla_shard_start(None, 0, None, None, a, b, 1, 1, 16, 16, None) == kla.ERR_CUDA
