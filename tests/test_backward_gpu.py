@@ -16,7 +16,7 @@ import torch
 import oracle
 from bayesian_filtering_linear_gb300 import kla
 from bayesian_filtering_linear_gb300.inputs import make_inputs, make_workload
-from helpers import to_dev
+from helpers import assert_close, plain_rel, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -52,14 +52,14 @@ def bwd_errors(out: dict, ref: dict, heads=None) -> dict:
             got = got.reshape((B * H,) + got.shape[2:])[np.asarray(list(heads))][:, None]
         want, scale = ref[ORACLE_NAME[n]], ref[ORACLE_NAME[n] + "_scale"]
         errs[n] = float(np.max(np.abs(got - want) / (scale + 1e-30))) if want.size else 0.0
+        errs["rel_" + n] = plain_rel(got, want)
     return errs
 
 
 def check(out, ref, io, what, heads=None):
     errs = bwd_errors(out, ref, heads)
     tol = BWD_TOL[IO[io]]
-    bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"{what}: {errs} exceed {tol}"
+    assert_close(errs, tol, f"backward {what}")
 
 
 def run_both(x, io, gy, glamT, getaT, with_state=True, state_grads=True, heads=None):
@@ -142,10 +142,13 @@ def test_backward_few_heads_split_columns():
 
 
 def test_backward_headline_workload_sampled_heads():
+    """Full headline size; 32 of the 128 heads against the oracle (its
+    per-element reverse pass keeps every forward state, ~0.8 GB of fp64
+    gradients and scales for 32 heads)."""
     x = make_workload("headline")
     B, H, T, dk, dv = 8, 16, 4096, 64, 64
     gy, gl, ge = upstream(B, H, T, dk, dv, "bf16", seed=6)
-    heads = [0, 77, 127]
+    heads = list(range(0, 128, 4))
     out, ref = run_both(x, "bf16", gy, gl, ge, heads=heads)
     check(out, ref, "bf16", "headline", heads=heads)
     for n in GRADS:
@@ -154,10 +157,11 @@ def test_backward_headline_workload_sampled_heads():
 
 def test_backward_long_workload_sampled_head():
     """B1 H16 T65536 d128 bf16 at full size (columns split over blocks, the
-    row-sum pass) against the oracle on one head."""
+    row-sum pass) against the oracle on four heads (one oracle thread per
+    head, ~35 s)."""
     x = make_workload("long")
     B, H, T, dk, dv = 1, 16, 65536, 128, 128
     gy, gl, ge = upstream(B, H, T, dk, dv, "bf16", seed=8)
-    heads = [5]
+    heads = [0, 5, 10, 15]
     out, ref = run_both(x, "bf16", gy, gl, ge, heads=heads)
     check(out, ref, "bf16", "long", heads=heads)
