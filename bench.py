@@ -49,10 +49,14 @@ DESCRIPTIONS = {
     "tiny": "tiny B1 H1 T256 dk16 dv16 fp32 I/O",
     "decode": "decode kla_step B256 H16 dk64 dv64 fp32, state from a 1024-token kla_forward prefix",
 }
-FLOPS_PER_ELEMENT_STEP = 13  # algorithmic count of the printed recursion
+# Algorithmic flops per element-step of the printed recursion (FMA = 2, each
+# reciprocal or division = 1): c = k²Λ^v (1), a² + p̄λ (2), its reciprocal (1),
+# λr + c (2), a·r (1), kΛ^v v (1), fη + b (2), η/λ (1), y += qμ (2).
+FLOPS_PER_ELEMENT_STEP = 13
 # Backward: the checkpointing forward (13) plus the adjoint step as written in
 # kla_backward.cu with the forward quantities it needs recomputed (48).
 BWD_FLOPS_PER_ELEMENT_STEP = 13 + 48
+ORACLE_FLAGS = "g++ -O2 -std=c++17 -fno-fast-math -ffp-contract=off, std::thread over heads"
 L2_FLUSH_BYTES = 256 << 20   # written between steps when a workload's inputs fit in L2
 TRAFFIC_FILES = {"headline": os.path.join(ROOT, "profiles", "traffic_headline.json")}
 KERNEL_SOURCES = [os.path.join(ROOT, "bayesian_filtering_linear_gb300", "csrc", f)
@@ -147,11 +151,55 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_oracle_variants(wname: str, nthreads: int) -> dict:
+    """The oracle's other timed builds on the same recipe, as it stands: fp64
+    on one thread (a sample of heads) and the fp32 build of the same loop on
+    all threads. Returns {name: {value, unit, cores, sample}}."""
+    import oracle
+    from bayesian_filtering_linear_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[wname]
+    out = {}
+    if wname == "decode":
+        return out
+    heads_all = w.B * w.H
+    for name, prec, threads, heads in (("fp64_1_thread", "f64", 1, min(heads_all, 4)),
+                                       ("fp32_all_threads", "f32", nthreads, heads_all)):
+        x = make_inputs(1, heads, w.T, w.dk, w.dv, io=w.io, seed=w.seed, a_logit_mean=w.a_logit_mean)
+        t0 = time.perf_counter()
+        oracle.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
+                       precision=prec, nthreads=threads, want_scales=False)
+        dt = time.perf_counter() - t0
+        used = min(threads, heads)
+        out[name] = {"value": heads * w.T / dt, "unit": "tokens/s", "cores": used,
+                     "sample": f"{heads} heads x {w.T} tokens of the {wname} recipe, {prec} C++ loop, {used} threads"}
+    return out
+
+
 def cpu_oracle_sample(wname: str, nthreads: int) -> tuple[float, dict]:
     """Time the fp64 oracle, as it stands, on a bounded sample of a workload's
     recipe (same shapes per head, fresh draws): whole heads of the forward
     workloads, or 64 single-token steps over all heads for decode. Returns
-    (tokens/s, description)."""
+    (tokens/s, description); the description also carries the CPU model, the
+    compiler flags and the other builds' rates (cpu_oracle_variants)."""
     import oracle
     from bayesian_filtering_linear_gb300.inputs import WORKLOADS, make_inputs
     w = WORKLOADS[wname]
@@ -168,7 +216,7 @@ def cpu_oracle_sample(wname: str, nthreads: int) -> tuple[float, dict]:
         dt = time.perf_counter() - t0
         used = min(nthreads, heads)
         return heads * steps / dt, {
-            "kind": "oracle", "cores": used,
+            "kind": "oracle", "cores": used, "cpu_model": cpu_model(), "compiler": ORACLE_FLAGS,
             "sample": f"{steps} single-token steps over {heads} heads (d_k=d_v={w.dk}), fp64 C++ loop, "
                       f"{used} threads, state converted to fp32 between steps"}
     heads = w.B * w.H
@@ -182,7 +230,9 @@ def cpu_oracle_sample(wname: str, nthreads: int) -> tuple[float, dict]:
     return heads * tokens / dt, {
         "kind": "oracle", "cores": used,
         "sample": f"all {heads} heads x {tokens} tokens of the {wname} recipe (d_k={w.dk}, d_v={w.dv}, "
-                  f"{w.io}-rounded inputs), fp64 C++ loop, {used} threads"}
+                  f"{w.io}-rounded inputs), fp64 C++ loop, {used} threads",
+        "cpu_model": cpu_model(), "compiler": ORACLE_FLAGS,
+        "other_builds": cpu_oracle_variants(wname, nthreads)}
 
 
 def run_reference(args, world, rank):
@@ -315,6 +365,9 @@ def run_kla(args, world, rank, local):
     dev = torch.device("cuda", local)
     wname = args.workload
     w = WORKLOADS[wname]
+    if args.T:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.T)
     if rank == 0:
         x = make_workload(w, device=dev)
     else:  # independent batch per rank
@@ -399,7 +452,8 @@ def run_kla(args, world, rank, local):
         "metric": METRICS[wname], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": DESCRIPTIONS[wname], "B": w.B, "H": w.H,
+        "config": {"workload": DESCRIPTIONS[wname] + (f" (T overridden to {w.T})" if args.T else ""),
+                   "B": w.B, "H": w.H,
                    "T": w.T, "dk": w.dk, "dv": w.dv, "io": w.io, "strategy": plan["strategy"],
                    "chunk_len": plan["chunk_len"], "cols_per_block": plan["cols_per_block"],
                    "rows_per_lane": plan["rows_per_lane"],
@@ -607,6 +661,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("kla", "reference"), default="kla")
     ap.add_argument("--workload", choices=tuple(METRICS), default="headline")
     ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward")
+    ap.add_argument("--T", type=int, default=0,
+                    help="override the workload's sequence length (for profiling a smaller case of its shape)")
     args = ap.parse_args(argv)
     world, rank, local = dist_info()
     if world > 1:
