@@ -380,7 +380,8 @@ def run_kla(args, world, rank, local):
     if args.pass_ == "backward":
         return run_kla_backward(args, world, rank, local, w, x, stream)
 
-    plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io)
+    fwd_opt = {"strategy": args.strategy, "chunk_len": args.chunk_len}
+    plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io, **fwd_opt)
     ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev) if plan["workspace_bytes"] else None
     y = torch.empty((w.B, w.H, w.T, w.dv), dtype=x["q"].dtype, device=dev)
     lamT = torch.empty_like(x["lam0"])
@@ -394,7 +395,7 @@ def run_kla(args, world, rank, local):
 
     def step():
         kla.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
-                    y=y, lamT=lamT, etaT=etaT, workspace=ws, stream=stream)
+                    y=y, lamT=lamT, etaT=etaT, workspace=ws, stream=stream, **fwd_opt)
 
     total_ms, per_launch_ms, clocks = timed_steps(step, args, world, local, stream, flush)
     # With a flush between steps the step time is the launch time (events
@@ -420,7 +421,7 @@ def run_kla(args, world, rank, local):
     def compute(b, s):
         d, (yb, lb, eb) = devb[b], outs[b]
         kla.forward(d["q"], d["k"], d["v"], d["lam_v"], d["a"], d["pbar"], d["lam0"], d["eta0"],
-                    y=yb, lamT=lb, etaT=eb, workspace=ws, stream=s)
+                    y=yb, lamT=lb, etaT=eb, workspace=ws, stream=s, **fwd_opt)
 
     def copy_out(b, s):
         for t_h, t in zip(outs_h[b], outs[b]):
@@ -663,6 +664,10 @@ def main(argv=None):
     ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward")
     ap.add_argument("--T", type=int, default=0,
                     help="override the workload's sequence length (for profiling a smaller case of its shape)")
+    ap.add_argument("--strategy", choices=("auto", "sequential", "chunked"), default="auto",
+                    help="force the forward's strategy (default: the planner's choice)")
+    ap.add_argument("--chunk-len", dest="chunk_len", type=int, default=0,
+                    help="tokens per chunk with --strategy chunked (0: the planner's choice)")
     args = ap.parse_args(argv)
     world, rank, local = dist_info()
     if world > 1:
