@@ -452,7 +452,7 @@ def run_kla(args, world, rank, local):
     print(json.dumps({
         "metric": METRICS[wname], "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32", "io_dtype": w.io, "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[wname] + (f" (T overridden to {w.T})" if args.T else ""),
                    "B": w.B, "H": w.H,
                    "T": w.T, "dk": w.dk, "dv": w.dv, "io": w.io, "strategy": plan["strategy"],
