@@ -106,3 +106,28 @@ def make_workload(w: Workload | str, *, device: str | torch.device = "cpu", **kw
         w = WORKLOADS[w]
     return make_inputs(w.B, w.H, w.T, w.dk, w.dv, io=w.io, seed=w.seed,
                        a_logit_mean=w.a_logit_mean, device=device, **kw)
+
+
+def make_conv_inputs(B: int, H: int, T: int, D: int, W: int, *, io: str = "f32", seed: int = 0,
+                     device: str | torch.device = "cpu") -> dict:
+    """Seeded inputs of the causal convolution that feeds the scan: x
+    ``[B,H,T,D]`` ~ N(0, 1) and the carried window ``[B,H,W-1,D]`` ~ N(0, 1)
+    in the I/O dtype; fp32 taps ``[H,D,W]`` ~ N(0, 1/W) and bias ``[H,D]`` ~
+    N(0, 1/4); and, for the backward, gy ``[B,H,T,D]`` ~ N(0, 1) and
+    gwindow_out ``[B,H,W-1,D]`` ~ N(0, 1) in the I/O dtype. Draw order: x,
+    window, weight, bias, gy, gwindow_out."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, dtype=torch.float32, device=dev)
+
+    dt = _DTYPES[io]
+    x = randn(B, H, T, D).to(dt).contiguous()
+    window = randn(B, H, W - 1, D).to(dt).contiguous()
+    weight = (randn(H, D, W) * W ** -0.5).contiguous()
+    bias = (randn(H, D) * 0.5).contiguous()
+    gy = randn(B, H, T, D).to(dt).contiguous()
+    gwindow_out = randn(B, H, W - 1, D).to(dt).contiguous()
+    return {"x": x, "window": window, "weight": weight, "bias": bias, "gy": gy, "gwindow_out": gwindow_out}

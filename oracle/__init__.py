@@ -15,6 +15,9 @@ Contents
   optionally dL/dλ_T, dL/dη_T), with condition scales.
 * :mod:`oracle.exact` — exact-rational information-form Möbius recursion and
   dense Gaussian conditioning of the joint chain, used to pin the C++ loop.
+* :mod:`oracle.gates` — the gate activations of the inputs and their chain rule.
+* :mod:`oracle.conv` — the causal depthwise convolution with SiLU of the block
+  around the scan (Methodologie §4), forward and backward, in fp64 numpy.
 
 Source: "Technische Samenvatting: Kalman Linear Attention (KLA)"
 (gist.science/nl/paper/2602.10743), Methodologie §1 (model) and §2 (Möbius
