@@ -220,6 +220,23 @@ bool overlaps_partially(const void* x, const void* y, size_t bytes) {
   return a < b + bytes && b < a + bytes;
 }
 
+// Byte ranges [x, x + nx) and [y, y + ny) intersect (null or empty ranges never do).
+bool ranges_overlap(const void* x, size_t nx, const void* y, size_t ny) {
+  if (!x || !y || nx == 0 || ny == 0) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(x), b = reinterpret_cast<uintptr_t>(y);
+  return a < b + ny && b < a + nx;
+}
+
+// Shape checks of the causal convolution entry points.
+kla_status check_conv_shape(int B, int H, int T, int D, int W) {
+  if (B < 0 || H < 0 || T < 0) return KLA_ERR_INVALID_ARG;
+  if (D < 4 || D > 1024 || D % 4 != 0 || W < 1 || W > 8) return KLA_ERR_UNSUPPORTED_SHAPE;
+  const long long bh = (long long)B * H;
+  if (bh > INT_MAX) return KLA_ERR_UNSUPPORTED_SHAPE;
+  if (bh > 0 && (long long)T > (1LL << 46) / (bh * D)) return KLA_ERR_UNSUPPORTED_SHAPE;
+  return KLA_OK;
+}
+
 void fill_info(const Plan& p, kla_plan_info* out) {
   out->strategy = p.strategy;
   out->chunk_len = p.chunk_len;
@@ -540,6 +557,100 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
                       gpbar, gv, glam_v, glam0, geta0, B, H, T, dk, dv, (int)io, gates};
   const cudaError_t e = kla::launch_backward(f, b, workspace, s);
   return e == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+kla_status kla_conv(const void* x, const float* weight, const float* bias, const void* window_in, void* y,
+                    void* window_out, int B, int H, int T, int D, int W, kla_dtype io, int activation,
+                    void* stream) {
+  // ---- validation: no CUDA call before it passes ---------------------------
+  kla_status st = check_conv_shape(B, H, T, D, W);
+  if (st != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  if (activation != KLA_ACT_NONE && activation != KLA_ACT_SILU) return KLA_ERR_INVALID_ARG;
+  if (W == 1) window_in = window_out = nullptr;  // empty windows
+  const long long bh = (long long)B * H;
+  if (bh > 0 && !weight) return KLA_ERR_INVALID_ARG;
+  if (bh * T > 0 && (!x || !y)) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, weight, bias, window_in, y, window_out};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  const size_t xb = (size_t)bh * T * D * io_size(io), wb = (size_t)bh * (W - 1) * D * io_size(io);
+  const size_t tb = (size_t)H * D * W * sizeof(float), bb = (size_t)H * D * sizeof(float);
+  const void* ins[] = {x, weight, bias, window_in};
+  const size_t in_bytes[] = {xb, tb, bb, wb};
+  for (int i = 0; i < 4; ++i) {
+    if (ranges_overlap(y, xb, ins[i], in_bytes[i])) return KLA_ERR_INVALID_ARG;
+    if (i != 3 && ranges_overlap(window_out, wb, ins[i], in_bytes[i])) return KLA_ERR_INVALID_ARG;
+  }
+  if (overlaps_partially(window_out, window_in, wb) || ranges_overlap(window_out, wb, y, xb))
+    return KLA_ERR_INVALID_ARG;
+  if (bh == 0) return KLA_OK;
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  const kla::ConvPlan p = kla::conv_plan(bh, T, D, W, sms);
+  kla::ConvArgs a{};
+  a.x = x; a.weight = weight; a.bias = bias; a.win = window_in; a.y = y; a.wout = window_out;
+  a.B = B; a.H = H; a.T = T; a.D = D; a.W = W; a.io = (int)io; a.act = activation;
+  a.L = p.L; a.chunks_per_block = p.chunks_per_block;
+  return kla::launch_conv(a, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+}
+
+size_t kla_conv_backward_workspace_size(int B, int H, int T, int D, int W) {
+  if (check_conv_shape(B, H, T, D, W) != KLA_OK) return (size_t)-1;
+  const long long bh = (long long)B * H;
+  if (bh == 0) return 0;
+  int sms = 0;
+  if (device_sms(&sms) != KLA_OK) return (size_t)-1;
+  return kla::conv_partial_bytes(B, H, D, W, kla::conv_plan(bh, T, D, W, sms));
+}
+
+kla_status kla_conv_backward(const void* x, const float* weight, const float* bias, const void* window_in,
+                             const void* gy, const void* gwindow_out, void* gx, float* gweight, float* gbias,
+                             void* gwindow, int B, int H, int T, int D, int W, kla_dtype io, int activation,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  // ---- validation: no CUDA call before it passes ---------------------------
+  kla_status st = check_conv_shape(B, H, T, D, W);
+  if (st != KLA_OK) return st;
+  if (io != KLA_F32 && io != KLA_BF16) return KLA_ERR_INVALID_ARG;
+  if (activation != KLA_ACT_NONE && activation != KLA_ACT_SILU) return KLA_ERR_INVALID_ARG;
+  if (W == 1) window_in = gwindow_out = gwindow = nullptr;  // empty windows
+  const long long bh = (long long)B * H;
+  if (bh > 0 && !weight) return KLA_ERR_INVALID_ARG;
+  if (bh * T > 0 && (!x || !gx)) return KLA_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, weight, bias, window_in, gy, gwindow_out, gx, gweight, gbias, gwindow, workspace};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return KLA_ERR_MISALIGNED;
+  const size_t xb = (size_t)bh * T * D * io_size(io), wb = (size_t)bh * (W - 1) * D * io_size(io);
+  const size_t tb = (size_t)H * D * W * sizeof(float), bb = (size_t)H * D * sizeof(float);
+  const void* ins[] = {x, weight, bias, window_in, gy, gwindow_out};
+  const size_t in_bytes[] = {xb, tb, bb, wb, xb, wb};
+  const void* outs[] = {gx, gweight, gbias, gwindow};
+  const size_t out_bytes[] = {xb, tb, bb, wb};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (ranges_overlap(outs[o], out_bytes[o], ins[i], in_bytes[i])) return KLA_ERR_INVALID_ARG;
+    for (int p = o + 1; p < 4; ++p)
+      if (ranges_overlap(outs[o], out_bytes[o], outs[p], out_bytes[p])) return KLA_ERR_INVALID_ARG;
+  }
+  const bool want_sums = gweight || gbias;
+  if (bh == 0 && !(want_sums && H > 0)) return KLA_OK;
+  int sms = 0;
+  if ((st = device_sms(&sms)) != KLA_OK) return st;
+  const kla::ConvPlan p = kla::conv_plan(bh, T, D, W, sms);
+  const size_t part_bytes = bh > 0 ? kla::conv_partial_bytes(B, H, D, W, p) : 0;
+  if (want_sums && part_bytes > 0 && (!workspace || ws_bytes < part_bytes)) return KLA_ERR_WORKSPACE;
+  if (want_sums && part_bytes > 0)
+    for (int o = 0; o < 4; ++o)
+      if (ranges_overlap(workspace, part_bytes, outs[o], out_bytes[o])) return KLA_ERR_INVALID_ARG;
+  kla::ConvArgs a{};
+  a.x = x; a.weight = weight; a.bias = bias; a.win = window_in;
+  a.gy = gy; a.gwout = gwindow_out; a.gx = gx; a.gwin = gwindow; a.gweight = gweight; a.gbias = gbias;
+  a.part = want_sums && part_bytes > 0 ? reinterpret_cast<float*>(workspace) : nullptr;
+  a.nparts = bh > 0 ? (long long)B * p.blocks_y : 0;
+  a.B = B; a.H = H; a.T = T; a.D = D; a.W = W; a.io = (int)io; a.act = activation;
+  a.L = p.L; a.chunks_per_block = p.chunks_per_block;
+  return kla::launch_conv_backward(a, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KLA_OK
+                                                                                                : KLA_ERR_CUDA;
 }
 
 }  // extern "C"

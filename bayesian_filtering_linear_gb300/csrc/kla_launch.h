@@ -98,4 +98,31 @@ struct StepArgs {
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 
+// Causal depthwise convolution with optional SiLU (kla_conv.cu), forward and
+// backward. x, y, gy, gx: [B,H,T,D] io; weight [H,D,W], bias [H,D] fp32;
+// windows [B,H,W-1,D] io. Null optional pointers mean zeros / not wanted.
+struct ConvArgs {
+  const void* x;
+  const float *weight, *bias;
+  const void* win;    // carried inputs before token 0
+  void *y, *wout;     // forward outputs
+  const void *gy, *gwout;
+  void *gx, *gwin;    // backward outputs (io)
+  float *gweight, *gbias;
+  float* part;        // backward block partials [H][nparts][D][W+1], or null (no gweight/gbias)
+  long long nparts;   // B · blocks along T
+  int B, H, T, D, W;
+  int io, act;
+  int L, chunks_per_block;  // tokens per thread chunk; chunks per block
+};
+struct ConvPlan {
+  int L, chunks_per_block, threads, blocks_y;
+  long long nparts;
+  size_t smem_bwd;
+};
+ConvPlan conv_plan(long long bh, int T, int D, int W, int num_sms);
+size_t conv_partial_bytes(int B, int H, int D, int W, const ConvPlan& p);
+cudaError_t launch_conv(const ConvArgs& a, const ConvPlan& p, cudaStream_t s);
+cudaError_t launch_conv_backward(const ConvArgs& a, const ConvPlan& p, cudaStream_t s);
+
 }  // namespace kla

@@ -25,7 +25,8 @@ _IO = {torch.float32: F32, torch.bfloat16: BF16}
 EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_forward", "kla_step",
            "kla_status_string", "kla_version", "kla_forward_chunked_noalloc", "kla_backward_workspace_size",
            "kla_backward", "kla_forward_uncertainty", "kla_step_gated", "kla_backward_plan_for_sms",
-           "kla_shard_map", "kla_shard_start")
+           "kla_shard_map", "kla_shard_start", "kla_conv", "kla_conv_backward_workspace_size",
+           "kla_conv_backward")
 
 
 class Options(ctypes.Structure):
@@ -81,6 +82,12 @@ def load_library(path: str = LIB_PATH):
     lib.kla_shard_map.argtypes = [vp] * 7 + [i] * 7 + [vp]
     lib.kla_shard_start.restype = i
     lib.kla_shard_start.argtypes = [vp, i, vp, vp, vp, vp, i, i, i, i, vp]
+    lib.kla_conv.restype = i
+    lib.kla_conv.argtypes = [vp] * 6 + [i] * 7 + [vp]
+    lib.kla_conv_backward_workspace_size.restype = sz
+    lib.kla_conv_backward_workspace_size.argtypes = [i] * 5
+    lib.kla_conv_backward.restype = i
+    lib.kla_conv_backward.argtypes = [vp] * 10 + [i] * 7 + [vp, sz, vp]
     return lib
 
 
@@ -368,3 +375,94 @@ def forward_context_parallel(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, g
     maps = exchange_maps(local, group)
     lam_s, eta_s = shard_start(maps[:rank].contiguous(), lam0, eta0, stream=stream)
     return forward(q, k, v, lam_v, a, pbar, lam_s, eta_s, gates=gates, stream=stream, **forward_kw)
+
+
+# ---- causal depthwise convolution with SiLU (the block around the scan) -------
+
+ACT_NONE, ACT_SILU = 0, 1
+
+
+def _conv_shapes(x, weight, window, W):
+    B, H, T, D = x.shape
+    if tuple(weight.shape) != (H, D, W):
+        raise ValueError(f"weight has shape {tuple(weight.shape)}, expected {(H, D, W)}")
+    return B, H, T, D
+
+
+def conv(x, weight, bias=None, window=None, *, activation: int = ACT_SILU, y=None, window_out=None,
+         update_window: bool = False, stream=None):
+    """Causal depthwise convolution of ``x`` ``[B,H,T,D]`` with taps ``weight``
+    ``[H,D,W]`` (fp32; tap W-1 multiplies the current token), optional
+    ``bias`` ``[H,D]`` and SiLU (kla_conv). ``window`` ``[B,H,W-1,D]`` holds
+    the W-1 inputs before the first token (None: zeros). Returns ``(y,
+    window_out)``; with ``update_window`` the window is updated in place and
+    returned as window_out."""
+    W = weight.shape[-1]
+    B, H, T, D = _conv_shapes(x, weight, window, W)
+    dev, dt = x.device, x.dtype
+    if dt not in _IO:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    _need(weight, "weight", torch.float32, (H, D, W), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (H, D), dev)
+    wshape = (B, H, W - 1, D)
+    if window is not None:
+        _need(window, "window", dt, wshape, dev)
+    if y is None:
+        y = torch.empty((B, H, T, D), dtype=dt, device=dev)
+    else:
+        _need(y, "y", dt, (B, H, T, D), dev)
+    if update_window:
+        if window is None:
+            raise ValueError("update_window needs a window")
+        window_out = window
+    elif window_out is None:
+        window_out = torch.empty(wshape, dtype=dt, device=dev)
+    else:
+        _need(window_out, "window_out", dt, wshape, dev)
+    with torch.cuda.device(dev):
+        st = LIB.kla_conv(_ptr(x), _ptr(weight), _ptr(bias), _ptr(window), _ptr(y), _ptr(window_out),
+                          B, H, T, D, W, _IO[dt], int(activation), _stream(stream))
+    _check(st, "kla_conv")
+    return y, window_out
+
+
+def conv_backward(x, weight, bias=None, window=None, *, gy=None, gwindow_out=None, activation: int = ACT_SILU,
+                  param_grads: bool = True, window_grad: bool = True, workspace=None, stream=None):
+    """Gradients through :func:`conv` (kla_conv_backward) given ``gy`` = dL/dy
+    and optionally ``gwindow_out`` = dL/d(window out). Returns a dict with
+    ``gx`` and, with ``window_grad``, ``gwindow`` (I/O dtype), and with
+    ``param_grads`` ``gweight`` ``[H,D,W]`` and ``gbias`` ``[H,D]`` (fp32)."""
+    W = weight.shape[-1]
+    B, H, T, D = _conv_shapes(x, weight, window, W)
+    dev, dt = x.device, x.dtype
+    if dt not in _IO:
+        raise TypeError(f"unsupported I/O dtype {dt}")
+    _need(weight, "weight", torch.float32, (H, D, W), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float32, (H, D), dev)
+    wshape = (B, H, W - 1, D)
+    for name, t in (("window", window), ("gwindow_out", gwindow_out)):
+        if t is not None:
+            _need(t, name, dt, wshape, dev)
+    if gy is not None:
+        _need(gy, "gy", dt, (B, H, T, D), dev)
+    out = {"gx": torch.empty((B, H, T, D), dtype=dt, device=dev)}
+    if window_grad:
+        out["gwindow"] = torch.empty(wshape, dtype=dt, device=dev)
+    if param_grads:
+        out["gweight"] = torch.empty((H, D, W), dtype=torch.float32, device=dev)
+        out["gbias"] = torch.empty((H, D), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        if workspace is None and param_grads:
+            nbytes = LIB.kla_conv_backward_workspace_size(B, H, T, D, W)
+            if nbytes == ctypes.c_size_t(-1).value:
+                raise KlaError(ERR_CUDA, "kla_conv_backward_workspace_size")
+            workspace = torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = LIB.kla_conv_backward(_ptr(x), _ptr(weight), _ptr(bias), _ptr(window), _ptr(gy), _ptr(gwindow_out),
+                                   _ptr(out["gx"]), _ptr(out.get("gweight")), _ptr(out.get("gbias")),
+                                   _ptr(out.get("gwindow")), B, H, T, D, W, _IO[dt], int(activation),
+                                   _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "kla_conv_backward")
+    return out

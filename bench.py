@@ -1,7 +1,8 @@
 """Benchmark of the KLA scan (one JSON line).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kla|reference]
-                    [--workload headline|medium|long|tiny|decode] [--pass forward|backward]
+                    [--workload headline|medium|long|tiny|decode]
+                    [--pass forward|backward|conv|conv_backward]
 
 By default a step is one kla_forward over the headline workload — B=8, H=16,
 T=4096, d_k=d_v=64, bf16 inputs/outputs, fp32 state — with inputs resident
@@ -17,6 +18,9 @@ the slowest rank's time.
 
 ``--pass backward`` times kla_backward instead (gradients of every input for a
 random dL/dy and dL/dλ_T, dL/dη_T) on the same forward workloads.
+``--pass conv`` times the block's causal convolution with SiLU on the
+workload's q, k and v streams (kla_conv, width 4, one launch each);
+``--pass conv_backward`` its backward (kla_conv_backward).
 
 ``--impl reference`` times the fp64 CPU oracle (the stand-in reference arm,
 on this host's cores) on a bounded sample of the same workload.
@@ -379,6 +383,8 @@ def run_kla(args, world, rank, local):
         return run_kla_decode(args, world, rank, local, w, x, stream)
     if args.pass_ == "backward":
         return run_kla_backward(args, world, rank, local, w, x, stream)
+    if args.pass_ in ("conv", "conv_backward"):
+        return run_conv(args, world, rank, local, w, stream, backward=args.pass_ == "conv_backward")
 
     fwd_opt = {"strategy": args.strategy, "chunk_len": args.chunk_len}
     plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io, **fwd_opt)
@@ -634,6 +640,136 @@ def run_kla_backward(args, world, rank, local, w, x, stream):
     }), flush=True)
 
 
+CONV_TAPS = 4  # kernel width of the block's causal convolution (the pages give none; 4 as in Mamba-style blocks)
+
+
+def run_conv(args, world, rank, local, w, stream, backward: bool):
+    """The block's convolution prologue on the workload's streams: q, k and v
+    (``[B,H,T,d]``) each through kla_conv with its own taps, bias and SiLU
+    (three launches per step), or through kla_conv_backward (gradients of the
+    input, taps and bias). HBM-bound: reported against the measured copy
+    bandwidth."""
+    import torch
+    from bayesian_filtering_linear_gb300 import kla
+    from bayesian_filtering_linear_gb300.inputs import make_conv_inputs
+    dev = torch.device("cuda", local)
+    W = CONV_TAPS
+    dims = {"q": w.dk, "k": w.dk, "v": w.dv}
+    s = {n: make_conv_inputs(w.B, w.H, w.T, d, W, io=w.io, seed=w.seed + 100 * i + 1000 * rank, device=dev)
+         for i, (n, d) in enumerate(dims.items())}
+    ys = {n: torch.empty_like(s[n]["x"]) for n in dims}
+    wos = {n: torch.empty_like(s[n]["window"]) for n in dims}  # window after the last token
+    ws = {}
+    if backward:
+        for n, d in dims.items():
+            ws[n] = torch.empty(max(16, kla.LIB.kla_conv_backward_workspace_size(w.B, w.H, w.T, d, W)),
+                                dtype=torch.uint8, device=dev)
+
+    def run_one(n, src, out, s_):
+        if backward:
+            return kla.conv_backward(src["x"], src["weight"], src["bias"], None, gy=src["gy"], window_grad=False,
+                                     workspace=ws[n], stream=s_)
+        return kla.conv(src["x"], src["weight"], src["bias"], None, y=out, window_out=wos[n] if out is not None else None,
+                        stream=s_)
+
+    def step():
+        for n in dims:
+            run_one(n, s[n], ys[n], stream)
+
+    in_bytes = sum(s[n]["x"].numel() * s[n]["x"].element_size() for n in dims)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = None
+    if in_bytes * (3 if backward else 2) < 2 * l2:
+        scratch = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = lambda: scratch.fill_(1.0)
+    total_ms, per_launch_ms, clocks = timed_steps(step, args, world, local, stream, flush)
+    ms_per_step = per_launch_ms if flush else total_ms / args.steps
+    tokens = w.B * w.H * w.T
+    value = tokens * world / (ms_per_step * 1e-3)
+
+    # end to end: the streams (and gy) in from pinned host memory, the results out
+    keys = ("x", "gy") if backward else ("x",)
+    host = {n: {k: s[n][k].cpu().pin_memory() for k in keys} for n in dims}
+    nb = E2E_BUFFERS
+    devb = [{n: {k: torch.empty_like(s[n][k]) for k in keys} for n in dims} for _ in range(nb)]
+    results = [None] * nb
+    sample = {n: run_one(n, s[n], ys[n], stream) for n in dims}
+    flat = lambda r: list(r.values()) if isinstance(r, dict) else [r[0]]
+    outs_h = [{n: [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in flat(sample[n])] for n in dims}
+              for _ in range(nb)]
+    h2d = sum(t.numel() * t.element_size() for n in dims for t in host[n].values())
+    d2h = sum(t.numel() * t.element_size() for n in dims for t in outs_h[0][n])
+
+    def copy_in(b, s_):
+        for n in dims:
+            for k in keys:
+                devb[b][n][k].copy_(host[n][k], non_blocking=True)
+
+    def compute(b, s_):
+        results[b] = {n: run_one(n, dict(s[n], **devb[b][n]), None, s_) for n in dims}
+
+    def copy_out(b, s_):
+        for n in dims:
+            for t_h, t in zip(outs_h[b][n], flat(results[b][n])):
+                t.record_stream(s_)
+                t_h.copy_(t, non_blocking=True)
+
+    e2e_ms = pipelined_e2e(copy_in, compute, copy_out, args, world, stream)
+    if rank != 0:
+        return
+    esz = s["q"]["x"].element_size()
+    # algorithmic bytes: every stream element read once (and gy) and its output written once; taps and bias
+    elems = sum(w.B * w.H * w.T * d for d in dims.values())
+    params = sum(w.H * d * (W + 1) * 4 for d in dims.values())
+    alg_bytes = elems * esz * (3 if backward else 2) + params * (2 if backward else 1)
+    peaks = measured_peaks()
+    peak_gbs = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
+    cpu_value, cpu_desc = cpu_oracle_conv_sample(w, W, backward)
+    name = "backward of the causal convolution" if backward else "causal convolution + SiLU"
+    print(json.dumps({
+        "metric": METRICS[w.name].replace("KLA scan tokens/s", f"KLA block {name} of q, k, v: tokens/s"),
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "io_dtype": w.io, "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[w.name] + f"; {name} of q, k and v (width {W}, own taps each)",
+                   "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv, "io": w.io, "taps": W,
+                   "l2": (f"streams fit in L2: {L2_FLUSH_BYTES >> 20} MB written between steps" if flush
+                          else "streams larger than L2; no flush"),
+                   "parallelism": f"{world} independent batches"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s",
+                     "frac": achieved / peak_gbs, "traffic": None,
+                     "kernel": "kla_conv_bwd_kernel + finish" if backward else "kla_conv_kernel",
+                     "kernel_ms": per_launch_ms, "launches_per_step": 6 if backward else 3,
+                     "peak_basis": "measured copy bandwidth", "bytes_per_step": alg_bytes},
+        "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
+        "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": E2E_OVERLAP},
+        "gpu_launches": (6 if backward else 3) * args.steps,
+        "clocks": clocks.summary(),
+    }), flush=True)
+
+
+def cpu_oracle_conv_sample(w, W: int, backward: bool) -> tuple[float, dict]:
+    """The fp64 numpy oracle of the convolution, as it stands, on 16 heads × up
+    to 1024 tokens of q, k and v of the workload. Returns (tokens/s, description)."""
+    from bayesian_filtering_linear_gb300.inputs import make_conv_inputs
+    from oracle import conv as C
+    heads, tokens = min(16, w.B * w.H), min(w.T, 1024)
+    t_total = 0.0
+    for i, d in enumerate((w.dk, w.dk, w.dv)):
+        p = {k: v.double().numpy() for k, v in make_conv_inputs(1, heads, tokens, d, W, io=w.io, seed=i).items()}
+        t0 = time.perf_counter()
+        if backward:
+            C.conv_backward(p["x"], p["weight"][:heads], p["bias"][:heads], None, p["gy"])
+        else:
+            C.conv(p["x"], p["weight"][:heads], p["bias"][:heads])
+        t_total += time.perf_counter() - t0
+    return heads * tokens / t_total, {"kind": "oracle", "cores": 1,
+                                      "sample": f"{heads} heads x {tokens} tokens of q, k and v of the {w.name} "
+                                                f"recipe, fp64 numpy oracle (one thread)"}
+
+
 def cpu_oracle_backward_sample(w, nthreads: int) -> tuple[float, dict]:
     """The fp64 oracle's backward, as it stands, on 16 heads of the recipe
     (up to 1024 tokens). Returns (tokens/s, description)."""
@@ -661,7 +797,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("kla", "reference"), default="kla")
     ap.add_argument("--workload", choices=tuple(METRICS), default="headline")
-    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward"), default="forward")
+    ap.add_argument("--pass", dest="pass_", choices=("forward", "backward", "conv", "conv_backward"),
+                    default="forward")
     ap.add_argument("--T", type=int, default=0,
                     help="override the workload's sequence length (for profiling a smaller case of its shape)")
     ap.add_argument("--strategy", choices=("auto", "sequential", "chunked"), default="auto",

@@ -287,6 +287,57 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
                         float* glam0, float* geta0, int B, int H, int T, int dk, int dv,
                         kla_dtype io, int gates, void* workspace, size_t ws_bytes, void* stream);
 
+/* Causal depthwise 1-D convolution with an optional SiLU: the short
+ * convolution of the Mamba-like block that the KLA layer sits in
+ * (Methodologie §4 "Architectuur" of the summary: 1-D causal convolutions and
+ * SiLU activations around the scan; the summary gives neither the width nor
+ * the weights, so both are arguments). It maps a [B,H,T,D] stream — e.g. the
+ * projections that become q, k or v, each with its own taps — channel by
+ * channel (channel = (h, d)):
+ *     u[t] = bias[h,d] + Σ_{k<W} weight[h,d,k] · x[t − (W−1) + k]
+ *     y[t] = SiLU(u[t]) = u[t] / (1 + e^(−u[t]))   (KLA_ACT_SILU), or u[t] (KLA_ACT_NONE)
+ * Tap W−1 multiplies the current token, so weight[h,d,:] is the layout of a
+ * depthwise torch Conv1d weight [H·D, 1, W] with left padding. Inputs before
+ * token 0 come from a carried window of the W−1 previous inputs, so a
+ * sequence cut into pieces — down to one token per call for decoding — gives
+ * the same result as one call.
+ *   x, y [B,H,T,D] in `io`; y must not overlap any input.
+ *   weight [H,D,W] fp32 (required when B·H > 0); bias [H,D] fp32 or NULL (0).
+ *   window_in [B,H,W−1,D] in `io`: inputs of tokens −(W−1)…−1 (NULL: zeros).
+ *   window_out [B,H,W−1,D] in `io` or NULL: the last W−1 inputs of
+ *     (window_in, x), the window_in of the next call. It may be window_in
+ *     itself (an in-place update) but must not overlap it otherwise, nor x or y.
+ *   With W = 1 the windows are empty and their pointers are ignored.
+ *   D: a multiple of 4 in [4, 1024]; W in [1, 8] (else UNSUPPORTED_SHAPE);
+ *   B, H, T ≥ 0 (T = 0 only copies the window). activation: kla_activation
+ *   (else INVALID_ARG). Pointers 16-byte aligned (else MISALIGNED). */
+typedef enum kla_activation { KLA_ACT_NONE = 0, KLA_ACT_SILU = 1 } kla_activation;
+
+kla_status kla_conv(const void* x, const float* weight, const float* bias, const void* window_in, void* y,
+                    void* window_out, int B, int H, int T, int D, int W, kla_dtype io, int activation,
+                    void* stream);
+
+/* Backward of kla_conv for a loss L, given gy = dL/dy [B,H,T,D] (`io`; NULL:
+ * zero) and gwindow_out = dL/d(window_out) [B,H,W−1,D] (`io`; NULL: zero).
+ *   Forward arguments (x, weight, bias, window_in, W, activation) as in the
+ *   kla_conv call being differentiated.
+ *   gx [B,H,T,D] in `io` (required when B·H·T > 0): dL/dx.
+ *   gwindow [B,H,W−1,D] in `io` or NULL: dL/d(window_in).
+ *   gweight [H,D,W] and gbias [H,D] fp32, each NULL to skip: dL/dweight and
+ *     dL/dbias, summed over B and T. The sums run in a fixed order (no
+ *     atomics), so repeated calls give identical bits.
+ *   Outputs are written, not accumulated, and must not overlap any input or
+ *   each other.
+ *   workspace / ws_bytes: device scratch of at least
+ *     kla_conv_backward_workspace_size() bytes when gweight or gbias is wanted
+ *     (else KLA_ERR_WORKSPACE); may be NULL otherwise.
+ * Shape, alignment and error rules as for kla_conv. */
+size_t kla_conv_backward_workspace_size(int B, int H, int T, int D, int W);
+kla_status kla_conv_backward(const void* x, const float* weight, const float* bias, const void* window_in,
+                             const void* gy, const void* gwindow_out, void* gx, float* gweight, float* gbias,
+                             void* gwindow, int B, int H, int T, int D, int W, kla_dtype io, int activation,
+                             void* workspace, size_t ws_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kla_status_string(kla_status s);
 

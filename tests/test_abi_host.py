@@ -288,3 +288,78 @@ def test_shard_entry_points_without_a_device_report_cuda_error():
         pytest.skip("a device is present")
     a, b = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
     assert L.kla_shard_start(None, 0, None, None, a, b, 1, 1, 16, 16, None) == kla.ERR_CUDA
+
+
+def conv_call(B=1, H=1, T=8, D=16, W=4, io=kla.F32, act=kla.ACT_SILU, x=None, weight=None, bias=None,
+              win=None, y=None, wout=None):
+    """kla_conv with distinct, non-overlapping placeholder regions by default."""
+    x = ctypes.c_void_p(0x100000) if x is None else x
+    weight = ctypes.c_void_p(0x200000) if weight is None else weight
+    y = ctypes.c_void_p(0x300000) if y is None else y
+    return L.kla_conv(x, weight, bias, win, y, wout, B, H, T, D, W, io, act, None)
+
+
+def test_conv_validates_before_any_cuda_call():
+    assert conv_call(D=6) == kla.ERR_UNSUPPORTED_SHAPE       # not a multiple of 4
+    assert conv_call(D=2048) == kla.ERR_UNSUPPORTED_SHAPE
+    assert conv_call(W=0) == kla.ERR_UNSUPPORTED_SHAPE
+    assert conv_call(W=9) == kla.ERR_UNSUPPORTED_SHAPE
+    assert conv_call(T=-1) == kla.ERR_INVALID_ARG
+    assert conv_call(io=5) == kla.ERR_INVALID_ARG
+    assert conv_call(act=2) == kla.ERR_INVALID_ARG
+    assert conv_call(weight=ctypes.c_void_p(0)) == kla.ERR_INVALID_ARG
+    assert conv_call(x=ctypes.c_void_p(0)) == kla.ERR_INVALID_ARG
+    assert conv_call(y=ctypes.c_void_p(0)) == kla.ERR_INVALID_ARG
+    assert conv_call(bias=MIS) == kla.ERR_MISALIGNED
+    assert conv_call(win=MIS) == kla.ERR_MISALIGNED
+    # y over x (8 tokens × 16 channels × 4 bytes from 0x100000)
+    assert conv_call(y=ctypes.c_void_p(0x100000 + 256)) == kla.ERR_INVALID_ARG
+    # window out over x, partially over the window in, over y
+    assert conv_call(win=ctypes.c_void_p(0x400000), wout=ctypes.c_void_p(0x100000)) == kla.ERR_INVALID_ARG
+    assert conv_call(win=ctypes.c_void_p(0x400000), wout=ctypes.c_void_p(0x400000 + 64)) == kla.ERR_INVALID_ARG
+    assert conv_call(wout=ctypes.c_void_p(0x300000)) == kla.ERR_INVALID_ARG
+    # empty batch: nothing to do, no CUDA call
+    assert conv_call(B=0, x=ctypes.c_void_p(0), y=ctypes.c_void_p(0), weight=ctypes.c_void_p(0)) == kla.OK
+
+
+def test_conv_with_one_tap_ignores_the_window_pointers():
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    # misaligned / overlapping window pointers are ignored for W = 1, so validation passes and the
+    # missing device is reported
+    assert conv_call(W=1, win=MIS, wout=ctypes.c_void_p(0x100000)) == kla.ERR_CUDA
+    assert conv_call(W=4, win=MIS) == kla.ERR_MISALIGNED
+
+
+def test_conv_backward_validates_before_any_cuda_call():
+    b = L.kla_conv_backward
+    x, wt, gy, gx = (ctypes.c_void_p(a) for a in (0x100000, 0x200000, 0x300000, 0x400000))
+    gw, gb, gwin = (ctypes.c_void_p(a) for a in (0x500000, 0x600000, 0x700000))
+
+    def call(**kw):
+        args = dict(x=x, weight=wt, bias=None, win=None, gy=gy, gwo=None, gx=gx, gw=gw, gb=gb, gwin=gwin,
+                    B=1, H=1, T=8, D=16, W=4, io=kla.F32, act=kla.ACT_SILU, ws=ctypes.c_void_p(0x800000),
+                    ws_bytes=1 << 20)
+        args.update(kw)
+        a = args
+        return b(a["x"], a["weight"], a["bias"], a["win"], a["gy"], a["gwo"], a["gx"], a["gw"], a["gb"],
+                 a["gwin"], a["B"], a["H"], a["T"], a["D"], a["W"], a["io"], a["act"], a["ws"], a["ws_bytes"],
+                 None)
+
+    assert call(D=12 + 2) == kla.ERR_UNSUPPORTED_SHAPE
+    assert call(W=10) == kla.ERR_UNSUPPORTED_SHAPE
+    assert call(act=-1) == kla.ERR_INVALID_ARG
+    assert call(gx=None) == kla.ERR_INVALID_ARG
+    assert call(weight=None) == kla.ERR_INVALID_ARG
+    assert call(gw=MIS) == kla.ERR_MISALIGNED
+    assert call(ws=MIS) == kla.ERR_MISALIGNED
+    assert call(gx=ctypes.c_void_p(0x100000 + 64)) == kla.ERR_INVALID_ARG       # gx over x
+    assert call(gwin=ctypes.c_void_p(0x400000 + 128)) == kla.ERR_INVALID_ARG    # gwindow over gx
+    assert call(gb=ctypes.c_void_p(0x200000)) == kla.ERR_INVALID_ARG            # gbias over the taps
+    # no batch, no weight gradient wanted: nothing to do
+    assert call(B=0, x=None, gx=None, gy=None, gw=None, gb=None, ws=None, ws_bytes=0) == kla.OK
+    if not torch.cuda.is_available():
+        assert L.kla_conv_backward_workspace_size(1, 1, 8, 16, 4) == ctypes.c_size_t(-1).value
+        assert call() == kla.ERR_CUDA
+    assert L.kla_conv_backward_workspace_size(1, 1, 8, 18, 4) == ctypes.c_size_t(-1).value
+    assert L.kla_conv_backward_workspace_size(0, 3, 8, 16, 4) == 0
