@@ -5,8 +5,9 @@ element, on seeded inputs from ``inputs.make_conv_inputs``.
 Error measure: |gpu − oracle| / (|oracle| + s), with s the same quantity
 computed on absolute values (for y: |bias| + Σ_k |w_k x_k|; for gx and the
 window gradient: Σ_k |w_k| |gu| + |gwindow_out|; for the tap and bias
-gradients: Σ |gu| |x| and Σ |gu|), so that cancellation in a sum is not
-counted against the kernel. Tolerances: outputs in the I/O dtype 2e-5 (fp32:
+gradients: Σ |gu| |x| and Σ |gu|; with |gu| read as |gy|·σ(u)(1 + |u|(1 −
+σ(u))), the terms of gy·SiLU'(u) in absolute value), so that cancellation in
+a sum is not counted against the kernel. Tolerances: outputs in the I/O dtype 2e-5 (fp32:
 a W-term fp32 sum and the hardware exponential and reciprocal in SiLU) or
 4e-3 (bf16: round-to-nearest-even of the output, 2^-9 relative); the fp32 tap
 and bias gradients 1e-4 (fp32 sums over up to a thousand tokens per thread
@@ -63,9 +64,12 @@ def oracle_backward(p, act, use_bias, use_window, use_gwo=True):
     gy = f64(p["gy"])
     gwo = f64(p["gwindow_out"]) if use_gwo else None
     g = C.conv_backward(x, w, b, win, gy, gwo, act)
-    # scales: the same sums over absolute values of gu, the taps and the inputs
+    # scales: the same sums over absolute values. SiLU'(u) = σ(1 + u(1 − σ))
+    # cancels to zero near u ≈ −1.28, so its scale is σ(1 + |u|(1 − σ)), the
+    # sum of its terms in absolute value, not |SiLU'(u)|
     u = C.preactivation(x, w, b, win)
-    gu_abs = np.abs(gy * C.dsilu(u)) if act else np.abs(gy)
+    sg = C.sigmoid(u)
+    gu_abs = np.abs(gy) * sg * (1.0 + np.abs(u) * (1.0 - sg)) if act else np.abs(gy)
     s = C.conv_backward(np.abs(x), np.abs(w), None, None if win is None else np.abs(win), gu_abs,
                         None if gwo is None else np.abs(gwo), activation=False)
     return g, s
