@@ -587,12 +587,10 @@ kla_status kla_conv(const void* x, const float* weight, const float* bias, const
   if (bh == 0) return KLA_OK;
   int sms = 0;
   if ((st = device_sms(&sms)) != KLA_OK) return st;
-  const kla::ConvPlan p = kla::conv_plan(bh, T, D, W, sms);
   kla::ConvArgs a{};
   a.x = x; a.weight = weight; a.bias = bias; a.win = window_in; a.y = y; a.wout = window_out;
   a.B = B; a.H = H; a.T = T; a.D = D; a.W = W; a.io = (int)io; a.act = activation;
-  a.L = p.L; a.chunks_per_block = p.chunks_per_block;
-  return kla::launch_conv(a, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
+  return kla::launch_conv(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KLA_OK : KLA_ERR_CUDA;
 }
 
 size_t kla_conv_backward_workspace_size(int B, int H, int T, int D, int W) {

@@ -41,6 +41,11 @@ namespace kla {
 namespace {
 
 constexpr int kConvThreads = 256;
+// forward: consecutive tokens per thread and stage; eight for W > 5 so that a
+// stage (at least one thread's rows) always holds the W−1 rows before the next
+template <int W>
+__host__ __device__ constexpr int conv_rows() { return W > 5 ? 8 : 4; }
+constexpr int kConvStages = 4;  // forward: shared-memory stages (three in flight)
 
 __device__ __forceinline__ float4 load4ch(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ float4 load4ch(const __nv_bfloat16* p) {
@@ -56,6 +61,15 @@ __device__ __forceinline__ void store4ch(__nv_bfloat16* p, float4 v) {
   r.x = *reinterpret_cast<const uint32_t*>(&lo);
   r.y = *reinterpret_cast<const uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(p) = r;
+}
+
+// Four channels of one row from shared memory.
+__device__ __forceinline__ float4 lds4ch(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 lds4ch(const __nv_bfloat16* p) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ float f4get(const float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
@@ -120,56 +134,142 @@ __device__ __forceinline__ float4 preact(const float4 (&w)[W], const float4& bia
   return u;
 }
 
+// 8-byte asynchronous copy (rows of bf16 streams whose width is not a
+// multiple of eight channels are only 8-byte aligned).
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+// Forward: a block owns the token range [T0, T1) of one stream (b, h) and
+// streams it through kConvStages shared-memory stages of TT tokens (all D
+// channels; a stage is one contiguous span of x) with cp.async, kConvStages−1
+// stages in flight. Thread (g, c) computes tokens c·R … c·R+R−1 of a stage for
+// channels 4g … 4g+3, reading its R+W−1 input rows from shared memory (rows
+// before the stage from the previous stage's buffer, which is refilled only
+// after the stage is done). The W−1 rows before T0 — x, the carried window,
+// or zeros — are placed at the end of the last buffer before the first stage.
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a) {
-  const ConvLane l = conv_lane(a);
-  if (!l.active) return;
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int R = conv_rows<W>(), S = kConvStages;
+  const int D = a.D, G = D >> 2, T = a.T;
+  const int cpb = a.chunks_per_block, TT = cpb * R;
+  const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g;
   const long long bh = blockIdx.x;
   const int h = (int)(bh % a.H);
-  const int T = a.T, D = a.D;
-  float4 w[W], bias;
-  load_taps<W>(a, h, l.d0, w, bias);
-  const IO* __restrict__ x = reinterpret_cast<const IO*>(a.x) + bh * (long long)T * D + l.d0;
-  IO* __restrict__ y = reinterpret_cast<IO*>(a.y) + bh * (long long)T * D + l.d0;
-  const IO* win = a.win ? reinterpret_cast<const IO*>(a.win) + bh * (long long)(W - 1) * D + l.d0 : nullptr;
+  const long long T0 = (long long)blockIdx.y * a.range, T1 = min(T0 + (long long)a.range, (long long)T);
+  const size_t row = (size_t)D * sizeof(IO);
+  const size_t stage_bytes = (size_t)TT * row;
+  const IO* __restrict__ xg = reinterpret_cast<const IO*>(a.x) + bh * (long long)T * D;
+  IO* __restrict__ yg = reinterpret_cast<IO*>(a.y) + bh * (long long)T * D;
+  const IO* win = a.win ? reinterpret_cast<const IO*>(a.win) + bh * (long long)(W - 1) * D : nullptr;
+  auto buf = [&](long long n) { return reinterpret_cast<IO*>(smem + (size_t)(n % S) * stage_bytes); };
+  const bool wide = row % 16 == 0;  // 16-byte copies; else 8-byte ones
 
-  // Walk tokens tau = t0 − (W−1) + m, m ∈ [0, M): the first W−1 only fill the
-  // ring; token m sits in slot m mod W.
-  float4 xr[W];
-  const long long base = l.t0 - (W - 1);
-  const int M = (int)(l.t1 - l.t0) + W - 1;
-#pragma unroll 2
-  for (int mb = 0; mb < M; mb += W) {
+  // Queue the copy of `bytes` contiguous bytes (a multiple of 8) into shared memory.
+  auto copy_span = [&](void* dst, const void* src, size_t bytes) {
+    char* d = reinterpret_cast<char*>(dst);
+    const char* s0 = reinterpret_cast<const char*>(src);
+    if (wide) {
+      for (size_t o = (size_t)tid * 16; o < bytes; o += kConvThreads * 16) cp_async16(d + o, s0 + o);
+    } else {
+      for (size_t o = (size_t)tid * 8; o < bytes; o += kConvThreads * 8) cp_async8(d + o, s0 + o);
+    }
+  };
+  auto stage_copy = [&](long long n) {
+    const long long ts = T0 + n * TT, te = min(ts + TT, T1);
+    if (ts < te) copy_span(buf(n), xg + ts * D, (size_t)(te - ts) * row);
+  };
+
+  // rows before T0, at the end of buffer S−1 (= the buffer before stage 0)
+  if (W > 1) {
+    IO* halo = reinterpret_cast<IO*>(smem + (size_t)(S - 1) * stage_bytes) + (size_t)(TT - (W - 1)) * D;
+    if (T0 > 0) {
+      copy_span(halo, xg + (T0 - (W - 1)) * D, (size_t)(W - 1) * row);
+    } else if (win) {
+      copy_span(halo, win, (size_t)(W - 1) * row);
+    } else {
+      for (int i = tid; i < (W - 1) * D; i += kConvThreads) halo[i] = from_f32<IO>(0.0f);
+    }
+  }
 #pragma unroll
-    for (int s = 0; s < W; ++s) {
-      const int m = mb + s;
-      if (m < M) {
-        const long long tau = base + m;
-        xr[s] = input_at<IO, W>(x, win, tau, T, D);
-        if (m >= W - 1) {
-          float4 u = preact<W>(w, bias, xr, s);
+  for (int n = 0; n < S - 1; ++n) {
+    stage_copy(n);
+    cp_async_commit();
+  }
+
+  float4 w[W], bias;
+  load_taps<W>(a, h, d0, w, bias);
+  const long long nst = (T1 - T0 + TT - 1) / TT;
+  for (long long n = 0; n < nst; ++n) {
+    cp_async_wait<S - 2>();
+    __syncthreads();  // stage n (and the halo) landed for every thread
+    if (c < cpb) {
+      const IO* cur = buf(n);
+      const IO* prev = buf(n + S - 1);
+      const long long ts = T0 + n * TT + (long long)c * R;  // first token of this thread
+      float4 xr[R + W - 1];
+#pragma unroll
+      for (int i = 0; i < R + W - 1; ++i) {
+        const int r = c * R - (W - 1) + i;  // row within the stage (negative: previous stage)
+        if (ts - (W - 1) + i < T1)
+          xr[i] = r >= 0 ? lds4ch(cur + (size_t)r * D + d0) : lds4ch(prev + (size_t)(TT + r) * D + d0);
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        if (ts + j < T1) {
+          float4 u = bias;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            const float4 xv = xr[j + k];
+            u.x = fmaf(w[k].x, xv.x, u.x);
+            u.y = fmaf(w[k].y, xv.y, u.y);
+            u.z = fmaf(w[k].z, xv.z, u.z);
+            u.w = fmaf(w[k].w, xv.w, u.w);
+          }
           if (ACT) {
             u.x *= sigmoid_fast(u.x);
             u.y *= sigmoid_fast(u.y);
             u.z *= sigmoid_fast(u.z);
             u.w *= sigmoid_fast(u.w);
           }
-          store4ch(y + tau * D, u);
+          store4ch(yg + (ts + j) * D + d0, u);
         }
       }
     }
+    __syncthreads();  // nobody reads buffer (n − 1) any more
+    stage_copy(n + S - 1);
+    cp_async_commit();
   }
+  cp_async_wait<0>();
 
-  // The window after the last token, written by chunk 0's thread: the last
-  // W−1 inputs of (window, x). All are read before any is written, so the
-  // window out may be the window in.
-  if (W > 1 && l.chunk == 0 && a.wout) {
-    IO* wout = reinterpret_cast<IO*>(a.wout) + bh * (long long)(W - 1) * D + l.d0;
-    float4 keep[W > 1 ? W - 1 : 1];
+  // The window after the last token, written by the first block of the
+  // stream: the last W−1 inputs of (window, x). Every value is read before
+  // any is written, so the window out may be the window in.
+  if (W > 1 && blockIdx.y == 0 && a.wout) {
+    IO* wout = reinterpret_cast<IO*>(a.wout) + bh * (long long)(W - 1) * D;
+    // item i = tid + q·256 < G·(W−1): window row i / G, channel group i % G (G ≤ 256)
+    float4 v[W > 1 ? W - 1 : 1];
 #pragma unroll
-    for (int j = 0; j < W - 1; ++j) keep[j] = input_at<IO, W>(x, win, (long long)T - (W - 1) + j, T, D);
+    for (int q = 0; q < W - 1; ++q) {
+      const int i = tid + q * kConvThreads;
+      v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < G * (W - 1)) {
+        const int j = i / G, gg = i - j * G;
+        const long long tau = (long long)T - (W - 1) + j;
+        if (tau >= 0) v[q] = load4ch(xg + tau * D + 4 * gg);
+        else if (win) v[q] = load4ch(win + (tau + W - 1) * D + 4 * gg);
+      }
+    }
+    __syncthreads();
 #pragma unroll
-    for (int j = 0; j < W - 1; ++j) store4ch(wout + (long long)j * D, keep[j]);
+    for (int q = 0; q < W - 1; ++q) {
+      const int i = tid + q * kConvThreads;
+      if (i < G * (W - 1)) {
+        const int j = i / G, gg = i - j * G;
+        store4ch(wout + (long long)j * D + 4 * gg, v[q]);
+      }
+    }
   }
 }
 
@@ -303,29 +403,50 @@ __global__ void __launch_bounds__(256) kla_conv_bwd_finish_kernel(const ConvArgs
   }
 }
 
-template <typename IO, int W>
-cudaError_t launch_w(const ConvArgs& a, bool backward, dim3 grid, size_t smem, cudaStream_t s) {
-  if (backward) {
-    if (a.act) kla_conv_bwd_kernel<IO, W, true><<<grid, kConvThreads, smem, s>>>(a);
-    else kla_conv_bwd_kernel<IO, W, false><<<grid, kConvThreads, smem, s>>>(a);
-  } else {
-    if (a.act) kla_conv_kernel<IO, W, true><<<grid, kConvThreads, 0, s>>>(a);
-    else kla_conv_kernel<IO, W, false><<<grid, kConvThreads, 0, s>>>(a);
-  }
+// Forward launch: blocks of one stream split its tokens into ranges of whole
+// stages, as many ranges as keep every block of the grid resident at once
+// (one wave; streams beyond that are whole-sequence blocks in later waves).
+template <typename IO, int W, bool ACT>
+cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
+  const long long bh = (long long)a.B * a.H;
+  a.chunks_per_block = kConvThreads / (a.D / 4);
+  const long long TT = (long long)a.chunks_per_block * conv_rows<W>();
+  const size_t smem = (size_t)kConvStages * TT * a.D * sizeof(IO);
+  auto fn = kla_conv_kernel<IO, W, ACT>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kConvThreads, smem)) != cudaSuccess) return e;
+  const long long slots = (long long)std::max(occ, 1) * num_sms;
+  const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
+  const long long nsplit = std::max(1LL, std::min(nst, slots / bh));
+  a.range = (int)(TT * ((nst + nsplit - 1) / nsplit));
+  const long long blocks_y = a.T > 0 ? ((long long)a.T + a.range - 1) / a.range : 1;
+  fn<<<dim3((unsigned)bh, (unsigned)blocks_y), kConvThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
+template <typename IO, int W>
+cudaError_t launch_w(const ConvArgs& a, bool backward, dim3 grid, size_t smem, int num_sms, cudaStream_t s) {
+  if (backward) {
+    if (a.act) kla_conv_bwd_kernel<IO, W, true><<<grid, kConvThreads, smem, s>>>(a);
+    else kla_conv_bwd_kernel<IO, W, false><<<grid, kConvThreads, smem, s>>>(a);
+    return cudaGetLastError();
+  }
+  return a.act ? launch_fwd<IO, W, true>(a, num_sms, s) : launch_fwd<IO, W, false>(a, num_sms, s);
+}
+
 template <typename IO>
-cudaError_t launch_io(const ConvArgs& a, bool backward, dim3 grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_io(const ConvArgs& a, bool backward, dim3 grid, size_t smem, int num_sms, cudaStream_t s) {
   switch (a.W) {
-    case 1: return launch_w<IO, 1>(a, backward, grid, smem, s);
-    case 2: return launch_w<IO, 2>(a, backward, grid, smem, s);
-    case 3: return launch_w<IO, 3>(a, backward, grid, smem, s);
-    case 4: return launch_w<IO, 4>(a, backward, grid, smem, s);
-    case 5: return launch_w<IO, 5>(a, backward, grid, smem, s);
-    case 6: return launch_w<IO, 6>(a, backward, grid, smem, s);
-    case 7: return launch_w<IO, 7>(a, backward, grid, smem, s);
-    case 8: return launch_w<IO, 8>(a, backward, grid, smem, s);
+    case 1: return launch_w<IO, 1>(a, backward, grid, smem, num_sms, s);
+    case 2: return launch_w<IO, 2>(a, backward, grid, smem, num_sms, s);
+    case 3: return launch_w<IO, 3>(a, backward, grid, smem, num_sms, s);
+    case 4: return launch_w<IO, 4>(a, backward, grid, smem, num_sms, s);
+    case 5: return launch_w<IO, 5>(a, backward, grid, smem, num_sms, s);
+    case 6: return launch_w<IO, 6>(a, backward, grid, smem, num_sms, s);
+    case 7: return launch_w<IO, 7>(a, backward, grid, smem, num_sms, s);
+    case 8: return launch_w<IO, 8>(a, backward, grid, smem, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -337,9 +458,9 @@ ConvPlan conv_plan(long long bh, int T, int D, int W, int num_sms) {
   const int G = D / 4;
   p.chunks_per_block = kConvThreads / G;
   p.threads = kConvThreads;
-  // Shortest chunk (≥ 16 tokens, a power of two) that keeps the grid within
-  // about four blocks per SM — one wave at the kernels' occupancy — so the
-  // recomputed W−1 inputs at each chunk start stay a small share.
+  // Backward: shortest per-thread chunk (≥ 16 tokens, a power of two) that
+  // keeps the grid within about four blocks per SM, so the recomputed W−1
+  // inputs at each chunk's ends stay a small share.
   auto blocks_y = [&](long long L) {
     const long long chunks = T > 0 ? (T + L - 1) / L : 1;
     return (chunks + p.chunks_per_block - 1) / p.chunks_per_block;
@@ -357,19 +478,19 @@ size_t conv_partial_bytes(int B, int H, int D, int W, const ConvPlan& p) {
   return (size_t)H * B * p.blocks_y * D * (W + 1) * sizeof(float);
 }
 
-cudaError_t launch_conv(const ConvArgs& a, const ConvPlan& p, cudaStream_t s) {
+cudaError_t launch_conv(const ConvArgs& a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
   if (bh == 0) return cudaSuccess;
-  const dim3 grid((unsigned)bh, (unsigned)p.blocks_y);
-  return a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, false, grid, 0, s) : launch_io<float>(a, false, grid, 0, s);
+  return a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, false, dim3(), 0, num_sms, s)
+                         : launch_io<float>(a, false, dim3(), 0, num_sms, s);
 }
 
 cudaError_t launch_conv_backward(const ConvArgs& a, const ConvPlan& p, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
   if (bh > 0) {
     const dim3 grid((unsigned)bh, (unsigned)p.blocks_y);
-    const cudaError_t e = a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, true, grid, p.smem_bwd, s)
-                                          : launch_io<float>(a, true, grid, p.smem_bwd, s);
+    const cudaError_t e = a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, true, grid, p.smem_bwd, 0, s)
+                                          : launch_io<float>(a, true, grid, p.smem_bwd, 0, s);
     if (e != cudaSuccess) return e;
   }
   if (a.H > 0 && (a.gweight || a.gbias)) {

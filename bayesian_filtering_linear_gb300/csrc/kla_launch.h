@@ -113,16 +113,19 @@ struct ConvArgs {
   long long nparts;   // B · blocks along T
   int B, H, T, D, W;
   int io, act;
-  int L, chunks_per_block;  // tokens per thread chunk; chunks per block
+  int L, chunks_per_block;  // backward: tokens per thread chunk; chunks per block
+  int range;                // forward: tokens per block (set by launch_conv)
 };
 struct ConvPlan {
   int L, chunks_per_block, threads, blocks_y;
   long long nparts;
   size_t smem_bwd;
 };
+// The backward's geometry and its partial-sum workspace.
 ConvPlan conv_plan(long long bh, int T, int D, int W, int num_sms);
 size_t conv_partial_bytes(int B, int H, int D, int W, const ConvPlan& p);
-cudaError_t launch_conv(const ConvArgs& a, const ConvPlan& p, cudaStream_t s);
+// The forward chooses its own geometry (shared-memory stages, tokens per block).
+cudaError_t launch_conv(const ConvArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_conv_backward(const ConvArgs& a, const ConvPlan& p, cudaStream_t s);
 
 }  // namespace kla
