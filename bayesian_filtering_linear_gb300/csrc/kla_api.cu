@@ -599,7 +599,7 @@ size_t kla_conv_backward_workspace_size(int B, int H, int T, int D, int W) {
   if (bh == 0) return 0;
   int sms = 0;
   if (device_sms(&sms) != KLA_OK) return (size_t)-1;
-  return kla::conv_partial_bytes(B, H, D, W, kla::conv_plan(bh, T, D, W, sms));
+  return kla::conv_partial_bytes(B, H, T, D, W, sms);
 }
 
 kla_status kla_conv_backward(const void* x, const float* weight, const float* bias, const void* window_in,
@@ -634,8 +634,7 @@ kla_status kla_conv_backward(const void* x, const float* weight, const float* bi
   if (bh == 0 && !(want_sums && H > 0)) return KLA_OK;
   int sms = 0;
   if ((st = device_sms(&sms)) != KLA_OK) return st;
-  const kla::ConvPlan p = kla::conv_plan(bh, T, D, W, sms);
-  const size_t part_bytes = bh > 0 ? kla::conv_partial_bytes(B, H, D, W, p) : 0;
+  const size_t part_bytes = kla::conv_partial_bytes(B, H, T, D, W, sms);
   if (want_sums && part_bytes > 0 && (!workspace || ws_bytes < part_bytes)) return KLA_ERR_WORKSPACE;
   if (want_sums && part_bytes > 0)
     for (int o = 0; o < 4; ++o)
@@ -644,11 +643,9 @@ kla_status kla_conv_backward(const void* x, const float* weight, const float* bi
   a.x = x; a.weight = weight; a.bias = bias; a.win = window_in;
   a.gy = gy; a.gwout = gwindow_out; a.gx = gx; a.gwin = gwindow; a.gweight = gweight; a.gbias = gbias;
   a.part = want_sums && part_bytes > 0 ? reinterpret_cast<float*>(workspace) : nullptr;
-  a.nparts = bh > 0 ? (long long)B * p.blocks_y : 0;
   a.B = B; a.H = H; a.T = T; a.D = D; a.W = W; a.io = (int)io; a.act = activation;
-  a.L = p.L; a.chunks_per_block = p.chunks_per_block;
-  return kla::launch_conv_backward(a, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KLA_OK
-                                                                                                : KLA_ERR_CUDA;
+  return kla::launch_conv_backward(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KLA_OK
+                                                                                                  : KLA_ERR_CUDA;
 }
 
 }  // extern "C"

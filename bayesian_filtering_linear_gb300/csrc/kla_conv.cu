@@ -45,7 +45,8 @@ constexpr int kConvThreads = 256;
 // stage (at least one thread's rows) always holds the W−1 rows before the next
 template <int W>
 __host__ __device__ constexpr int conv_rows() { return W > 5 ? 8 : 4; }
-constexpr int kConvStages = 4;  // forward: shared-memory stages (three in flight)
+constexpr int kConvStages = 4;     // forward: shared-memory stages (three in flight)
+constexpr int kConvBwdStages = 3;  // backward: stages of x and gy (two in flight)
 
 __device__ __forceinline__ float4 load4ch(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ float4 load4ch(const __nv_bfloat16* p) {
@@ -80,27 +81,6 @@ __device__ __forceinline__ void f4set(float4& v, int e, float s) {
 // σ(u) with the hardware reciprocal; 0 for u below about −88 (e^−u overflows).
 __device__ __forceinline__ float sigmoid_fast(float u) { return rcp_approx(1.0f + __expf(-u)); }
 
-// Thread → (channel group, chunk) of the block's (b, h).
-struct ConvLane {
-  int g, d0;         // channel group and its first channel
-  long long chunk;   // token chunk index
-  long long t0, t1;  // tokens [t0, t1) of the chunk
-  bool active;
-};
-__device__ __forceinline__ ConvLane conv_lane(const ConvArgs& a) {
-  ConvLane l;
-  const int G = a.D >> 2;
-  const int c = (int)threadIdx.x / G;
-  l.g = (int)threadIdx.x - c * G;
-  l.d0 = 4 * l.g;
-  l.chunk = (long long)blockIdx.y * a.chunks_per_block + c;
-  l.t0 = l.chunk * a.L;
-  l.t1 = min(l.t0 + a.L, (long long)a.T);
-  // chunk 0 always runs: it owns the windows, also when T = 0
-  l.active = c < a.chunks_per_block && (l.chunk == 0 || l.t0 < a.T);
-  return l;
-}
-
 template <int W>
 __device__ __forceinline__ void load_taps(const ConvArgs& a, int h, int d0, float4 (&w)[W], float4& bias) {
   const float* wp = a.weight + ((size_t)h * a.D + d0) * W;  // [H][D][W]: four channels' taps are contiguous
@@ -109,29 +89,6 @@ __device__ __forceinline__ void load_taps(const ConvArgs& a, int h, int d0, floa
 #pragma unroll
     for (int e = 0; e < 4; ++e) f4set(w[k], e, __ldg(wp + e * W + k));
   bias = a.bias ? __ldg(reinterpret_cast<const float4*>(a.bias + (size_t)h * a.D + d0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// Input of token tau of this thread's stream: x for 0 ≤ tau < T, the carried
-// window for tau < 0 (zeros without one), zeros past the end.
-template <typename IO, int W>
-__device__ __forceinline__ float4 input_at(const IO* x, const IO* win, long long tau, int T, int D) {
-  if (tau >= 0) return tau < T ? load4ch(x + tau * D) : make_float4(0.f, 0.f, 0.f, 0.f);
-  return win ? load4ch(win + (tau + W - 1) * D) : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// u of the token in ring slot s (its window is slots s+1 … s+W, mod W).
-template <int W>
-__device__ __forceinline__ float4 preact(const float4 (&w)[W], const float4& bias, const float4 (&xr)[W], int s) {
-  float4 u = bias;
-#pragma unroll
-  for (int k = 0; k < W; ++k) {
-    const float4 xv = xr[(s + 1 + k) % W];
-    u.x = fmaf(w[k].x, xv.x, u.x);
-    u.y = fmaf(w[k].y, xv.y, u.y);
-    u.z = fmaf(w[k].z, xv.z, u.z);
-    u.w = fmaf(w[k].w, xv.w, u.w);
-  }
-  return u;
 }
 
 // 8-byte asynchronous copy (rows of bf16 streams whose width is not a
@@ -273,116 +230,222 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
   }
 }
 
+// Backward: a block owns the token range [T0, T1) of one stream. gu is
+// needed on [T0, T1e), T1e = min(T1 + W − 1, T) (gx of the range's last
+// tokens reaches W − 1 tokens further), so x and gy stream through
+// kConvBwdStages shared-memory stages over [T0, T1e) (x with the W − 1 rows
+// before T0 at the end of the last buffer, as in the forward). Stage n: each
+// thread forms gu of its R tokens × 4 channels into a two-stage fp32 ring in
+// shared memory and adds its tokens below T1 to its tap and bias partial
+// sums; then gx of stage n − 1 is complete and is written (gu rows past the
+// stage come from stage n; tokens at or past T1e have gu = 0). The first
+// block of a stream also writes the gradient of the window in (tokens −(W−1)
+// … −1) once stage 0's gu exists.
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvArgs a) {
-  extern __shared__ float4 red[];  // [chunks_per_block][G][W + 1] per-thread partial sums
-  const ConvLane l = conv_lane(a);
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int R = conv_rows<W>(), S = kConvBwdStages;
+  const int D = a.D, G = D >> 2, T = a.T;
+  const int cpb = a.chunks_per_block, TT = cpb * R;
+  const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g;
   const long long bh = blockIdx.x;
   const int h = (int)(bh % a.H);
-  const int T = a.T, D = a.D, G = D >> 2;
-  const int c = (int)threadIdx.x / G;
-  float4 gw[W], gb = make_float4(0.f, 0.f, 0.f, 0.f);
+  const long long T0 = (long long)blockIdx.y * a.range, T1 = min(T0 + (long long)a.range, (long long)T);
+  const long long T1e = min(T1 + (W - 1), (long long)T);
+  const size_t row = (size_t)D * sizeof(IO);
+  const size_t stage_bytes = (size_t)TT * row;
+  const size_t gu_stage = (size_t)TT * D;  // floats
+  IO* xs = reinterpret_cast<IO*>(smem);
+  IO* gys = reinterpret_cast<IO*>(smem + (size_t)S * stage_bytes);
+  float* gus = reinterpret_cast<float*>(smem + 2 * (size_t)S * stage_bytes);
+  const long long off = bh * (long long)T * D;
+  const IO* __restrict__ xg = reinterpret_cast<const IO*>(a.x) + off;
+  const IO* __restrict__ gyg = a.gy ? reinterpret_cast<const IO*>(a.gy) + off : nullptr;  // null: zero
+  IO* __restrict__ gxg = reinterpret_cast<IO*>(a.gx) + off;
+  const long long woff = bh * (long long)(W - 1) * D;
+  const IO* win = a.win ? reinterpret_cast<const IO*>(a.win) + woff : nullptr;
+  const IO* gwo = a.gwout ? reinterpret_cast<const IO*>(a.gwout) + woff : nullptr;
+  IO* gwin = a.gwin ? reinterpret_cast<IO*>(a.gwin) + woff : nullptr;
+  const long long tail = (long long)T - (W - 1);  // first input copied into the window out
+  const bool wide = row % 16 == 0;
+
+  auto copy_span = [&](void* dst, const void* src, size_t bytes) {
+    char* d = reinterpret_cast<char*>(dst);
+    const char* s0 = reinterpret_cast<const char*>(src);
+    if (wide) {
+      for (size_t o = (size_t)tid * 16; o < bytes; o += kConvThreads * 16) cp_async16(d + o, s0 + o);
+    } else {
+      for (size_t o = (size_t)tid * 8; o < bytes; o += kConvThreads * 8) cp_async8(d + o, s0 + o);
+    }
+  };
+  auto stage_copy = [&](long long n) {
+    const long long ts = T0 + n * TT, te = min(ts + TT, T1e);
+    if (ts >= te) return;
+    const size_t b = (size_t)(n % S) * stage_bytes;
+    copy_span(reinterpret_cast<char*>(xs) + b, xg + ts * D, (size_t)(te - ts) * row);
+    if (gyg) copy_span(reinterpret_cast<char*>(gys) + b, gyg + ts * D, (size_t)(te - ts) * row);
+  };
+  if (W > 1) {
+    IO* halo = xs + (size_t)(S - 1) * TT * D + (size_t)(TT - (W - 1)) * D;
+    if (T0 > 0) {
+      copy_span(halo, xg + (T0 - (W - 1)) * D, (size_t)(W - 1) * row);
+    } else if (win) {
+      copy_span(halo, win, (size_t)(W - 1) * row);
+    } else {
+      for (int i = tid; i < (W - 1) * D; i += kConvThreads) halo[i] = from_f32<IO>(0.0f);
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < S - 1; ++n) {
+    stage_copy(n);
+    cp_async_commit();
+  }
+
+  float4 w[W], bias, gw[W], gb = make_float4(0.f, 0.f, 0.f, 0.f);
+  load_taps<W>(a, h, d0, w, bias);
 #pragma unroll
   for (int k = 0; k < W; ++k) gw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  if (l.active) {
-    float4 w[W], bias;
-    load_taps<W>(a, h, l.d0, w, bias);
-    const long long off = bh * (long long)T * D + l.d0;
-    const IO* __restrict__ x = reinterpret_cast<const IO*>(a.x) + off;
-    const IO* __restrict__ gy = a.gy ? reinterpret_cast<const IO*>(a.gy) + off : nullptr;  // null: zero
-    IO* __restrict__ gx = reinterpret_cast<IO*>(a.gx) + off;
-    const long long woff = bh * (long long)(W - 1) * D + l.d0;
-    const IO* win = a.win ? reinterpret_cast<const IO*>(a.win) + woff : nullptr;
-    const IO* gwo = a.gwout ? reinterpret_cast<const IO*>(a.gwout) + woff : nullptr;
-    IO* gwin = a.gwin ? reinterpret_cast<IO*>(a.gwin) + woff : nullptr;
-
-    // Walk tau = t0 − (W−1) + m, m ∈ [0, M), M = L + 2(W−1): gu is formed for
-    // tokens in [t0, min(t1 + W − 1, T)), and gx of token tau − (W−1) is
-    // complete once gu of tau is. Chunk 0 also emits tokens −(W−1)…−1 (the
-    // gradient of the window in).
-    float4 xr[W], gr[W];
-    const long long base = l.t0 - (W - 1);
-    const long long emit_lo = l.chunk == 0 ? -(long long)(W - 1) : l.t0;
-    const long long tail = (long long)T - (W - 1);  // first input copied into the window out
-    const int M = (int)(l.t1 - l.t0) + 2 * (W - 1);
-#pragma unroll 2
-    for (int mb = 0; mb < M; mb += W) {
+  // gx of this thread's tokens in stage m (gu of stage m, and of m + 1 past its end)
+  auto emit = [&](long long m) {
+    if (c >= cpb) return;
+    const long long sm0 = T0 + m * TT;
+    const float* gu_m = gus + (size_t)(m & 1) * gu_stage;
+    const float* gu_n = gus + (size_t)((m + 1) & 1) * gu_stage;
 #pragma unroll
-      for (int s = 0; s < W; ++s) {
-        const int m = mb + s;
-        if (m < M) {
-          const long long tau = base + m;
-          xr[s] = input_at<IO, W>(x, win, tau, T, D);
-          float4 gu = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (tau >= l.t0 && tau < T) {
-            const float4 u = preact<W>(w, bias, xr, s);
-            if (gy) gu = load4ch(gy + tau * D);
-            if (ACT) {
+    for (int j = 0; j < R; ++j) {
+      const long long te = sm0 + c * R + j;
+      if (te < T1) {
+        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (gwo && te >= tail) gv = load4ch(gwo + (te - tail) * D + d0);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float ue = f4get(u, e), sg = sigmoid_fast(ue);
-                f4set(gu, e, f4get(gu, e) * (sg * fmaf(ue, 1.0f - sg, 1.0f)));
-              }
-            }
-            if (tau < l.t1) {
-              gb.x += gu.x; gb.y += gu.y; gb.z += gu.z; gb.w += gu.w;
-#pragma unroll
-              for (int k = 0; k < W; ++k) {
-                const float4 xv = xr[(s + 1 + k) % W];
-                gw[k].x = fmaf(gu.x, xv.x, gw[k].x);
-                gw[k].y = fmaf(gu.y, xv.y, gw[k].y);
-                gw[k].z = fmaf(gu.z, xv.z, gw[k].z);
-                gw[k].w = fmaf(gu.w, xv.w, gw[k].w);
-              }
-            }
-          }
-          gr[s] = gu;
-          const long long te = tau - (W - 1);  // the token whose gx is now complete
-          if (te >= emit_lo && te < l.t1) {
-            float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (gwo && te >= tail) g = load4ch(gwo + (te - tail) * D);
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-              const float4 gv = gr[(s - k + W) % W];  // gu of token tau − k
-              g.x = fmaf(w[k].x, gv.x, g.x);
-              g.y = fmaf(w[k].y, gv.y, g.y);
-              g.z = fmaf(w[k].z, gv.z, g.z);
-              g.w = fmaf(w[k].w, gv.w, g.w);
-            }
-            if (te >= 0) store4ch(gx + te * D, g);
-            else if (gwin) store4ch(gwin + (te + W - 1) * D, g);
+        for (int k = 0; k < W; ++k) {
+          const long long tt = te + (W - 1) - k;  // gu of token tt meets tap k
+          if (tt < T1e) {
+            const int r = (int)(tt - sm0);
+            const float4 gu = lds4ch(r < TT ? gu_m + (size_t)r * D + d0 : gu_n + (size_t)(r - TT) * D + d0);
+            gv.x = fmaf(w[k].x, gu.x, gv.x);
+            gv.y = fmaf(w[k].y, gu.y, gv.y);
+            gv.z = fmaf(w[k].z, gu.z, gv.z);
+            gv.w = fmaf(w[k].w, gu.w, gv.w);
           }
         }
+        store4ch(gxg + te * D + d0, gv);
       }
     }
-  }
+  };
+  // gradient of the window in: tokens −(W−1) … −1, all reached by stage 0's gu
+  auto emit_window = [&]() {
+    if (W == 1 || blockIdx.y != 0 || !gwin) return;
+    for (int i = tid; i < G * (W - 1); i += kConvThreads) {
+      const int j = i / G, gg = i - j * G;
+      const long long te = (long long)j - (W - 1);
+      float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (gwo && te >= tail) gv = load4ch(gwo + (te - tail) * D + 4 * gg);
+      const float* wp = a.weight + ((size_t)h * D + 4 * gg) * W;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const long long tt = te + (W - 1) - k;
+        if (tt >= 0 && tt < T1e) {
+          const float4 gu = lds4ch(gus + (size_t)tt * D + 4 * gg);  // stage 0 (tt < W − 1 ≤ TT)
+          gv.x = fmaf(__ldg(wp + 0 * W + k), gu.x, gv.x);
+          gv.y = fmaf(__ldg(wp + 1 * W + k), gu.y, gv.y);
+          gv.z = fmaf(__ldg(wp + 2 * W + k), gu.z, gv.z);
+          gv.w = fmaf(__ldg(wp + 3 * W + k), gu.w, gv.w);
+        }
+      }
+      store4ch(gwin + (long long)j * D + 4 * gg, gv);
+    }
+  };
 
-  if (!a.part) return;  // no weight or bias gradient wanted
-  // Block partial: threads of the same channel group summed in chunk order.
-  const int cpb = a.chunks_per_block;
+  const long long nst = (T1e - T0 + TT - 1) / TT;
+  for (long long n = 0; n < nst; ++n) {
+    cp_async_wait<S - 2>();
+    __syncthreads();  // stage n landed; gx of stage n − 2 is done with its gu
+    if (c < cpb) {
+      const IO* xc = xs + (size_t)(n % S) * TT * D;
+      const IO* xp = xs + (size_t)((n + S - 1) % S) * TT * D;
+      const IO* gyc = gys + (size_t)(n % S) * TT * D;
+      float* gu_out = gus + (size_t)(n & 1) * gu_stage;
+      const long long ts = T0 + n * TT + (long long)c * R;
+      float4 xr[R + W - 1];
+#pragma unroll
+      for (int i = 0; i < R + W - 1; ++i) {
+        const int r = c * R - (W - 1) + i;
+        if (ts - (W - 1) + i < T1e)
+          xr[i] = r >= 0 ? lds4ch(xc + (size_t)r * D + d0) : lds4ch(xp + (size_t)(TT + r) * D + d0);
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        float4 gu = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ts + j < T1e) {
+          if (gyg) gu = lds4ch(gyc + (size_t)(c * R + j) * D + d0);
+          if (ACT) {
+            float4 u = bias;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              u.x = fmaf(w[k].x, xr[j + k].x, u.x);
+              u.y = fmaf(w[k].y, xr[j + k].y, u.y);
+              u.z = fmaf(w[k].z, xr[j + k].z, u.z);
+              u.w = fmaf(w[k].w, xr[j + k].w, u.w);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float ue = f4get(u, e), sg = sigmoid_fast(ue);
+              f4set(gu, e, f4get(gu, e) * (sg * fmaf(ue, 1.0f - sg, 1.0f)));
+            }
+          }
+          if (ts + j < T1) {
+            gb.x += gu.x; gb.y += gu.y; gb.z += gu.z; gb.w += gu.w;
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              gw[k].x = fmaf(gu.x, xr[j + k].x, gw[k].x);
+              gw[k].y = fmaf(gu.y, xr[j + k].y, gw[k].y);
+              gw[k].z = fmaf(gu.z, xr[j + k].z, gw[k].z);
+              gw[k].w = fmaf(gu.w, xr[j + k].w, gw[k].w);
+            }
+          }
+        }
+        *reinterpret_cast<float4*>(gu_out + (size_t)(c * R + j) * D + d0) = gu;
+      }
+    }
+    __syncthreads();  // gu of stage n visible; x and gy of stage n − 1 no longer read
+    stage_copy(n + S - 1);
+    cp_async_commit();
+    if (n >= 1) emit(n - 1);
+    else emit_window();
+  }
+  cp_async_wait<0>();
+  if (nst >= 1) emit(nst - 1);
+  else emit_window();  // T = 0: the window's gradient is the window out's
+
+  if (!a.part) return;  // no tap or bias gradient wanted
+  // Block partial: the threads of a channel group summed in chunk order,
+  // through shared memory (the gu ring is free now).
+  __syncthreads();
+  float4* red = reinterpret_cast<float4*>(gus);  // [cpb][G][W + 1]
   if (c < cpb) {
-    float4* r = red + ((size_t)c * G + l.g) * (W + 1);
+    float4* r = red + ((size_t)c * G + g) * (W + 1);
 #pragma unroll
     for (int k = 0; k < W; ++k) r[k] = gw[k];
     r[W] = gb;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G * (W + 1); i += blockDim.x) {
-    const int g = i / (W + 1), k = i - g * (W + 1);
-    float4 s = red[(size_t)g * (W + 1) + k];
+  for (int i = tid; i < G * (W + 1); i += kConvThreads) {
+    const int gg = i / (W + 1), k = i - gg * (W + 1);
+    float4 sum = red[(size_t)gg * (W + 1) + k];
     for (int cc = 1; cc < cpb; ++cc) {
-      const float4 v = red[((size_t)cc * G + g) * (W + 1) + k];
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      const float4 v = red[((size_t)cc * G + gg) * (W + 1) + k];
+      sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
     // partials [H][P][D][W + 1], P = B · gridDim.y, p = b · gridDim.y + blockIdx.y
     const long long b = bh / a.H;
     const long long p = b * gridDim.y + blockIdx.y;
-    float* dst = a.part + (((size_t)h * a.nparts + p) * D + 4 * g) * (W + 1) + k;
-    dst[0] = s.x;
-    dst[W + 1] = s.y;
-    dst[2 * (W + 1)] = s.z;
-    dst[3 * (W + 1)] = s.w;
+    float* dst = a.part + (((size_t)h * a.nparts + p) * D + 4 * gg) * (W + 1) + k;
+    dst[0] = sum.x;
+    dst[W + 1] = sum.y;
+    dst[2 * (W + 1)] = sum.z;
+    dst[3 * (W + 1)] = sum.w;
   }
 }
 
@@ -426,77 +489,93 @@ cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename IO, int W>
-cudaError_t launch_w(const ConvArgs& a, bool backward, dim3 grid, size_t smem, int num_sms, cudaStream_t s) {
-  if (backward) {
-    if (a.act) kla_conv_bwd_kernel<IO, W, true><<<grid, kConvThreads, smem, s>>>(a);
-    else kla_conv_bwd_kernel<IO, W, false><<<grid, kConvThreads, smem, s>>>(a);
-    return cudaGetLastError();
+template <typename IO, int W, bool ACT>
+cudaError_t launch_bwd(ConvArgs a, int num_sms, cudaStream_t s) {
+  const long long bh = (long long)a.B * a.H;
+  a.chunks_per_block = kConvThreads / (a.D / 4);
+  const long long TT = (long long)a.chunks_per_block * conv_rows<W>();
+  const size_t smem = 2 * (size_t)kConvBwdStages * TT * a.D * sizeof(IO) + 2 * (size_t)TT * a.D * sizeof(float);
+  auto fn = kla_conv_bwd_kernel<IO, W, ACT>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kConvThreads, smem)) != cudaSuccess) return e;
+  const long long slots = (long long)std::max(occ, 1) * num_sms;
+  const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
+  // never more ranges than the partial-sum workspace was sized for
+  const long long nsplit =
+      std::max(1LL, std::min({nst, slots / bh, conv_bwd_splits(bh, a.T, TT, num_sms)}));
+  a.range = (int)(TT * ((nst + nsplit - 1) / nsplit));
+  const long long blocks_y = a.T > 0 ? ((long long)a.T + a.range - 1) / a.range : 1;
+  a.nparts = a.part ? (long long)a.B * blocks_y : 0;
+  fn<<<dim3((unsigned)bh, (unsigned)blocks_y), kConvThreads, smem, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.gweight || a.gbias) {
+    const long long n = (long long)a.H * a.D * (W + 1);
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
+    kla_conv_bwd_finish_kernel<<<blocks, 256, 0, s>>>(a, W);
+    e = cudaGetLastError();
   }
+  return e;
+}
+
+template <typename IO, int W>
+cudaError_t launch_w(const ConvArgs& a, bool backward, int num_sms, cudaStream_t s) {
+  if (backward) return a.act ? launch_bwd<IO, W, true>(a, num_sms, s) : launch_bwd<IO, W, false>(a, num_sms, s);
   return a.act ? launch_fwd<IO, W, true>(a, num_sms, s) : launch_fwd<IO, W, false>(a, num_sms, s);
 }
 
 template <typename IO>
-cudaError_t launch_io(const ConvArgs& a, bool backward, dim3 grid, size_t smem, int num_sms, cudaStream_t s) {
+cudaError_t launch_io(const ConvArgs& a, bool backward, int num_sms, cudaStream_t s) {
   switch (a.W) {
-    case 1: return launch_w<IO, 1>(a, backward, grid, smem, num_sms, s);
-    case 2: return launch_w<IO, 2>(a, backward, grid, smem, num_sms, s);
-    case 3: return launch_w<IO, 3>(a, backward, grid, smem, num_sms, s);
-    case 4: return launch_w<IO, 4>(a, backward, grid, smem, num_sms, s);
-    case 5: return launch_w<IO, 5>(a, backward, grid, smem, num_sms, s);
-    case 6: return launch_w<IO, 6>(a, backward, grid, smem, num_sms, s);
-    case 7: return launch_w<IO, 7>(a, backward, grid, smem, num_sms, s);
-    case 8: return launch_w<IO, 8>(a, backward, grid, smem, num_sms, s);
+    case 1: return launch_w<IO, 1>(a, backward, num_sms, s);
+    case 2: return launch_w<IO, 2>(a, backward, num_sms, s);
+    case 3: return launch_w<IO, 3>(a, backward, num_sms, s);
+    case 4: return launch_w<IO, 4>(a, backward, num_sms, s);
+    case 5: return launch_w<IO, 5>(a, backward, num_sms, s);
+    case 6: return launch_w<IO, 6>(a, backward, num_sms, s);
+    case 7: return launch_w<IO, 7>(a, backward, num_sms, s);
+    case 8: return launch_w<IO, 8>(a, backward, num_sms, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-ConvPlan conv_plan(long long bh, int T, int D, int W, int num_sms) {
-  ConvPlan p{};
-  const int G = D / 4;
-  p.chunks_per_block = kConvThreads / G;
-  p.threads = kConvThreads;
-  // Backward: shortest per-thread chunk (≥ 16 tokens, a power of two) that
-  // keeps the grid within about four blocks per SM, so the recomputed W−1
-  // inputs at each chunk's ends stay a small share.
-  auto blocks_y = [&](long long L) {
-    const long long chunks = T > 0 ? (T + L - 1) / L : 1;
-    return (chunks + p.chunks_per_block - 1) / p.chunks_per_block;
-  };
-  long long L = 16;
-  while (L < (1 << 20) && (bh * blocks_y(L) > 4LL * num_sms || blocks_y(L) > 65535)) L *= 2;
-  p.L = (int)L;
-  p.blocks_y = (int)blocks_y(L);
-  p.nparts = 0;  // set per batch count by the caller: B · blocks_y
-  p.smem_bwd = (size_t)p.chunks_per_block * G * (W + 1) * sizeof(float4);
-  return p;
+// Ranges per stream of the backward: enough for two blocks per SM, at most
+// one per stage of TT tokens.
+long long conv_bwd_splits(long long bh, int T, long long TT, int num_sms) {
+  const long long nst = std::max(1LL, ((long long)T + TT - 1) / TT);
+  return std::max(1LL, std::min(nst, 2LL * num_sms / std::max(bh, 1LL)));
 }
 
-size_t conv_partial_bytes(int B, int H, int D, int W, const ConvPlan& p) {
-  return (size_t)H * B * p.blocks_y * D * (W + 1) * sizeof(float);
+size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms) {
+  const long long bh = (long long)B * H;
+  if (bh == 0) return 0;
+  const long long TT = (long long)(kConvThreads / (D / 4)) * (W > 5 ? 8 : 4);
+  const long long nst = std::max(1LL, ((long long)T + TT - 1) / TT);
+  const long long nsplit = conv_bwd_splits(bh, T, TT, num_sms);
+  const long long range = TT * ((nst + nsplit - 1) / nsplit);
+  const long long blocks_y = T > 0 ? ((long long)T + range - 1) / range : 1;
+  return (size_t)H * B * blocks_y * D * (W + 1) * sizeof(float);
 }
 
 cudaError_t launch_conv(const ConvArgs& a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
   if (bh == 0) return cudaSuccess;
-  return a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, false, dim3(), 0, num_sms, s)
-                         : launch_io<float>(a, false, dim3(), 0, num_sms, s);
+  return a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, false, num_sms, s) : launch_io<float>(a, false, num_sms, s);
 }
 
-cudaError_t launch_conv_backward(const ConvArgs& a, const ConvPlan& p, cudaStream_t s) {
+cudaError_t launch_conv_backward(const ConvArgs& a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
-  if (bh > 0) {
-    const dim3 grid((unsigned)bh, (unsigned)p.blocks_y);
-    const cudaError_t e = a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, true, grid, p.smem_bwd, 0, s)
-                                          : launch_io<float>(a, true, grid, p.smem_bwd, 0, s);
-    if (e != cudaSuccess) return e;
-  }
-  if (a.H > 0 && (a.gweight || a.gbias)) {
+  if (bh > 0)
+    return a.io == IO_BF16 ? launch_io<__nv_bfloat16>(a, true, num_sms, s) : launch_io<float>(a, true, num_sms, s);
+  if (a.H > 0 && (a.gweight || a.gbias)) {  // no batch: the sums are zero
     const long long n = (long long)a.H * a.D * (a.W + 1);
     const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
-    kla_conv_bwd_finish_kernel<<<blocks, 256, 0, s>>>(a, a.W);
+    ConvArgs z = a;
+    z.nparts = 0;
+    kla_conv_bwd_finish_kernel<<<blocks, 256, 0, s>>>(z, a.W);
     return cudaGetLastError();
   }
   return cudaSuccess;

@@ -110,22 +110,20 @@ struct ConvArgs {
   void *gx, *gwin;    // backward outputs (io)
   float *gweight, *gbias;
   float* part;        // backward block partials [H][nparts][D][W+1], or null (no gweight/gbias)
-  long long nparts;   // B · blocks along T
+  long long nparts;   // B · blocks along T; set by the backward launcher
   int B, H, T, D, W;
   int io, act;
-  int L, chunks_per_block;  // backward: tokens per thread chunk; chunks per block
-  int range;                // forward: tokens per block (set by launch_conv)
+  int chunks_per_block;  // token groups (of four or eight) per stage; set by the launchers
+  int range;             // tokens per block; set by the launchers
 };
-struct ConvPlan {
-  int L, chunks_per_block, threads, blocks_y;
-  long long nparts;
-  size_t smem_bwd;
-};
-// The backward's geometry and its partial-sum workspace.
-ConvPlan conv_plan(long long bh, int T, int D, int W, int num_sms);
-size_t conv_partial_bytes(int B, int H, int D, int W, const ConvPlan& p);
-// The forward chooses its own geometry (shared-memory stages, tokens per block).
+// Both launchers choose their geometry (shared-memory stages, tokens per
+// block) from the kernel's occupancy on `num_sms` SMs. The backward's
+// per-block partial sums of the tap and bias gradients need
+// conv_partial_bytes() of workspace in `part` (an upper bound over the
+// geometries the launcher can choose).
+long long conv_bwd_splits(long long bh, int T, long long TT, int num_sms);
+size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms);
 cudaError_t launch_conv(const ConvArgs& a, int num_sms, cudaStream_t s);
-cudaError_t launch_conv_backward(const ConvArgs& a, const ConvPlan& p, cudaStream_t s);
+cudaError_t launch_conv_backward(const ConvArgs& a, int num_sms, cudaStream_t s);
 
 }  // namespace kla
