@@ -230,7 +230,7 @@ bool ranges_overlap(const void* x, size_t nx, const void* y, size_t ny) {
 // Shape checks of the causal convolution entry points.
 kla_status check_conv_shape(int B, int H, int T, int D, int W) {
   if (B < 0 || H < 0 || T < 0) return KLA_ERR_INVALID_ARG;
-  if (D < 4 || D > 1024 || D % 4 != 0 || W < 1 || W > 8) return KLA_ERR_UNSUPPORTED_SHAPE;
+  if (D < 4 || D > 512 || D % 4 != 0 || W < 1 || W > 8) return KLA_ERR_UNSUPPORTED_SHAPE;
   const long long bh = (long long)B * H;
   if (bh > INT_MAX) return KLA_ERR_UNSUPPORTED_SHAPE;
   if (bh > 0 && (long long)T > (1LL << 46) / (bh * D)) return KLA_ERR_UNSUPPORTED_SHAPE;

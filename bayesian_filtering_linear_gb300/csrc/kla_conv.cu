@@ -30,6 +30,7 @@
 // shared memory, and a second kernel sums the blocks' partials in a fixed
 // order. No atomics.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda_bf16.h>
 
@@ -41,10 +42,11 @@ namespace kla {
 namespace {
 
 constexpr int kConvThreads = 256;
-// forward: consecutive tokens per thread and stage; eight for W > 5 so that a
-// stage (at least one thread's rows) always holds the W−1 rows before the next
-template <int W>
-__host__ __device__ constexpr int conv_rows() { return W > 5 ? 8 : 4; }
+constexpr int kMaxDevices = 256;
+// Consecutive tokens per thread and stage. With D ≤ 512 a stage holds at
+// least two threads' rows, eight tokens, so it always covers the W − 1 ≤ 7
+// rows that the next stage reads before its start.
+constexpr int kConvRows = 4;
 constexpr int kConvStages = 4;     // forward: shared-memory stages (three in flight)
 constexpr int kConvBwdStages = 3;  // backward: stages of x and gy (two in flight)
 
@@ -108,7 +110,7 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int R = conv_rows<W>(), S = kConvStages;
+  constexpr int R = kConvRows, S = kConvStages;
   const int D = a.D, G = D >> 2, T = a.T;
   const int cpb = a.chunks_per_block, TT = cpb * R;
   const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g;
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int R = conv_rows<W>(), S = kConvBwdStages;
+  constexpr int R = kConvRows, S = kConvBwdStages;
   const int D = a.D, G = D >> 2, T = a.T;
   const int cpb = a.chunks_per_block, TT = cpb * R;
   const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g;
@@ -336,7 +338,8 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
   };
   // gradient of the window in: tokens −(W−1) … −1, all reached by stage 0's gu
   auto emit_window = [&]() {
-    if (W == 1 || blockIdx.y != 0 || !gwin) return;
+    if constexpr (W == 1) return;
+    if (blockIdx.y != 0 || !gwin) return;
     for (int i = tid; i < G * (W - 1); i += kConvThreads) {
       const int j = i / G, gg = i - j * G;
       const long long te = (long long)j - (W - 1);
@@ -421,9 +424,10 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
 
   if (!a.part) return;  // no tap or bias gradient wanted
   // Block partial: the threads of a channel group summed in chunk order,
-  // through shared memory (the gu ring is free now).
+  // through shared memory (all of it is free now: 16·(W+1)·256 bytes at
+  // most, under the 20·TT·D ≥ 20·1024 bytes of the stages and the gu ring).
   __syncthreads();
-  float4* red = reinterpret_cast<float4*>(gus);  // [cpb][G][W + 1]
+  float4* red = reinterpret_cast<float4*>(smem);  // [cpb][G][W + 1]
   if (c < cpb) {
     float4* r = red + ((size_t)c * G + g) * (W + 1);
 #pragma unroll
@@ -466,6 +470,30 @@ __global__ void __launch_bounds__(256) kla_conv_bwd_finish_kernel(const ConvArgs
   }
 }
 
+// Blocks per SM of kernel `fn` with `smem_max` bytes of dynamic shared
+// memory — the most any launch of that instantiation asks for (a stage holds
+// at most 256 threads' rows: TT·D ≤ 1024·kConvRows) — with the kernel's shared-memory
+// limit raised to it; looked up once per kernel and device and cached.
+template <typename F>
+cudaError_t blocks_per_sm(F fn, size_t smem_max, int* occ) {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kConvThreads, smem_max)) != cudaSuccess)
+      return e;
+    n = std::max(n, 1);
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  *occ = n;
+  return cudaSuccess;
+}
+
 // Forward launch: blocks of one stream split its tokens into ranges of whole
 // stages, as many ranges as keep every block of the grid resident at once
 // (one wave; streams beyond that are whole-sequence blocks in later waves).
@@ -473,13 +501,13 @@ template <typename IO, int W, bool ACT>
 cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
   a.chunks_per_block = kConvThreads / (a.D / 4);
-  const long long TT = (long long)a.chunks_per_block * conv_rows<W>();
+  const long long TT = (long long)a.chunks_per_block * kConvRows;
   const size_t smem = (size_t)kConvStages * TT * a.D * sizeof(IO);
+  constexpr size_t smem_max = (size_t)kConvStages * 1024 * kConvRows * sizeof(IO);
   auto fn = kla_conv_kernel<IO, W, ACT>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int occ = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kConvThreads, smem)) != cudaSuccess) return e;
+  const cudaError_t e = blocks_per_sm(fn, smem_max, &occ);
+  if (e != cudaSuccess) return e;
   const long long slots = (long long)std::max(occ, 1) * num_sms;
   const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
   const long long nsplit = std::max(1LL, std::min(nst, slots / bh));
@@ -493,13 +521,14 @@ template <typename IO, int W, bool ACT>
 cudaError_t launch_bwd(ConvArgs a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
   a.chunks_per_block = kConvThreads / (a.D / 4);
-  const long long TT = (long long)a.chunks_per_block * conv_rows<W>();
+  const long long TT = (long long)a.chunks_per_block * kConvRows;
   const size_t smem = 2 * (size_t)kConvBwdStages * TT * a.D * sizeof(IO) + 2 * (size_t)TT * a.D * sizeof(float);
+  constexpr size_t smem_max =
+      (2 * (size_t)kConvBwdStages * sizeof(IO) + 2 * sizeof(float)) * 1024 * kConvRows;
   auto fn = kla_conv_bwd_kernel<IO, W, ACT>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int occ = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kConvThreads, smem)) != cudaSuccess) return e;
+  cudaError_t e = blocks_per_sm(fn, smem_max, &occ);
+  if (e != cudaSuccess) return e;
   const long long slots = (long long)std::max(occ, 1) * num_sms;
   const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
   // never more ranges than the partial-sum workspace was sized for
@@ -552,7 +581,7 @@ long long conv_bwd_splits(long long bh, int T, long long TT, int num_sms) {
 size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms) {
   const long long bh = (long long)B * H;
   if (bh == 0) return 0;
-  const long long TT = (long long)(kConvThreads / (D / 4)) * (W > 5 ? 8 : 4);
+  const long long TT = (long long)(kConvThreads / (D / 4)) * kConvRows;
   const long long nst = std::max(1LL, ((long long)T + TT - 1) / TT);
   const long long nsplit = conv_bwd_splits(bh, T, TT, num_sms);
   const long long range = TT * ((nst + nsplit - 1) / nsplit);

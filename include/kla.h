@@ -308,7 +308,7 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
  *     (window_in, x), the window_in of the next call. It may be window_in
  *     itself (an in-place update) but must not overlap it otherwise, nor x or y.
  *   With W = 1 the windows are empty and their pointers are ignored.
- *   D: a multiple of 4 in [4, 1024]; W in [1, 8] (else UNSUPPORTED_SHAPE);
+ *   D: a multiple of 4 in [4, 512]; W in [1, 8] (else UNSUPPORTED_SHAPE);
  *   B, H, T ≥ 0 (T = 0 only copies the window). activation: kla_activation
  *   (else INVALID_ARG). Pointers 16-byte aligned (else MISALIGNED). */
 typedef enum kla_activation { KLA_ACT_NONE = 0, KLA_ACT_SILU = 1 } kla_activation;

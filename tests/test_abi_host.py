@@ -301,7 +301,7 @@ def conv_call(B=1, H=1, T=8, D=16, W=4, io=kla.F32, act=kla.ACT_SILU, x=None, we
 
 def test_conv_validates_before_any_cuda_call():
     assert conv_call(D=6) == kla.ERR_UNSUPPORTED_SHAPE       # not a multiple of 4
-    assert conv_call(D=2048) == kla.ERR_UNSUPPORTED_SHAPE
+    assert conv_call(D=1024) == kla.ERR_UNSUPPORTED_SHAPE
     assert conv_call(W=0) == kla.ERR_UNSUPPORTED_SHAPE
     assert conv_call(W=9) == kla.ERR_UNSUPPORTED_SHAPE
     assert conv_call(T=-1) == kla.ERR_INVALID_ARG

@@ -90,9 +90,9 @@ CASES = [  # B, H, T, D, W
     (1, 2, 50, 8, 7),
     (2, 2, 99, 8, 8),
     (1, 3, 33, 12, 4),    # three channel groups: 85 chunks per block
-    (1, 1, 40, 1024, 4),  # one chunk per block
-    (1, 1, 40, 1024, 8),  # eight tokens a stage, seven rows of window
-    (2, 1, 9, 1024, 7),
+    (1, 1, 40, 512, 4),   # the widest stream: eight tokens a stage
+    (1, 1, 40, 512, 8),   # seven rows of window from the previous stage
+    (2, 1, 9, 512, 7),
     (1, 1, 3000, 4, 8),   # one channel group; 8-byte rows in bf16
     (1, 2, 777, 20, 3),   # five channel groups; 8-byte copies in bf16
     (3, 2, 5000, 16, 4),  # several blocks along T: batch and block partials
