@@ -474,9 +474,10 @@ __global__ void __launch_bounds__(256) kla_conv_bwd_finish_kernel(const ConvArgs
 // memory — the most any launch of that instantiation asks for (a stage holds
 // at most 256 threads' rows: TT·D ≤ 1024·kConvRows) — with the kernel's shared-memory
 // limit raised to it; looked up once per kernel and device and cached.
-template <typename F>
-cudaError_t blocks_per_sm(F fn, size_t smem_max, int* occ) {
-  static std::atomic<int> cache[kMaxDevices];
+template <auto Kernel>
+cudaError_t blocks_per_sm(size_t smem_max, int* occ) {
+  static std::atomic<int> cache[kMaxDevices];  // one per kernel instantiation
+  const auto fn = Kernel;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -506,7 +507,7 @@ cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   constexpr size_t smem_max = (size_t)kConvStages * 1024 * kConvRows * sizeof(IO);
   auto fn = kla_conv_kernel<IO, W, ACT>;
   int occ = 0;
-  const cudaError_t e = blocks_per_sm(fn, smem_max, &occ);
+  const cudaError_t e = blocks_per_sm<kla_conv_kernel<IO, W, ACT>>(smem_max, &occ);
   if (e != cudaSuccess) return e;
   const long long slots = (long long)std::max(occ, 1) * num_sms;
   const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
@@ -527,7 +528,7 @@ cudaError_t launch_bwd(ConvArgs a, int num_sms, cudaStream_t s) {
       (2 * (size_t)kConvBwdStages * sizeof(IO) + 2 * sizeof(float)) * 1024 * kConvRows;
   auto fn = kla_conv_bwd_kernel<IO, W, ACT>;
   int occ = 0;
-  cudaError_t e = blocks_per_sm(fn, smem_max, &occ);
+  cudaError_t e = blocks_per_sm<kla_conv_bwd_kernel<IO, W, ACT>>(smem_max, &occ);
   if (e != cudaSuccess) return e;
   const long long slots = (long long)std::max(occ, 1) * num_sms;
   const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
