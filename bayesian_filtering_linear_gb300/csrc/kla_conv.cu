@@ -159,41 +159,53 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
 
   float4 w[W], bias;
   load_taps<W>(a, h, d0, w, bias);
-  const long long nst = (T1 - T0 + TT - 1) / TT;
-  for (long long n = 0; n < nst; ++n) {
+  // y of one token from its W input rows xr[j … j+W−1]
+  auto output = [&](const float4 (&xr)[R + W - 1], int j) {
+    float4 u = bias;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const float4 xv = xr[j + k];
+      u.x = fmaf(w[k].x, xv.x, u.x);
+      u.y = fmaf(w[k].y, xv.y, u.y);
+      u.z = fmaf(w[k].z, xv.z, u.z);
+      u.w = fmaf(w[k].w, xv.w, u.w);
+    }
+    if (ACT) {
+      u.x *= sigmoid_fast(u.x);
+      u.y *= sigmoid_fast(u.y);
+      u.z *= sigmoid_fast(u.z);
+      u.w *= sigmoid_fast(u.w);
+    }
+    return u;
+  };
+  // The S stage buffers are one ring of S·TT rows; stage n starts at row
+  // (n mod S)·TT, and the rows before it wrap from the ring's end. Offsets
+  // inside a stage are 32-bit; the stage's global base is formed once.
+  const IO* ring = reinterpret_cast<const IO*>(smem);
+  const int ring_rows = S * TT, r0 = c * R;
+  const int nst = (int)((T1 - T0 + TT - 1) / TT);
+  for (int n = 0; n < nst; ++n) {
     cp_async_wait<S - 2>();
     __syncthreads();  // stage n (and the halo) landed for every thread
-    if (c < cpb) {
-      const IO* cur = buf(n);
-      const IO* prev = buf(n + S - 1);
-      const long long ts = T0 + n * TT + (long long)c * R;  // first token of this thread
+    const long long t_stage = T0 + (long long)n * TT;
+    const int rows = (int)min((long long)TT, T1 - t_stage);  // tokens of this stage
+    if (c < cpb && r0 < rows) {
+      const int q0 = (n % S) * TT + r0 - (W - 1);
       float4 xr[R + W - 1];
 #pragma unroll
       for (int i = 0; i < R + W - 1; ++i) {
-        const int r = c * R - (W - 1) + i;  // row within the stage (negative: previous stage)
-        if (ts - (W - 1) + i < T1)
-          xr[i] = r >= 0 ? lds4ch(cur + (size_t)r * D + d0) : lds4ch(prev + (size_t)(TT + r) * D + d0);
+        int q = q0 + i;
+        q += q < 0 ? ring_rows : 0;
+        xr[i] = lds4ch(ring + q * D + d0);  // rows past the stage's end are read but not used
       }
+      IO* yo = yg + t_stage * D + d0 + r0 * D;
+      if (r0 + R <= rows) {
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        if (ts + j < T1) {
-          float4 u = bias;
+        for (int j = 0; j < R; ++j) store4ch(yo + j * D, output(xr, j));
+      } else {
 #pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const float4 xv = xr[j + k];
-            u.x = fmaf(w[k].x, xv.x, u.x);
-            u.y = fmaf(w[k].y, xv.y, u.y);
-            u.z = fmaf(w[k].z, xv.z, u.z);
-            u.w = fmaf(w[k].w, xv.w, u.w);
-          }
-          if (ACT) {
-            u.x *= sigmoid_fast(u.x);
-            u.y *= sigmoid_fast(u.y);
-            u.z *= sigmoid_fast(u.z);
-            u.w *= sigmoid_fast(u.w);
-          }
-          store4ch(yg + (ts + j) * D + d0, u);
-        }
+        for (int j = 0; j < R; ++j)
+          if (r0 + j < rows) store4ch(yo + j * D, output(xr, j));
       }
     }
     __syncthreads();  // nobody reads buffer (n − 1) any more
@@ -308,31 +320,53 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
 #pragma unroll
   for (int k = 0; k < W; ++k) gw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  // gx of this thread's tokens in stage m (gu of stage m, and of m + 1 past its end)
-  auto emit = [&](long long m) {
+  // gx of this thread's tokens in stage m: gu of stage m, and of m + 1 past
+  // its end (the two gu buffers form a ring of 2·TT rows). Full stages away
+  // from the sequence end take the path without per-token checks.
+  const int r0 = c * R;
+  auto emit = [&](int m) {
     if (c >= cpb) return;
-    const long long sm0 = T0 + m * TT;
-    const float* gu_m = gus + (size_t)(m & 1) * gu_stage;
-    const float* gu_n = gus + (size_t)((m + 1) & 1) * gu_stage;
+    const long long sm0 = T0 + (long long)m * TT;
+    const long long last = sm0 + r0 + R - 1;  // this thread's last token
+    const int gq0 = (m & 1) * TT + r0 + (W - 1);  // gu row of token sm0 + r0 + W − 1
+    IO* go = gxg + sm0 * D + d0 + r0 * D;
+    auto gx_of = [&](int j, float4 gv) {
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        int q = gq0 + j - k;
+        q -= q >= 2 * TT ? 2 * TT : 0;
+        const float4 gu = lds4ch(gus + q * D + d0);
+        gv.x = fmaf(w[k].x, gu.x, gv.x);
+        gv.y = fmaf(w[k].y, gu.y, gv.y);
+        gv.z = fmaf(w[k].z, gu.z, gv.z);
+        gv.w = fmaf(w[k].w, gu.w, gv.w);
+      }
+      return gv;
+    };
+    if (last < T1 && last + (W - 1) < T1e && !(gwo && last >= tail)) {
+#pragma unroll
+      for (int j = 0; j < R; ++j) store4ch(go + j * D, gx_of(j, make_float4(0.f, 0.f, 0.f, 0.f)));
+      return;
+    }
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const long long te = sm0 + c * R + j;
+      const long long te = sm0 + r0 + j;
       if (te < T1) {
         float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
         if (gwo && te >= tail) gv = load4ch(gwo + (te - tail) * D + d0);
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-          const long long tt = te + (W - 1) - k;  // gu of token tt meets tap k
-          if (tt < T1e) {
-            const int r = (int)(tt - sm0);
-            const float4 gu = lds4ch(r < TT ? gu_m + (size_t)r * D + d0 : gu_n + (size_t)(r - TT) * D + d0);
+          if (te + (W - 1) - k < T1e) {  // gu of later tokens is zero
+            int q = gq0 + j - k;
+            q -= q >= 2 * TT ? 2 * TT : 0;
+            const float4 gu = lds4ch(gus + q * D + d0);
             gv.x = fmaf(w[k].x, gu.x, gv.x);
             gv.y = fmaf(w[k].y, gu.y, gv.y);
             gv.z = fmaf(w[k].z, gu.z, gv.z);
             gv.w = fmaf(w[k].w, gu.w, gv.w);
           }
         }
-        store4ch(gxg + te * D + d0, gv);
+        store4ch(go + j * D, gv);
       }
     }
   };
@@ -361,55 +395,68 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
     }
   };
 
-  const long long nst = (T1e - T0 + TT - 1) / TT;
-  for (long long n = 0; n < nst; ++n) {
+  // gu of one token (row j of this thread) from gy and its W input rows;
+  // its terms are added to the partial sums when `own`
+  auto grad_u = [&](const float4 (&xr)[R + W - 1], const IO* gyr, int j, bool own) {
+    float4 gu = gyg ? lds4ch(gyr + j * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ACT) {
+      float4 u = bias;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        u.x = fmaf(w[k].x, xr[j + k].x, u.x);
+        u.y = fmaf(w[k].y, xr[j + k].y, u.y);
+        u.z = fmaf(w[k].z, xr[j + k].z, u.z);
+        u.w = fmaf(w[k].w, xr[j + k].w, u.w);
+      }
+      float sg = sigmoid_fast(u.x);
+      gu.x *= sg * fmaf(u.x, 1.0f - sg, 1.0f);
+      sg = sigmoid_fast(u.y);
+      gu.y *= sg * fmaf(u.y, 1.0f - sg, 1.0f);
+      sg = sigmoid_fast(u.z);
+      gu.z *= sg * fmaf(u.z, 1.0f - sg, 1.0f);
+      sg = sigmoid_fast(u.w);
+      gu.w *= sg * fmaf(u.w, 1.0f - sg, 1.0f);
+    }
+    if (own) {
+      gb.x += gu.x; gb.y += gu.y; gb.z += gu.z; gb.w += gu.w;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        gw[k].x = fmaf(gu.x, xr[j + k].x, gw[k].x);
+        gw[k].y = fmaf(gu.y, xr[j + k].y, gw[k].y);
+        gw[k].z = fmaf(gu.z, xr[j + k].z, gw[k].z);
+        gw[k].w = fmaf(gu.w, xr[j + k].w, gw[k].w);
+      }
+    }
+    return gu;
+  };
+  const int ring_rows = S * TT;
+  const int nst = (int)((T1e - T0 + TT - 1) / TT);
+  for (int n = 0; n < nst; ++n) {
     cp_async_wait<S - 2>();
     __syncthreads();  // stage n landed; gx of stage n − 2 is done with its gu
-    if (c < cpb) {
-      const IO* xc = xs + (size_t)(n % S) * TT * D;
-      const IO* xp = xs + (size_t)((n + S - 1) % S) * TT * D;
-      const IO* gyc = gys + (size_t)(n % S) * TT * D;
-      float* gu_out = gus + (size_t)(n & 1) * gu_stage;
-      const long long ts = T0 + n * TT + (long long)c * R;
+    const long long t_stage = T0 + (long long)n * TT;
+    const int rows = (int)min((long long)TT, T1e - t_stage);  // tokens whose gu is needed
+    const int own = (int)max(0LL, min((long long)TT, T1 - t_stage));  // of those, tokens of this range
+    if (c < cpb && r0 < rows) {
+      const int q0 = (n % S) * TT + r0 - (W - 1);
       float4 xr[R + W - 1];
 #pragma unroll
       for (int i = 0; i < R + W - 1; ++i) {
-        const int r = c * R - (W - 1) + i;
-        if (ts - (W - 1) + i < T1e)
-          xr[i] = r >= 0 ? lds4ch(xc + (size_t)r * D + d0) : lds4ch(xp + (size_t)(TT + r) * D + d0);
+        int q = q0 + i;
+        q += q < 0 ? ring_rows : 0;
+        xr[i] = lds4ch(xs + q * D + d0);  // rows past the stage's end are read but not used
       }
+      const IO* gyr = gys + ((n % S) * TT + r0) * D + d0;
+      float* gu_out = gus + ((n & 1) * TT + r0) * D + d0;
+      if (r0 + R <= own) {  // every token needed and of this range
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        float4 gu = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ts + j < T1e) {
-          if (gyg) gu = lds4ch(gyc + (size_t)(c * R + j) * D + d0);
-          if (ACT) {
-            float4 u = bias;
+        for (int j = 0; j < R; ++j) *reinterpret_cast<float4*>(gu_out + j * D) = grad_u(xr, gyr, j, true);
+      } else {
 #pragma unroll
-            for (int k = 0; k < W; ++k) {
-              u.x = fmaf(w[k].x, xr[j + k].x, u.x);
-              u.y = fmaf(w[k].y, xr[j + k].y, u.y);
-              u.z = fmaf(w[k].z, xr[j + k].z, u.z);
-              u.w = fmaf(w[k].w, xr[j + k].w, u.w);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float ue = f4get(u, e), sg = sigmoid_fast(ue);
-              f4set(gu, e, f4get(gu, e) * (sg * fmaf(ue, 1.0f - sg, 1.0f)));
-            }
-          }
-          if (ts + j < T1) {
-            gb.x += gu.x; gb.y += gu.y; gb.z += gu.z; gb.w += gu.w;
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-              gw[k].x = fmaf(gu.x, xr[j + k].x, gw[k].x);
-              gw[k].y = fmaf(gu.y, xr[j + k].y, gw[k].y);
-              gw[k].z = fmaf(gu.z, xr[j + k].z, gw[k].z);
-              gw[k].w = fmaf(gu.w, xr[j + k].w, gw[k].w);
-            }
-          }
+        for (int j = 0; j < R; ++j) {
+          const float4 gu = r0 + j < rows ? grad_u(xr, gyr, j, r0 + j < own) : make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(gu_out + j * D) = gu;
         }
-        *reinterpret_cast<float4*>(gu_out + (size_t)(c * R + j) * D + d0) = gu;
       }
     }
     __syncthreads();  // gu of stage n visible; x and gy of stage n − 1 no longer read
