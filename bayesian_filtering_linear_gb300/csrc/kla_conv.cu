@@ -15,15 +15,12 @@
 //                out for the last W−1 inputs; tokens before 0 go to gwindow)
 //   gw[h,d,k]  = Σ_{b,t} gu[t] · x[t − (W−1) + k],   gbias[h,d] = Σ_{b,t} gu[t]
 //
-// Work layout: a thread owns four channels of one head and a chunk of L
-// tokens, and walks them in order with the last W inputs (and, backward, the
-// last W values of gu) in a register ring; the ring index of each token is a
-// compile-time constant because the walk is unrolled by W. Threads of a block
-// cover consecutive channel groups, then consecutive chunks of one (b, h), so
-// each token row is read by consecutive threads. The chunk's first W−1 inputs
-// (and, backward, its last W−1 values of gu) are the neighbouring chunk's and
-// are recomputed, not exchanged. Both kernels stream from HBM: the bound is
-// the bytes of x, y (and gy, gx).
+// Work layout: a block owns a token range of one stream (b, h) and streams
+// it through shared-memory stages with cp.async; a thread computes four
+// consecutive tokens × four channels of a stage, the channels as two packed
+// fp32 pairs (fma/mul/add.rn.f32x2), with the exponential and reciprocal of
+// SiLU on the MUFU unit. Both kernels stream from HBM: the bound is the bytes
+// of x, y (and gy, gx).
 //
 // The backward's sums over (b, t) are deterministic: each thread sums its own
 // chunk in token order, a block sums its threads in chunk order through
@@ -49,48 +46,76 @@ constexpr int kMaxDevices = 256;
 constexpr int kConvRows = 4;
 constexpr int kConvStages = 4;     // forward: shared-memory stages (three in flight)
 constexpr int kConvBwdStages = 3;  // backward: stages of x and gy (two in flight)
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x·log2 e)
 
-__device__ __forceinline__ float4 load4ch(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ float4 load4ch(const __nv_bfloat16* p) {
+// ---- four channels as two packed fp32 pairs (channels 0, 1 and 2, 3) --------
+struct V4 {
+  f2 a, b;
+};
+__device__ __forceinline__ V4 v4_zero() { return {f2_make(0.f, 0.f), f2_make(0.f, 0.f)}; }
+__device__ __forceinline__ V4 v4_from(float4 v) { return {f2_make(v.x, v.y), f2_make(v.z, v.w)}; }
+// a bf16 pair (one 32-bit word) as fp32: the bf16 bits are the top half of the fp32 word
+__device__ __forceinline__ f2 bf2_to_f2(uint32_t v) {
+  return f2_make(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(f2 v) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(f2_lo(v), f2_hi(v));  // round to nearest even
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// global, read-only path
+__device__ __forceinline__ V4 ldg4(const float* p) { return v4_from(__ldg(reinterpret_cast<const float4*>(p))); }
+__device__ __forceinline__ V4 ldg4(const __nv_bfloat16* p) {
   const uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
-  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
-  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
-  return make_float4(lo.x, lo.y, hi.x, hi.y);
+  return {bf2_to_f2(r.x), bf2_to_f2(r.y)};
 }
-__device__ __forceinline__ void store4ch(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-__device__ __forceinline__ void store4ch(__nv_bfloat16* p, float4 v) {
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-  uint2 r;
-  r.x = *reinterpret_cast<const uint32_t*>(&lo);
-  r.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(p) = r;
+// shared memory
+__device__ __forceinline__ V4 lds4(const float* p) {
+  const ulonglong2 r = *reinterpret_cast<const ulonglong2*>(p);
+  return {r.x, r.y};
 }
-
-// Four channels of one row from shared memory.
-__device__ __forceinline__ float4 lds4ch(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 lds4ch(const __nv_bfloat16* p) {
+__device__ __forceinline__ V4 lds4(const __nv_bfloat16* p) {
   const uint2 r = *reinterpret_cast<const uint2*>(p);
-  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
-  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
-  return make_float4(lo.x, lo.y, hi.x, hi.y);
+  return {bf2_to_f2(r.x), bf2_to_f2(r.y)};
 }
-
-__device__ __forceinline__ float f4get(const float4& v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; }
-__device__ __forceinline__ void f4set(float4& v, int e, float s) {
-  if (e == 0) v.x = s; else if (e == 1) v.y = s; else if (e == 2) v.z = s; else v.w = s;
+__device__ __forceinline__ void sts4(float* p, V4 v) { *reinterpret_cast<ulonglong2*>(p) = make_ulonglong2(v.a, v.b); }
+// global stores
+__device__ __forceinline__ void stg4(float* p, V4 v) { *reinterpret_cast<ulonglong2*>(p) = make_ulonglong2(v.a, v.b); }
+__device__ __forceinline__ void stg4(__nv_bfloat16* p, V4 v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(f2_to_bf2(v.a), f2_to_bf2(v.b));
 }
+__device__ __forceinline__ V4 fma4(V4 w, V4 x, V4 acc) { return {f2_fma(w.a, x.a, acc.a), f2_fma(w.b, x.b, acc.b)}; }
 
-// σ(u) with the hardware reciprocal; 0 for u below about −88 (e^−u overflows).
-__device__ __forceinline__ float sigmoid_fast(float u) { return rcp_approx(1.0f + __expf(-u)); }
+// Base-2 exponential on the MUFU unit (PTX ex2.approx; 0 for large negative input).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// σ(u) = 1 / (1 + 2^(−u·log2 e)) of a pair; 0 once 2^(…) overflows (u below about −88).
+__device__ __forceinline__ f2 sigmoid2(f2 u) {
+  const f2 t = f2_mul(u, f2_make(-kLog2e, -kLog2e));
+  const f2 e = f2_make(ex2_approx(f2_lo(t)), ex2_approx(f2_hi(t)));
+  return f2_rcp(f2_add(e, f2_make(1.0f, 1.0f)));
+}
+// SiLU(u) = u·σ(u)
+__device__ __forceinline__ V4 silu4(V4 u) { return {f2_mul(u.a, sigmoid2(u.a)), f2_mul(u.b, sigmoid2(u.b))}; }
+// SiLU'(u) = σ(u)(1 + u(1 − σ(u)))
+__device__ __forceinline__ f2 dsilu2(f2 u) {
+  const f2 one = f2_make(1.0f, 1.0f);
+  const f2 sg = sigmoid2(u);
+  const f2 one_minus = f2_fma(sg, f2_make(-1.0f, -1.0f), one);
+  return f2_mul(sg, f2_fma(u, one_minus, one));
+}
 
 template <int W>
-__device__ __forceinline__ void load_taps(const ConvArgs& a, int h, int d0, float4 (&w)[W], float4& bias) {
+__device__ __forceinline__ void load_taps(const ConvArgs& a, int h, int d0, V4 (&w)[W], V4& bias) {
   const float* wp = a.weight + ((size_t)h * a.D + d0) * W;  // [H][D][W]: four channels' taps are contiguous
 #pragma unroll
-  for (int k = 0; k < W; ++k)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) f4set(w[k], e, __ldg(wp + e * W + k));
-  bias = a.bias ? __ldg(reinterpret_cast<const float4*>(a.bias + (size_t)h * a.D + d0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < W; ++k) {
+    w[k].a = f2_make(__ldg(wp + 0 * W + k), __ldg(wp + 1 * W + k));
+    w[k].b = f2_make(__ldg(wp + 2 * W + k), __ldg(wp + 3 * W + k));
+  }
+  bias = a.bias ? ldg4(a.bias + (size_t)h * a.D + d0) : v4_zero();
 }
 
 // 8-byte asynchronous copy (rows of bf16 streams whose width is not a
@@ -99,90 +124,81 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gmem_src) 
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
 }
 
+// Queue the copy of `bytes` contiguous bytes (a multiple of 8; of 16 when
+// `wide`) from global to shared memory, spread over the block's threads.
+__device__ __forceinline__ void copy_span(void* dst, const void* src, int bytes, bool wide, int tid) {
+  char* d = reinterpret_cast<char*>(dst);
+  const char* s = reinterpret_cast<const char*>(src);
+  if (wide) {
+    for (int o = tid * 16; o < bytes; o += kConvThreads * 16) cp_async16(d + o, s + o);
+  } else {
+    for (int o = tid * 8; o < bytes; o += kConvThreads * 8) cp_async8(d + o, s + o);
+  }
+}
+
+// The W − 1 input rows before a block's first token, at the end of the last
+// stage buffer: x when the range does not start the sequence, else the
+// carried window, else zeros.
+template <typename IO, int W>
+__device__ __forceinline__ void stage_halo(IO* halo, const IO* xg, const IO* win, long long T0, int D, int row,
+                                           bool wide, int tid) {
+  if (W == 1) return;
+  if (T0 > 0) {
+    copy_span(halo, xg + (T0 - (W - 1)) * D, (W - 1) * row, wide, tid);
+  } else if (win) {
+    copy_span(halo, win, (W - 1) * row, wide, tid);
+  } else {
+    for (int i = tid; i < (W - 1) * D; i += kConvThreads) halo[i] = from_f32<IO>(0.0f);
+  }
+}
+
 // Forward: a block owns the token range [T0, T1) of one stream (b, h) and
 // streams it through kConvStages shared-memory stages of TT tokens (all D
 // channels; a stage is one contiguous span of x) with cp.async, kConvStages−1
 // stages in flight. Thread (g, c) computes tokens c·R … c·R+R−1 of a stage for
-// channels 4g … 4g+3, reading its R+W−1 input rows from shared memory (rows
-// before the stage from the previous stage's buffer, which is refilled only
-// after the stage is done). The W−1 rows before T0 — x, the carried window,
-// or zeros — are placed at the end of the last buffer before the first stage.
+// channels 4g … 4g+3, reading its R+W−1 input rows from shared memory. The S
+// stage buffers form one ring of S·TT rows; the rows before a stage are the
+// end of the previous buffer (refilled only after the stage is done), and the
+// W−1 rows before T0 sit at the end of the ring before the first stage.
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int R = kConvRows, S = kConvStages;
   const int D = a.D, G = D >> 2, T = a.T;
   const int cpb = a.chunks_per_block, TT = cpb * R;
-  const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g;
+  const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g, r0 = c * R;
   const long long bh = blockIdx.x;
   const int h = (int)(bh % a.H);
   const long long T0 = (long long)blockIdx.y * a.range, T1 = min(T0 + (long long)a.range, (long long)T);
-  const size_t row = (size_t)D * sizeof(IO);
-  const size_t stage_bytes = (size_t)TT * row;
+  const int row = D * (int)sizeof(IO);
+  const bool wide = row % 16 == 0;  // 16-byte copies; else 8-byte ones
   const IO* __restrict__ xg = reinterpret_cast<const IO*>(a.x) + bh * (long long)T * D;
   IO* __restrict__ yg = reinterpret_cast<IO*>(a.y) + bh * (long long)T * D;
   const IO* win = a.win ? reinterpret_cast<const IO*>(a.win) + bh * (long long)(W - 1) * D : nullptr;
-  auto buf = [&](long long n) { return reinterpret_cast<IO*>(smem + (size_t)(n % S) * stage_bytes); };
-  const bool wide = row % 16 == 0;  // 16-byte copies; else 8-byte ones
+  IO* ring = reinterpret_cast<IO*>(smem);
+  const int ring_rows = S * TT;
 
-  // Queue the copy of `bytes` contiguous bytes (a multiple of 8) into shared memory.
-  auto copy_span = [&](void* dst, const void* src, size_t bytes) {
-    char* d = reinterpret_cast<char*>(dst);
-    const char* s0 = reinterpret_cast<const char*>(src);
-    if (wide) {
-      for (size_t o = (size_t)tid * 16; o < bytes; o += kConvThreads * 16) cp_async16(d + o, s0 + o);
-    } else {
-      for (size_t o = (size_t)tid * 8; o < bytes; o += kConvThreads * 8) cp_async8(d + o, s0 + o);
-    }
+  auto stage_copy = [&](int n) {
+    const long long ts = T0 + (long long)n * TT;
+    const int rows = (int)min((long long)TT, T1 - ts);
+    if (rows > 0) copy_span(ring + (n % S) * TT * D, xg + ts * D, rows * row, wide, tid);
   };
-  auto stage_copy = [&](long long n) {
-    const long long ts = T0 + n * TT, te = min(ts + TT, T1);
-    if (ts < te) copy_span(buf(n), xg + ts * D, (size_t)(te - ts) * row);
-  };
-
-  // rows before T0, at the end of buffer S−1 (= the buffer before stage 0)
-  if (W > 1) {
-    IO* halo = reinterpret_cast<IO*>(smem + (size_t)(S - 1) * stage_bytes) + (size_t)(TT - (W - 1)) * D;
-    if (T0 > 0) {
-      copy_span(halo, xg + (T0 - (W - 1)) * D, (size_t)(W - 1) * row);
-    } else if (win) {
-      copy_span(halo, win, (size_t)(W - 1) * row);
-    } else {
-      for (int i = tid; i < (W - 1) * D; i += kConvThreads) halo[i] = from_f32<IO>(0.0f);
-    }
-  }
+  stage_halo<IO, W>(ring + (ring_rows - (W - 1)) * D, xg, win, T0, D, row, wide, tid);
 #pragma unroll
   for (int n = 0; n < S - 1; ++n) {
     stage_copy(n);
     cp_async_commit();
   }
 
-  float4 w[W], bias;
+  V4 w[W], bias;
   load_taps<W>(a, h, d0, w, bias);
-  // y of one token from its W input rows xr[j … j+W−1]
-  auto output = [&](const float4 (&xr)[R + W - 1], int j) {
-    float4 u = bias;
+  // y of the token at row j of this thread, from input rows xr[j … j+W−1]
+  auto output = [&](const V4 (&xr)[R + W - 1], int j) {
+    V4 u = bias;
 #pragma unroll
-    for (int k = 0; k < W; ++k) {
-      const float4 xv = xr[j + k];
-      u.x = fmaf(w[k].x, xv.x, u.x);
-      u.y = fmaf(w[k].y, xv.y, u.y);
-      u.z = fmaf(w[k].z, xv.z, u.z);
-      u.w = fmaf(w[k].w, xv.w, u.w);
-    }
-    if (ACT) {
-      u.x *= sigmoid_fast(u.x);
-      u.y *= sigmoid_fast(u.y);
-      u.z *= sigmoid_fast(u.z);
-      u.w *= sigmoid_fast(u.w);
-    }
-    return u;
+    for (int k = 0; k < W; ++k) u = fma4(w[k], xr[j + k], u);
+    return ACT ? silu4(u) : u;
   };
-  // The S stage buffers are one ring of S·TT rows; stage n starts at row
-  // (n mod S)·TT, and the rows before it wrap from the ring's end. Offsets
-  // inside a stage are 32-bit; the stage's global base is formed once.
-  const IO* ring = reinterpret_cast<const IO*>(smem);
-  const int ring_rows = S * TT, r0 = c * R;
   const int nst = (int)((T1 - T0 + TT - 1) / TT);
   for (int n = 0; n < nst; ++n) {
     cp_async_wait<S - 2>();
@@ -191,21 +207,21 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
     const int rows = (int)min((long long)TT, T1 - t_stage);  // tokens of this stage
     if (c < cpb && r0 < rows) {
       const int q0 = (n % S) * TT + r0 - (W - 1);
-      float4 xr[R + W - 1];
+      V4 xr[R + W - 1];
 #pragma unroll
       for (int i = 0; i < R + W - 1; ++i) {
         int q = q0 + i;
         q += q < 0 ? ring_rows : 0;
-        xr[i] = lds4ch(ring + q * D + d0);  // rows past the stage's end are read but not used
+        xr[i] = lds4(ring + q * D + d0);  // rows past the stage's end are read but not used
       }
       IO* yo = yg + t_stage * D + d0 + r0 * D;
       if (r0 + R <= rows) {
 #pragma unroll
-        for (int j = 0; j < R; ++j) store4ch(yo + j * D, output(xr, j));
+        for (int j = 0; j < R; ++j) stg4(yo + j * D, output(xr, j));
       } else {
 #pragma unroll
         for (int j = 0; j < R; ++j)
-          if (r0 + j < rows) store4ch(yo + j * D, output(xr, j));
+          if (r0 + j < rows) stg4(yo + j * D, output(xr, j));
       }
     }
     __syncthreads();  // nobody reads buffer (n − 1) any more
@@ -219,17 +235,17 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
   // any is written, so the window out may be the window in.
   if (W > 1 && blockIdx.y == 0 && a.wout) {
     IO* wout = reinterpret_cast<IO*>(a.wout) + bh * (long long)(W - 1) * D;
-    // item i = tid + q·256 < G·(W−1): window row i / G, channel group i % G (G ≤ 256)
-    float4 v[W > 1 ? W - 1 : 1];
+    // item i = tid + q·256 < G·(W−1): window row i / G, channel group i % G (G ≤ 128)
+    V4 v[W > 1 ? W - 1 : 1];
 #pragma unroll
     for (int q = 0; q < W - 1; ++q) {
       const int i = tid + q * kConvThreads;
-      v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      v[q] = v4_zero();
       if (i < G * (W - 1)) {
         const int j = i / G, gg = i - j * G;
         const long long tau = (long long)T - (W - 1) + j;
-        if (tau >= 0) v[q] = load4ch(xg + tau * D + 4 * gg);
-        else if (win) v[q] = load4ch(win + (tau + W - 1) * D + 4 * gg);
+        if (tau >= 0) v[q] = ldg4(xg + tau * D + 4 * gg);
+        else if (win) v[q] = ldg4(win + (tau + W - 1) * D + 4 * gg);
       }
     }
     __syncthreads();
@@ -238,7 +254,7 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
       const int i = tid + q * kConvThreads;
       if (i < G * (W - 1)) {
         const int j = i / G, gg = i - j * G;
-        store4ch(wout + (long long)j * D + 4 * gg, v[q]);
+        stg4(wout + (long long)j * D + 4 * gg, v[q]);
       }
     }
   }
@@ -248,30 +264,30 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a
 // needed on [T0, T1e), T1e = min(T1 + W − 1, T) (gx of the range's last
 // tokens reaches W − 1 tokens further), so x and gy stream through
 // kConvBwdStages shared-memory stages over [T0, T1e) (x with the W − 1 rows
-// before T0 at the end of the last buffer, as in the forward). Stage n: each
-// thread forms gu of its R tokens × 4 channels into a two-stage fp32 ring in
-// shared memory and adds its tokens below T1 to its tap and bias partial
-// sums; then gx of stage n − 1 is complete and is written (gu rows past the
-// stage come from stage n; tokens at or past T1e have gu = 0). The first
-// block of a stream also writes the gradient of the window in (tokens −(W−1)
-// … −1) once stage 0's gu exists.
+// before T0 at the end of its ring, as in the forward). Stage n: each thread
+// forms gu of its R tokens × 4 channels into a two-stage fp32 ring in shared
+// memory and adds its tokens below T1 to its tap and bias partial sums; then
+// gx of stage n − 1 is complete and is written (gu rows past the stage come
+// from stage n; tokens at or past T1e have gu = 0). The first block of a
+// stream also writes the gradient of the window in (tokens −(W−1) … −1) once
+// stage 0's gu exists.
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int R = kConvRows, S = kConvBwdStages;
   const int D = a.D, G = D >> 2, T = a.T;
   const int cpb = a.chunks_per_block, TT = cpb * R;
-  const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g;
+  const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g, r0 = c * R;
   const long long bh = blockIdx.x;
   const int h = (int)(bh % a.H);
   const long long T0 = (long long)blockIdx.y * a.range, T1 = min(T0 + (long long)a.range, (long long)T);
   const long long T1e = min(T1 + (W - 1), (long long)T);
-  const size_t row = (size_t)D * sizeof(IO);
-  const size_t stage_bytes = (size_t)TT * row;
-  const size_t gu_stage = (size_t)TT * D;  // floats
-  IO* xs = reinterpret_cast<IO*>(smem);
-  IO* gys = reinterpret_cast<IO*>(smem + (size_t)S * stage_bytes);
-  float* gus = reinterpret_cast<float*>(smem + 2 * (size_t)S * stage_bytes);
+  const int row = D * (int)sizeof(IO);
+  const bool wide = row % 16 == 0;
+  const int ring_rows = S * TT;
+  IO* xs = reinterpret_cast<IO*>(smem);                           // x ring, S·TT rows
+  IO* gys = xs + (size_t)ring_rows * D;                           // gy stages
+  float* gus = reinterpret_cast<float*>(gys + (size_t)ring_rows * D);  // gu ring, 2·TT rows
   const long long off = bh * (long long)T * D;
   const IO* __restrict__ xg = reinterpret_cast<const IO*>(a.x) + off;
   const IO* __restrict__ gyg = a.gy ? reinterpret_cast<const IO*>(a.gy) + off : nullptr;  // null: zero
@@ -281,92 +297,52 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
   const IO* gwo = a.gwout ? reinterpret_cast<const IO*>(a.gwout) + woff : nullptr;
   IO* gwin = a.gwin ? reinterpret_cast<IO*>(a.gwin) + woff : nullptr;
   const long long tail = (long long)T - (W - 1);  // first input copied into the window out
-  const bool wide = row % 16 == 0;
 
-  auto copy_span = [&](void* dst, const void* src, size_t bytes) {
-    char* d = reinterpret_cast<char*>(dst);
-    const char* s0 = reinterpret_cast<const char*>(src);
-    if (wide) {
-      for (size_t o = (size_t)tid * 16; o < bytes; o += kConvThreads * 16) cp_async16(d + o, s0 + o);
-    } else {
-      for (size_t o = (size_t)tid * 8; o < bytes; o += kConvThreads * 8) cp_async8(d + o, s0 + o);
-    }
+  auto stage_copy = [&](int n) {
+    const long long ts = T0 + (long long)n * TT;
+    const int rows = (int)min((long long)TT, T1e - ts);
+    if (rows <= 0) return;
+    copy_span(xs + (n % S) * TT * D, xg + ts * D, rows * row, wide, tid);
+    if (gyg) copy_span(gys + (n % S) * TT * D, gyg + ts * D, rows * row, wide, tid);
   };
-  auto stage_copy = [&](long long n) {
-    const long long ts = T0 + n * TT, te = min(ts + TT, T1e);
-    if (ts >= te) return;
-    const size_t b = (size_t)(n % S) * stage_bytes;
-    copy_span(reinterpret_cast<char*>(xs) + b, xg + ts * D, (size_t)(te - ts) * row);
-    if (gyg) copy_span(reinterpret_cast<char*>(gys) + b, gyg + ts * D, (size_t)(te - ts) * row);
-  };
-  if (W > 1) {
-    IO* halo = xs + (size_t)(S - 1) * TT * D + (size_t)(TT - (W - 1)) * D;
-    if (T0 > 0) {
-      copy_span(halo, xg + (T0 - (W - 1)) * D, (size_t)(W - 1) * row);
-    } else if (win) {
-      copy_span(halo, win, (size_t)(W - 1) * row);
-    } else {
-      for (int i = tid; i < (W - 1) * D; i += kConvThreads) halo[i] = from_f32<IO>(0.0f);
-    }
-  }
+  stage_halo<IO, W>(xs + (ring_rows - (W - 1)) * D, xg, win, T0, D, row, wide, tid);
 #pragma unroll
   for (int n = 0; n < S - 1; ++n) {
     stage_copy(n);
     cp_async_commit();
   }
 
-  float4 w[W], bias, gw[W], gb = make_float4(0.f, 0.f, 0.f, 0.f);
+  V4 w[W], bias, gw[W], gb = v4_zero();
   load_taps<W>(a, h, d0, w, bias);
 #pragma unroll
-  for (int k = 0; k < W; ++k) gw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < W; ++k) gw[k] = v4_zero();
 
-  // gx of this thread's tokens in stage m: gu of stage m, and of m + 1 past
-  // its end (the two gu buffers form a ring of 2·TT rows). Full stages away
+  // gx of this thread's tokens in stage m from gu rows r0 … r0+R+W−2 of the
+  // two-stage gu ring (rows past stage m are stage m + 1's). Full stages away
   // from the sequence end take the path without per-token checks.
-  const int r0 = c * R;
   auto emit = [&](int m) {
     if (c >= cpb) return;
     const long long sm0 = T0 + (long long)m * TT;
     const long long last = sm0 + r0 + R - 1;  // this thread's last token
-    const int gq0 = (m & 1) * TT + r0 + (W - 1);  // gu row of token sm0 + r0 + W − 1
-    IO* go = gxg + sm0 * D + d0 + r0 * D;
-    auto gx_of = [&](int j, float4 gv) {
+    if (sm0 + r0 >= T1) return;
+    const int q0 = (m & 1) * TT + r0;
+    const bool full = last < T1 && last + (W - 1) < T1e && !(gwo && last >= tail);
+    V4 gr[R + W - 1];
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        int q = gq0 + j - k;
-        q -= q >= 2 * TT ? 2 * TT : 0;
-        const float4 gu = lds4ch(gus + q * D + d0);
-        gv.x = fmaf(w[k].x, gu.x, gv.x);
-        gv.y = fmaf(w[k].y, gu.y, gv.y);
-        gv.z = fmaf(w[k].z, gu.z, gv.z);
-        gv.w = fmaf(w[k].w, gu.w, gv.w);
-      }
-      return gv;
-    };
-    if (last < T1 && last + (W - 1) < T1e && !(gwo && last >= tail)) {
-#pragma unroll
-      for (int j = 0; j < R; ++j) store4ch(go + j * D, gx_of(j, make_float4(0.f, 0.f, 0.f, 0.f)));
-      return;
+    for (int i = 0; i < R + W - 1; ++i) {
+      int q = q0 + i;
+      q -= q >= 2 * TT ? 2 * TT : 0;
+      gr[i] = (full || sm0 + r0 + i < T1e) ? lds4(gus + q * D + d0) : v4_zero();  // gu past T1e is zero
     }
+    IO* go = gxg + sm0 * D + d0 + r0 * D;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       const long long te = sm0 + r0 + j;
-      if (te < T1) {
-        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (gwo && te >= tail) gv = load4ch(gwo + (te - tail) * D + d0);
+      if (full || te < T1) {
+        V4 gv = (!full && gwo && te >= tail) ? ldg4(gwo + (te - tail) * D + d0) : v4_zero();
 #pragma unroll
-        for (int k = 0; k < W; ++k) {
-          if (te + (W - 1) - k < T1e) {  // gu of later tokens is zero
-            int q = gq0 + j - k;
-            q -= q >= 2 * TT ? 2 * TT : 0;
-            const float4 gu = lds4ch(gus + q * D + d0);
-            gv.x = fmaf(w[k].x, gu.x, gv.x);
-            gv.y = fmaf(w[k].y, gu.y, gv.y);
-            gv.z = fmaf(w[k].z, gu.z, gv.z);
-            gv.w = fmaf(w[k].w, gu.w, gv.w);
-          }
-        }
-        store4ch(go + j * D, gv);
+        for (int k = 0; k < W; ++k) gv = fma4(w[k], gr[j + (W - 1) - k], gv);  // gu of token te + W−1−k
+        stg4(go + j * D, gv);
       }
     }
   };
@@ -377,59 +353,37 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
     for (int i = tid; i < G * (W - 1); i += kConvThreads) {
       const int j = i / G, gg = i - j * G;
       const long long te = (long long)j - (W - 1);
-      float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (gwo && te >= tail) gv = load4ch(gwo + (te - tail) * D + 4 * gg);
-      const float* wp = a.weight + ((size_t)h * D + 4 * gg) * W;
+      V4 gv = (gwo && te >= tail) ? ldg4(gwo + (te - tail) * D + 4 * gg) : v4_zero();
+      V4 wg[W], bg;
+      load_taps<W>(a, h, 4 * gg, wg, bg);
 #pragma unroll
       for (int k = 0; k < W; ++k) {
         const long long tt = te + (W - 1) - k;
-        if (tt >= 0 && tt < T1e) {
-          const float4 gu = lds4ch(gus + (size_t)tt * D + 4 * gg);  // stage 0 (tt < W − 1 ≤ TT)
-          gv.x = fmaf(__ldg(wp + 0 * W + k), gu.x, gv.x);
-          gv.y = fmaf(__ldg(wp + 1 * W + k), gu.y, gv.y);
-          gv.z = fmaf(__ldg(wp + 2 * W + k), gu.z, gv.z);
-          gv.w = fmaf(__ldg(wp + 3 * W + k), gu.w, gv.w);
-        }
+        if (tt >= 0 && tt < T1e) gv = fma4(wg[k], lds4(gus + tt * D + 4 * gg), gv);  // stage 0: tt < W−1 ≤ TT
       }
-      store4ch(gwin + (long long)j * D + 4 * gg, gv);
+      stg4(gwin + (long long)j * D + 4 * gg, gv);
     }
   };
 
-  // gu of one token (row j of this thread) from gy and its W input rows;
-  // its terms are added to the partial sums when `own`
-  auto grad_u = [&](const float4 (&xr)[R + W - 1], const IO* gyr, int j, bool own) {
-    float4 gu = gyg ? lds4ch(gyr + j * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+  // gu of the token at row j of this thread, from gy and input rows
+  // xr[j … j+W−1]; added to the partial sums when `own`
+  auto grad_u = [&](const V4 (&xr)[R + W - 1], const IO* gyr, int j, bool own) {
+    V4 gu = gyg ? lds4(gyr + j * D) : v4_zero();
     if (ACT) {
-      float4 u = bias;
+      V4 u = bias;
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        u.x = fmaf(w[k].x, xr[j + k].x, u.x);
-        u.y = fmaf(w[k].y, xr[j + k].y, u.y);
-        u.z = fmaf(w[k].z, xr[j + k].z, u.z);
-        u.w = fmaf(w[k].w, xr[j + k].w, u.w);
-      }
-      float sg = sigmoid_fast(u.x);
-      gu.x *= sg * fmaf(u.x, 1.0f - sg, 1.0f);
-      sg = sigmoid_fast(u.y);
-      gu.y *= sg * fmaf(u.y, 1.0f - sg, 1.0f);
-      sg = sigmoid_fast(u.z);
-      gu.z *= sg * fmaf(u.z, 1.0f - sg, 1.0f);
-      sg = sigmoid_fast(u.w);
-      gu.w *= sg * fmaf(u.w, 1.0f - sg, 1.0f);
+      for (int k = 0; k < W; ++k) u = fma4(w[k], xr[j + k], u);
+      gu.a = f2_mul(gu.a, dsilu2(u.a));
+      gu.b = f2_mul(gu.b, dsilu2(u.b));
     }
     if (own) {
-      gb.x += gu.x; gb.y += gu.y; gb.z += gu.z; gb.w += gu.w;
+      gb.a = f2_add(gb.a, gu.a);
+      gb.b = f2_add(gb.b, gu.b);
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        gw[k].x = fmaf(gu.x, xr[j + k].x, gw[k].x);
-        gw[k].y = fmaf(gu.y, xr[j + k].y, gw[k].y);
-        gw[k].z = fmaf(gu.z, xr[j + k].z, gw[k].z);
-        gw[k].w = fmaf(gu.w, xr[j + k].w, gw[k].w);
-      }
+      for (int k = 0; k < W; ++k) gw[k] = fma4(gu, xr[j + k], gw[k]);
     }
     return gu;
   };
-  const int ring_rows = S * TT;
   const int nst = (int)((T1e - T0 + TT - 1) / TT);
   for (int n = 0; n < nst; ++n) {
     cp_async_wait<S - 2>();
@@ -439,24 +393,21 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
     const int own = (int)max(0LL, min((long long)TT, T1 - t_stage));  // of those, tokens of this range
     if (c < cpb && r0 < rows) {
       const int q0 = (n % S) * TT + r0 - (W - 1);
-      float4 xr[R + W - 1];
+      V4 xr[R + W - 1];
 #pragma unroll
       for (int i = 0; i < R + W - 1; ++i) {
         int q = q0 + i;
         q += q < 0 ? ring_rows : 0;
-        xr[i] = lds4ch(xs + q * D + d0);  // rows past the stage's end are read but not used
+        xr[i] = lds4(xs + q * D + d0);  // rows past the stage's end are read but not used
       }
       const IO* gyr = gys + ((n % S) * TT + r0) * D + d0;
       float* gu_out = gus + ((n & 1) * TT + r0) * D + d0;
       if (r0 + R <= own) {  // every token needed and of this range
 #pragma unroll
-        for (int j = 0; j < R; ++j) *reinterpret_cast<float4*>(gu_out + j * D) = grad_u(xr, gyr, j, true);
+        for (int j = 0; j < R; ++j) sts4(gu_out + j * D, grad_u(xr, gyr, j, true));
       } else {
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const float4 gu = r0 + j < rows ? grad_u(xr, gyr, j, r0 + j < own) : make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(gu_out + j * D) = gu;
-        }
+        for (int j = 0; j < R; ++j) sts4(gu_out + j * D, r0 + j < rows ? grad_u(xr, gyr, j, r0 + j < own) : v4_zero());
       }
     }
     __syncthreads();  // gu of stage n visible; x and gy of stage n − 1 no longer read
@@ -474,19 +425,19 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
   // through shared memory (all of it is free now: 16·(W+1)·256 bytes at
   // most, under the 20·TT·D ≥ 20·1024 bytes of the stages and the gu ring).
   __syncthreads();
-  float4* red = reinterpret_cast<float4*>(smem);  // [cpb][G][W + 1]
+  float* red = reinterpret_cast<float*>(smem);  // [cpb][G][W + 1] groups of four floats
   if (c < cpb) {
-    float4* r = red + ((size_t)c * G + g) * (W + 1);
+    float* r = red + ((size_t)c * G + g) * (W + 1) * 4;
 #pragma unroll
-    for (int k = 0; k < W; ++k) r[k] = gw[k];
-    r[W] = gb;
+    for (int k = 0; k < W; ++k) sts4(r + 4 * k, gw[k]);
+    sts4(r + 4 * W, gb);
   }
   __syncthreads();
   for (int i = tid; i < G * (W + 1); i += kConvThreads) {
     const int gg = i / (W + 1), k = i - gg * (W + 1);
-    float4 sum = red[(size_t)gg * (W + 1) + k];
+    float4 sum = *reinterpret_cast<const float4*>(red + ((size_t)gg * (W + 1) + k) * 4);
     for (int cc = 1; cc < cpb; ++cc) {
-      const float4 v = red[((size_t)cc * G + gg) * (W + 1) + k];
+      const float4 v = *reinterpret_cast<const float4*>(red + (((size_t)cc * G + gg) * (W + 1) + k) * 4);
       sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
     }
     // partials [H][P][D][W + 1], P = B · gridDim.y, p = b · gridDim.y + blockIdx.y
