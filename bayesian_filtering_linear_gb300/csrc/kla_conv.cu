@@ -44,8 +44,15 @@ constexpr int kMaxDevices = 256;
 // least two threads' rows, eight tokens, so it always covers the W − 1 ≤ 7
 // rows that the next stage reads before its start.
 constexpr int kConvRows = 4;
-constexpr int kConvStages = 4;     // forward: shared-memory stages (three in flight)
-constexpr int kConvBwdStages = 3;  // backward: stages of x and gy (two in flight)
+// Shared-memory stages (a stage is TT·D ≈ 4096 elements; stages − 2 are in
+// flight while one is computed). The kernels are bound by the bytes in
+// flight per SM — HBM latency under load is microseconds — so the rings are
+// as deep as two or three blocks per SM allow: forward 64 KB (bf16) or 96 KB
+// (fp32) per block, backward (x and gy rings plus 32 KB of gu) 112 KB (bf16)
+// or 192 KB (fp32).
+template <typename IO>
+__host__ __device__ constexpr int conv_stages() { return sizeof(IO) == 2 ? 8 : 6; }
+constexpr int kConvBwdStages = 5;
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x·log2 e)
 
 // ---- four channels as two packed fp32 pairs (channels 0, 1 and 2, 3) --------
@@ -153,9 +160,9 @@ __device__ __forceinline__ void stage_halo(IO* halo, const IO* xg, const IO* win
 }
 
 // Forward: a block owns the token range [T0, T1) of one stream (b, h) and
-// streams it through kConvStages shared-memory stages of TT tokens (all D
-// channels; a stage is one contiguous span of x) with cp.async, kConvStages−1
-// stages in flight. Thread (g, c) computes tokens c·R … c·R+R−1 of a stage for
+// streams it through S shared-memory stages of TT tokens (all D channels; a
+// stage is one contiguous span of x) with cp.async, S − 2 stages in flight
+// while one is computed. Thread (g, c) computes tokens c·R … c·R+R−1 of a stage for
 // channels 4g … 4g+3, reading its R+W−1 input rows from shared memory. The S
 // stage buffers form one ring of S·TT rows; the rows before a stage are the
 // end of the previous buffer (refilled only after the stage is done), and the
@@ -163,7 +170,7 @@ __device__ __forceinline__ void stage_halo(IO* halo, const IO* xg, const IO* win
 template <typename IO, int W, bool ACT>
 __global__ void __launch_bounds__(kConvThreads) kla_conv_kernel(const ConvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  constexpr int R = kConvRows, S = kConvStages;
+  constexpr int R = kConvRows, S = conv_stages<IO>();
   const int D = a.D, G = D >> 2, T = a.T;
   const int cpb = a.chunks_per_block, TT = cpb * R;
   const int tid = threadIdx.x, c = tid / G, g = tid - c * G, d0 = 4 * g, r0 = c * R;
@@ -501,8 +508,8 @@ cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
   a.chunks_per_block = kConvThreads / (a.D / 4);
   const long long TT = (long long)a.chunks_per_block * kConvRows;
-  const size_t smem = (size_t)kConvStages * TT * a.D * sizeof(IO);
-  constexpr size_t smem_max = (size_t)kConvStages * 1024 * kConvRows * sizeof(IO);
+  const size_t smem = (size_t)conv_stages<IO>() * TT * a.D * sizeof(IO);
+  constexpr size_t smem_max = (size_t)conv_stages<IO>() * 1024 * kConvRows * sizeof(IO);
   auto fn = kla_conv_kernel<IO, W, ACT>;
   int occ = 0;
   const cudaError_t e = blocks_per_sm<kla_conv_kernel<IO, W, ACT>>(smem_max, &occ);
