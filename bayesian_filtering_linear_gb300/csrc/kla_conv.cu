@@ -325,30 +325,51 @@ __global__ void __launch_bounds__(kConvThreads) kla_conv_bwd_kernel(const ConvAr
   for (int k = 0; k < W; ++k) gw[k] = v4_zero();
 
   // gx of this thread's tokens in stage m from gu rows r0 … r0+R+W−2 of the
-  // two-stage gu ring (rows past stage m are stage m + 1's). Full stages away
-  // from the sequence end take the path without per-token checks.
+  // two-stage gu ring (rows past stage m are stage m + 1's). Positions are
+  // 32-bit offsets from the stage start; a thread whose tokens are all below
+  // T1, whose gu rows are all below T1e and which has no window-out gradient
+  // takes the path without checks.
   auto emit = [&](int m) {
     if (c >= cpb) return;
     const long long sm0 = T0 + (long long)m * TT;
-    const long long last = sm0 + r0 + R - 1;  // this thread's last token
-    if (sm0 + r0 >= T1) return;
+    const int lim1 = (int)min((long long)(2 * TT), T1 - sm0);    // rows below T1
+    const int lim1e = (int)min((long long)(2 * TT), T1e - sm0);  // rows below T1e
+    if (r0 >= lim1) return;
     const int q0 = (m & 1) * TT + r0;
-    const bool full = last < T1 && last + (W - 1) < T1e && !(gwo && last >= tail);
+    IO* go = gxg + sm0 * D + d0 + r0 * D;
     V4 gr[R + W - 1];
+    const bool has_tail = gwo && sm0 + r0 + R - 1 >= tail;
+    if (r0 + R <= lim1 && r0 + R + W - 1 <= lim1e && !has_tail) {
+#pragma unroll
+      for (int i = 0; i < R + W - 1; ++i) {
+        int q = q0 + i;
+        q -= q >= 2 * TT ? 2 * TT : 0;
+        gr[i] = lds4(gus + q * D + d0);
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        V4 gv = v4_zero();
+#pragma unroll
+        for (int k = 0; k < W; ++k) gv = fma4(w[k], gr[j + (W - 1) - k], gv);  // gu of token j + W−1−k
+        stg4(go + j * D, gv);
+      }
+      return;
+    }
+    // row of the first input copied into the window out (a row of this stage
+    // at or after it is a token within W − 1 of T, so clamping is exact)
+    const int tl = (int)max(-8LL, min(tail - sm0, 2LL * TT + 1));
 #pragma unroll
     for (int i = 0; i < R + W - 1; ++i) {
       int q = q0 + i;
       q -= q >= 2 * TT ? 2 * TT : 0;
-      gr[i] = (full || sm0 + r0 + i < T1e) ? lds4(gus + q * D + d0) : v4_zero();  // gu past T1e is zero
+      gr[i] = r0 + i < lim1e ? lds4(gus + q * D + d0) : v4_zero();  // gu past T1e is zero
     }
-    IO* go = gxg + sm0 * D + d0 + r0 * D;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const long long te = sm0 + r0 + j;
-      if (full || te < T1) {
-        V4 gv = (!full && gwo && te >= tail) ? ldg4(gwo + (te - tail) * D + d0) : v4_zero();
+      if (r0 + j < lim1) {
+        V4 gv = (gwo && r0 + j >= tl) ? ldg4(gwo + (r0 + j - tl) * D + d0) : v4_zero();
 #pragma unroll
-        for (int k = 0; k < W; ++k) gv = fma4(w[k], gr[j + (W - 1) - k], gv);  // gu of token te + W−1−k
+        for (int k = 0; k < W; ++k) gv = fma4(w[k], gr[j + (W - 1) - k], gv);
         stg4(go + j * D, gv);
       }
     }
