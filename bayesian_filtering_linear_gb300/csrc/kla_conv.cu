@@ -496,34 +496,23 @@ __global__ void __launch_bounds__(256) kla_conv_bwd_finish_kernel(const ConvArgs
   }
 }
 
-// Blocks per SM of kernel `fn` with `smem_max` bytes of dynamic shared
-// memory — the most any launch of that instantiation asks for (a stage holds
-// at most 256 threads' rows: TT·D ≤ 1024·kConvRows) — with the kernel's shared-memory
-// limit raised to it; looked up once per kernel and device and cached.
+// Raise kernel `Kernel`'s dynamic shared-memory limit to `smem_max` — the
+// most any launch of that instantiation asks for (a stage holds at most 256
+// threads' rows: TT·D ≤ 1024·kConvRows) — once per device.
 template <auto Kernel>
-cudaError_t blocks_per_sm(size_t smem_max, int* occ) {
-  static std::atomic<int> cache[kMaxDevices];  // one per kernel instantiation
-  const auto fn = Kernel;
+cudaError_t prepare_kernel(size_t smem_max) {
+  static std::atomic<int> done[kMaxDevices];  // one set per kernel instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  int n = cache[dev].load(std::memory_order_relaxed);
-  if (n <= 0) {
-    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max)) != cudaSuccess)
-      return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kConvThreads, smem_max)) != cudaSuccess)
-      return e;
-    n = std::max(n, 1);
-    cache[dev].store(n, std::memory_order_relaxed);
-  }
-  *occ = n;
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  if ((e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max)) != cudaSuccess)
+    return e;
+  done[dev].store(1, std::memory_order_relaxed);
   return cudaSuccess;
 }
 
-// Forward launch: blocks of one stream split its tokens into ranges of whole
-// stages, as many ranges as keep every block of the grid resident at once
-// (one wave; streams beyond that are whole-sequence blocks in later waves).
 template <typename IO, int W, bool ACT>
 cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   const long long bh = (long long)a.B * a.H;
@@ -532,14 +521,10 @@ cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   const size_t smem = (size_t)conv_stages<IO>() * TT * a.D * sizeof(IO);
   constexpr size_t smem_max = (size_t)conv_stages<IO>() * 1024 * kConvRows * sizeof(IO);
   auto fn = kla_conv_kernel<IO, W, ACT>;
-  int occ = 0;
-  const cudaError_t e = blocks_per_sm<kla_conv_kernel<IO, W, ACT>>(smem_max, &occ);
+  const cudaError_t e = prepare_kernel<kla_conv_kernel<IO, W, ACT>>(smem_max);
   if (e != cudaSuccess) return e;
-  const long long slots = (long long)std::max(occ, 1) * num_sms;
-  const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
-  const long long nsplit = std::max(1LL, std::min(nst, slots / bh));
-  a.range = (int)(TT * ((nst + nsplit - 1) / nsplit));
-  const long long blocks_y = a.T > 0 ? ((long long)a.T + a.range - 1) / a.range : 1;
+  long long blocks_y = 0;
+  a.range = conv_range(bh, a.T, TT, num_sms, &blocks_y);
   fn<<<dim3((unsigned)bh, (unsigned)blocks_y), kConvThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -553,16 +538,10 @@ cudaError_t launch_bwd(ConvArgs a, int num_sms, cudaStream_t s) {
   constexpr size_t smem_max =
       (2 * (size_t)kConvBwdStages * sizeof(IO) + 2 * sizeof(float)) * 1024 * kConvRows;
   auto fn = kla_conv_bwd_kernel<IO, W, ACT>;
-  int occ = 0;
-  cudaError_t e = blocks_per_sm<kla_conv_bwd_kernel<IO, W, ACT>>(smem_max, &occ);
+  cudaError_t e = prepare_kernel<kla_conv_bwd_kernel<IO, W, ACT>>(smem_max);
   if (e != cudaSuccess) return e;
-  const long long slots = (long long)std::max(occ, 1) * num_sms;
-  const long long nst = std::max(1LL, ((long long)a.T + TT - 1) / TT);
-  // never more ranges than the partial-sum workspace was sized for
-  const long long nsplit =
-      std::max(1LL, std::min({nst, slots / bh, conv_bwd_splits(bh, a.T, TT, num_sms)}));
-  a.range = (int)(TT * ((nst + nsplit - 1) / nsplit));
-  const long long blocks_y = a.T > 0 ? ((long long)a.T + a.range - 1) / a.range : 1;
+  long long blocks_y = 0;
+  a.range = conv_range(bh, a.T, TT, num_sms, &blocks_y);  // the rule conv_partial_bytes() sizes for
   a.nparts = a.part ? (long long)a.B * blocks_y : 0;
   fn<<<dim3((unsigned)bh, (unsigned)blocks_y), kConvThreads, smem, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -598,21 +577,38 @@ cudaError_t launch_io(const ConvArgs& a, bool backward, int num_sms, cudaStream_
 
 }  // namespace
 
-// Ranges per stream of the backward: enough for two blocks per SM, at most
-// one per stage of TT tokens.
-long long conv_bwd_splits(long long bh, int T, long long TT, int num_sms) {
+// Tokens per block. Both kernels are issue-bound on their busiest SM, whose
+// time is the total work of the blocks it runs, so each stream is cut into
+// the number n of ranges (of whole stages) that minimises the busiest SM's
+// share, ceil(B·H·n / SMs) / n — for 128 streams on 152 SMs, n = 7 is within
+// 2% of an even spread — with at least eight stages per range so that a
+// block's pipeline fill stays a small part of its work; ties go to the
+// smaller n.
+int conv_range(long long bh, int T, long long TT, int num_sms, long long* blocks_y) {
   const long long nst = std::max(1LL, ((long long)T + TT - 1) / TT);
-  return std::max(1LL, std::min(nst, 2LL * num_sms / std::max(bh, 1LL)));
+  const long long nmax = std::min(512LL, std::max(1LL, nst / 8));
+  const long long sms = std::max(num_sms, 1);
+  long long best = 1;
+  long long best_num = (bh + sms - 1) / sms, best_den = 1;  // cost = num / den
+  for (long long n = 2; n <= nmax; ++n) {
+    const long long num = (bh * n + sms - 1) / sms;
+    if (num * best_den < best_num * n) {
+      best = n;
+      best_num = num;
+      best_den = n;
+    }
+  }
+  const long long range = TT * ((nst + best - 1) / best);
+  *blocks_y = T > 0 ? ((long long)T + range - 1) / range : 1;
+  return (int)range;
 }
 
 size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms) {
   const long long bh = (long long)B * H;
   if (bh == 0) return 0;
   const long long TT = (long long)(kConvThreads / (D / 4)) * kConvRows;
-  const long long nst = std::max(1LL, ((long long)T + TT - 1) / TT);
-  const long long nsplit = conv_bwd_splits(bh, T, TT, num_sms);
-  const long long range = TT * ((nst + nsplit - 1) / nsplit);
-  const long long blocks_y = T > 0 ? ((long long)T + range - 1) / range : 1;
+  long long blocks_y = 0;
+  conv_range(bh, T, TT, num_sms, &blocks_y);
   return (size_t)H * B * blocks_y * D * (W + 1) * sizeof(float);
 }
 

@@ -116,12 +116,10 @@ struct ConvArgs {
   int chunks_per_block;  // token groups (of four or eight) per stage; set by the launchers
   int range;             // tokens per block; set by the launchers
 };
-// Both launchers choose their geometry (shared-memory stages, tokens per
-// block) from the kernel's occupancy on `num_sms` SMs. The backward's
-// per-block partial sums of the tap and bias gradients need
-// conv_partial_bytes() of workspace in `part` (an upper bound over the
-// geometries the launcher can choose).
-long long conv_bwd_splits(long long bh, int T, long long TT, int num_sms);
+// Both launchers choose their geometry (tokens per block from conv_range()
+// for `num_sms` SMs). The backward's per-block partial sums of the tap and
+// bias gradients need conv_partial_bytes() of workspace in `part`.
+int conv_range(long long bh, int T, long long TT, int num_sms, long long* blocks_y);
 size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms);
 cudaError_t launch_conv(const ConvArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_conv_backward(const ConvArgs& a, int num_sms, cudaStream_t s);
