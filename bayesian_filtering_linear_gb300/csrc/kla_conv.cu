@@ -53,6 +53,7 @@ constexpr int kConvRows = 4;
 template <typename IO>
 __host__ __device__ constexpr int conv_stages() { return sizeof(IO) == 2 ? 8 : 6; }
 constexpr int kConvBwdStages = 5;
+constexpr int kConvFwdMinStages = 8, kConvBwdMinStages = 32;  // stages per block range at least
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x·log2 e)
 
 // ---- four channels as two packed fp32 pairs (channels 0, 1 and 2, 3) --------
@@ -524,7 +525,7 @@ cudaError_t launch_fwd(ConvArgs a, int num_sms, cudaStream_t s) {
   const cudaError_t e = prepare_kernel<kla_conv_kernel<IO, W, ACT>>(smem_max);
   if (e != cudaSuccess) return e;
   long long blocks_y = 0;
-  a.range = conv_range(bh, a.T, TT, num_sms, &blocks_y);
+  a.range = conv_range(bh, a.T, TT, num_sms, kConvFwdMinStages, &blocks_y);
   fn<<<dim3((unsigned)bh, (unsigned)blocks_y), kConvThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -541,7 +542,7 @@ cudaError_t launch_bwd(ConvArgs a, int num_sms, cudaStream_t s) {
   cudaError_t e = prepare_kernel<kla_conv_bwd_kernel<IO, W, ACT>>(smem_max);
   if (e != cudaSuccess) return e;
   long long blocks_y = 0;
-  a.range = conv_range(bh, a.T, TT, num_sms, &blocks_y);  // the rule conv_partial_bytes() sizes for
+  a.range = conv_range(bh, a.T, TT, num_sms, kConvBwdMinStages, &blocks_y);  // as conv_partial_bytes()
   a.nparts = a.part ? (long long)a.B * blocks_y : 0;
   fn<<<dim3((unsigned)bh, (unsigned)blocks_y), kConvThreads, smem, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -581,18 +582,20 @@ cudaError_t launch_io(const ConvArgs& a, bool backward, int num_sms, cudaStream_
 // time is the total work of the blocks it runs, so each stream is cut into
 // the number n of ranges (of whole stages) that minimises the busiest SM's
 // share, ceil(B·H·n / SMs) / n — for 128 streams on 152 SMs, n = 7 is within
-// 2% of an even spread — with at least eight stages per range so that a
-// block's pipeline fill stays a small part of its work; ties go to the
-// smaller n.
-int conv_range(long long bh, int T, long long TT, int num_sms, long long* blocks_y) {
+// 2% of an even spread — with at least `min_stages` stages per range so that
+// a block's pipeline fill (and, backward, its extra tail stage) stays a small
+// part of its work: 8 forward, 32 backward (measured: at 128 streams of 64
+// stages, 7 ranges per stream made the backward 5% slower than 2). Ties go to
+// the larger n (more blocks resident to hide latency).
+int conv_range(long long bh, int T, long long TT, int num_sms, int min_stages, long long* blocks_y) {
   const long long nst = std::max(1LL, ((long long)T + TT - 1) / TT);
-  const long long nmax = std::min(512LL, std::max(1LL, nst / 8));
+  const long long nmax = std::min(512LL, std::max(1LL, nst / min_stages));
   const long long sms = std::max(num_sms, 1);
   long long best = 1;
   long long best_num = (bh + sms - 1) / sms, best_den = 1;  // cost = num / den
   for (long long n = 2; n <= nmax; ++n) {
     const long long num = (bh * n + sms - 1) / sms;
-    if (num * best_den < best_num * n) {
+    if (num * best_den <= best_num * n) {
       best = n;
       best_num = num;
       best_den = n;
@@ -608,7 +611,7 @@ size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms) {
   if (bh == 0) return 0;
   const long long TT = (long long)(kConvThreads / (D / 4)) * kConvRows;
   long long blocks_y = 0;
-  conv_range(bh, T, TT, num_sms, &blocks_y);
+  conv_range(bh, T, TT, num_sms, kConvBwdMinStages, &blocks_y);
   return (size_t)H * B * blocks_y * D * (W + 1) * sizeof(float);
 }
 

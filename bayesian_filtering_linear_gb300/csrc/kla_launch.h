@@ -119,7 +119,7 @@ struct ConvArgs {
 // Both launchers choose their geometry (tokens per block from conv_range()
 // for `num_sms` SMs). The backward's per-block partial sums of the tap and
 // bias gradients need conv_partial_bytes() of workspace in `part`.
-int conv_range(long long bh, int T, long long TT, int num_sms, long long* blocks_y);
+int conv_range(long long bh, int T, long long TT, int num_sms, int min_stages, long long* blocks_y);
 size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms);
 cudaError_t launch_conv(const ConvArgs& a, int num_sms, cudaStream_t s);
 cudaError_t launch_conv_backward(const ConvArgs& a, int num_sms, cudaStream_t s);
