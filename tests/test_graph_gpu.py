@@ -66,3 +66,43 @@ def test_captured_decode_steps_replay_exactly():
     torch.cuda.synchronize()
     for got, ref in zip(ys + [lam, eta], want):
         assert torch.equal(got, ref)
+
+
+def test_captured_conv_decode_and_backward_replay_exactly():
+    """The block's causal convolution fed one token per call with the window
+    updated in place (a decode loop), then its backward, captured once and
+    replayed: the same bits as the eager calls."""
+    from bayesian_filtering_linear_gb300.inputs import make_conv_inputs
+    B, H, T, D, W = 2, 4, 12, 64, 4
+    p = {k: v.cuda() for k, v in make_conv_inputs(B, H, T, D, W, io="bf16", seed=8).items()}
+    toks = [p["x"][:, :, t:t + 1].contiguous() for t in range(T)]
+    win = p["window"].clone()
+    ys = [torch.empty(B, H, 1, D, dtype=torch.bfloat16, device="cuda") for _ in range(T)]
+    ws = torch.empty(max(16, kla.LIB.kla_conv_backward_workspace_size(B, H, T, D, W)), dtype=torch.uint8,
+                     device="cuda")
+    grads = {}
+
+    def run():
+        for t in range(T):
+            kla.conv(toks[t], p["weight"], p["bias"], win, y=ys[t], update_window=True)
+        grads.update(kla.conv_backward(p["x"], p["weight"], p["bias"], p["window"], gy=p["gy"],
+                                       gwindow_out=p["gwindow_out"], workspace=ws))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()  # warm-up outside the capture (first-launch attributes)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    want = [y.clone() for y in ys] + [win.clone()] + [grads[k].clone() for k in sorted(grads)]
+    win.copy_(p["window"])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for y in ys:
+        y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    got = [y for y in ys] + [win] + [grads[k] for k in sorted(grads)]
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)
