@@ -53,6 +53,18 @@ DESCRIPTIONS = {
     "tiny": "tiny B1 H1 T256 dk16 dv16 fp32 I/O",
     "decode": "decode kla_step B256 H16 dk64 dv64 fp32, state from a 1024-token kla_forward prefix",
 }
+CONV_NAMES = {"conv": "causal convolution + SiLU", "conv_backward": "backward of the causal convolution"}
+
+
+def metric_for(wname: str, pass_: str) -> str:
+    """The metric string of a workload and pass (the same for both arms)."""
+    if pass_ == "backward":
+        return METRICS[wname].replace("KLA scan tokens/s", "KLA backward tokens/s")
+    if pass_ in CONV_NAMES:
+        return METRICS[wname].replace("KLA scan tokens/s", f"KLA block {CONV_NAMES[pass_]} of q, k, v: tokens/s")
+    return METRICS[wname]
+
+
 # Algorithmic flops per element-step of the printed recursion (FMA = 2, each
 # reciprocal or division = 1): c = k²Λ^v (1), a² + p̄λ (2), its reciprocal (1),
 # λr + c (2), a·r (1), kΛ^v v (1), fη + b (2), η/λ (1), y += qμ (2).
@@ -254,8 +266,28 @@ def run_reference(args, world, rank):
     x = make_inputs(1, heads, tokens, w.dk, w.dv, io=w.io, seed=w.seed, a_logit_mean=w.a_logit_mean,
                     random_state=wname == "decode")
     oracle.build()
-    run = lambda: oracle.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
-                                 nthreads=nthreads, want_scales=False)
+    kind = "fp64 C++ oracle"
+    if args.pass_ == "backward":
+        import numpy as np
+        gy = np.random.default_rng(0).standard_normal((1, heads, tokens, w.dv)).astype(np.float32)
+        run = lambda: oracle.backward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"], gy,
+                                      nthreads=nthreads, want_scales=False)
+        kind = "fp64 C++ reverse-mode oracle"
+    elif args.pass_ in CONV_NAMES:
+        from bayesian_filtering_linear_gb300.inputs import make_conv_inputs
+        from oracle import conv as C
+        streams = [{k: v.double().numpy() for k, v in make_conv_inputs(1, heads, tokens, d, CONV_TAPS, io=w.io,
+                                                                         seed=i).items()}
+                   for i, d in enumerate((w.dk, w.dk, w.dv))]
+        if args.pass_ == "conv":
+            run = lambda: [C.conv(p["x"], p["weight"], p["bias"]) for p in streams]
+        else:
+            run = lambda: [C.conv_backward(p["x"], p["weight"], p["bias"], None, p["gy"]) for p in streams]
+        nthreads = 1
+        kind = "fp64 numpy oracle of q, k and v's convolutions"
+    else:
+        run = lambda: oracle.forward(x["q"], x["k"], x["v"], x["lam_v"], x["a"], x["pbar"], x["lam0"], x["eta0"],
+                                     nthreads=nthreads, want_scales=False)
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
@@ -263,9 +295,9 @@ def run_reference(args, world, rank):
         run()
     dt = time.perf_counter() - t0
     value = heads * tokens * args.steps / dt
-    sample = f"each step: {heads} heads x {tokens} tokens of the {wname} recipe, fp64 C++ oracle"
+    sample = f"each step: {heads} heads x {tokens} tokens of the {wname} recipe, {kind}"
     print(json.dumps({
-        "impl": "reference", "metric": METRICS[wname], "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_for(wname, args.pass_), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[wname] + " (sampled)", "B": w.B, "H": w.H, "T": w.T,
@@ -618,7 +650,7 @@ def run_kla_backward(args, world, rank, local, w, x, stream):
     achieved = flops / (per_launch_ms * 1e-3) / 1e12
     cpu_value, cpu_desc = cpu_oracle_backward_sample(w, os.cpu_count() or 1)
     print(json.dumps({
-        "metric": METRICS[w.name].replace("KLA scan tokens/s", "KLA backward tokens/s"), "value": value,
+        "metric": metric_for(w.name, "backward"), "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
@@ -640,7 +672,7 @@ def run_kla_backward(args, world, rank, local, w, x, stream):
     }), flush=True)
 
 
-CONV_TAPS = 4  # kernel width of the block's causal convolution (the pages give none; 4 as in Mamba-style blocks)
+CONV_TAPS = 4  # width of the block's causal convolution (the KLA summary gives none; 4 as in Mamba-style blocks)
 
 
 def run_conv(args, world, rank, local, w, stream, backward: bool):
@@ -726,9 +758,9 @@ def run_conv(args, world, rank, local, w, stream, backward: bool):
     peak_gbs = float(peaks.get("hbm_gbs", 6800.0))
     achieved = alg_bytes / (per_launch_ms * 1e-3) / 1e9
     cpu_value, cpu_desc = cpu_oracle_conv_sample(w, W, backward)
-    name = "backward of the causal convolution" if backward else "causal convolution + SiLU"
+    name = CONV_NAMES["conv_backward" if backward else "conv"]
     print(json.dumps({
-        "metric": METRICS[w.name].replace("KLA scan tokens/s", f"KLA block {name} of q, k, v: tokens/s"),
+        "metric": metric_for(w.name, "conv_backward" if backward else "conv"),
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "io_dtype": w.io, "data": "synthetic",
