@@ -245,3 +245,48 @@ def test_conv_then_scan_layer_prologue():
                            f64(inp["pbar"]), f64(inp["lam0"]), f64(inp["eta0"]), want_scales=True)
     err = np.max(np.abs(f64(y) - ref["y"]) / (np.abs(ref["y"]) + ref["y_scale"] + 1e-30))
     assert err <= 1e-4
+
+
+def test_block_backward_chains_scan_and_convolutions():
+    """Training a KLA block end to end: q, k, v come from their own causal
+    convolutions with SiLU, the scan runs on them, and the gradients flow
+    back through kla_backward (dL/dq, dL/dk, dL/dv) into each convolution's
+    kla_conv_backward (dL/dx, taps, bias). The same chain in the oracle: the
+    fp64 convolutions, the fp64 scan's reverse mode, the fp64 convolution
+    backward. Error relative to the largest reference value of each gradient
+    (1e-4: fp32 arithmetic through two recursions and two W-term sums)."""
+    import oracle
+    from bayesian_filtering_linear_gb300.inputs import make_inputs
+    B, H, T, dk, dv, W = 1, 2, 96, 16, 16, 4
+    inp = {k: v.to(DEV) for k, v in make_inputs(B, H, T, dk, dv, io="f32", seed=12, random_state=True).items()}
+    conv_in = {n: on_device(make_conv_inputs(B, H, T, dk if n != "v" else dv, W, io="f32", seed=60 + i))
+               for i, n in enumerate(("q", "k", "v"))}
+    for n in ("q", "k", "v"):  # keep q, k in the scale of the scan's recipe
+        conv_in[n]["weight"] *= 0.5
+    mixed = dict(inp)
+    for n in ("q", "k", "v"):
+        mixed[n], _ = kla.conv(conv_in[n]["x"], conv_in[n]["weight"], conv_in[n]["bias"], conv_in[n]["window"])
+    g = torch.Generator().manual_seed(3)
+    gy = torch.randn(B, H, T, dv, generator=g).to(DEV)
+    gl, ge = torch.randn(B, H, dk, dv, generator=g).to(DEV), torch.randn(B, H, dk, dv, generator=g).to(DEV)
+    sg = kla.backward(mixed["q"], mixed["k"], mixed["v"], inp["lam_v"], inp["a"], inp["pbar"], inp["lam0"],
+                      inp["eta0"], gy=gy, glamT=gl, getaT=ge)
+    cg = {n: kla.conv_backward(conv_in[n]["x"], conv_in[n]["weight"], conv_in[n]["bias"], conv_in[n]["window"],
+                               gy=sg["g" + n]) for n in ("q", "k", "v")}
+    torch.cuda.synchronize()
+
+    ref_in = {n: C.conv(f64(conv_in[n]["x"]), f64(conv_in[n]["weight"]), f64(conv_in[n]["bias"]),
+                        f64(conv_in[n]["window"]))[0] for n in ("q", "k", "v")}
+    rs = oracle.backward64(ref_in["q"], ref_in["k"], ref_in["v"], f64(inp["lam_v"]), f64(inp["a"]), f64(inp["pbar"]),
+                           f64(inp["lam0"]), f64(inp["eta0"]), f64(gy), f64(gl), f64(ge))
+    for n in ("q", "k", "v"):
+        rc = C.conv_backward(f64(conv_in[n]["x"]), f64(conv_in[n]["weight"]), f64(conv_in[n]["bias"]),
+                             f64(conv_in[n]["window"]), rs["d" + n])
+        for name in ("gx", "gweight", "gbias", "gwindow"):
+            ref = rc[name]
+            err = np.max(np.abs(f64(cg[n][name]) - ref)) / np.max(np.abs(ref))
+            assert err <= 1e-4, (n, name, err)
+    # the scan's own gradients of the other inputs, for completeness
+    for name, key in (("glam_v", "dlam_v"), ("ga", "da"), ("gpbar", "dpbar"), ("glam0", "dlam0")):
+        err = np.max(np.abs(f64(sg[name]) - rs[key])) / np.max(np.abs(rs[key]))
+        assert err <= 1e-4, (name, err)
