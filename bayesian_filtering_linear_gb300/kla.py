@@ -466,3 +466,59 @@ def conv_backward(x, weight, bias=None, window=None, *, gy=None, gwindow_out=Non
                                    _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "kla_conv_backward")
     return out
+
+
+# ---- autograd: the entry points as differentiable torch operations ------------
+
+class _ScanFunction(torch.autograd.Function):
+    """kla_forward with kla_backward as its derivative."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, lam_v, a, pbar, lam0, eta0, gates):
+        y, lamT, etaT = forward(q, k, v, lam_v, a, pbar, lam0, eta0, gates=gates)
+        ctx.save_for_backward(q, k, v, lam_v, a, pbar, lam0, eta0)
+        ctx.gates = gates
+        return y, lamT, etaT
+
+    @staticmethod
+    def backward(ctx, gy, glamT, getaT):
+        q, k, v, lam_v, a, pbar, lam0, eta0 = ctx.saved_tensors
+        g = backward(q, k, v, lam_v, a, pbar, lam0, eta0,
+                     gy=None if gy is None else gy.to(q.dtype).contiguous(),
+                     glamT=None if glamT is None else glamT.contiguous(),
+                     getaT=None if getaT is None else getaT.contiguous(),
+                     state_grads=lam0 is not None, gates=ctx.gates)
+        return (g["gq"], g["gk"], g["gv"], g["glam_v"], g["ga"], g["gpbar"], g.get("glam0"), g.get("geta0"), None)
+
+
+def scan(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, gates: int = 0):
+    """Differentiable KLA scan (autograd): returns ``(y, lamT, etaT)`` like
+    :func:`forward`; gradients come from kla_backward."""
+    return _ScanFunction.apply(q, k, v, lam_v, a, pbar, lam0, eta0, int(gates))
+
+
+class _ConvFunction(torch.autograd.Function):
+    """kla_conv with kla_conv_backward as its derivative."""
+
+    @staticmethod
+    def forward(ctx, x, weight, bias, window, activation):
+        y, wout = conv(x, weight, bias, window, activation=activation)
+        ctx.save_for_backward(x, weight, bias, window)
+        ctx.activation = activation
+        return y, wout
+
+    @staticmethod
+    def backward(ctx, gy, gwindow_out):
+        x, weight, bias, window = ctx.saved_tensors
+        g = conv_backward(x, weight, bias, window,
+                          gy=None if gy is None else gy.to(x.dtype).contiguous(),
+                          gwindow_out=None if gwindow_out is None else gwindow_out.to(x.dtype).contiguous(),
+                          activation=ctx.activation, window_grad=window is not None)
+        return (g["gx"], g["gweight"], None if bias is None else g["gbias"], g.get("gwindow"), None)
+
+
+def causal_conv(x, weight, bias=None, window=None, *, activation: int = ACT_SILU):
+    """Differentiable causal convolution with SiLU (autograd): returns
+    ``(y, window_out)`` like :func:`conv`; gradients come from
+    kla_conv_backward."""
+    return _ConvFunction.apply(x, weight, bias, window, int(activation))
