@@ -98,6 +98,9 @@ CASES = [  # B, H, T, D, W
     (3, 2, 5000, 16, 4),  # several blocks along T: batch and block partials
     (1, 2, 2, 16, 6),     # T < W − 1: the window out keeps part of the window in
     (2, 2, 0, 16, 4),     # T = 0: the window is copied
+    (2, 2, 77, 64, 3),    # the compile-time widths of 64 and 128 channels
+    (1, 2, 45, 128, 8),
+    (1, 1, 2, 64, 6),
 ]
 
 
