@@ -1,8 +1,8 @@
 // Causal depthwise 1-D convolution with SiLU: launch geometry, the
 // partial-sum workspace and the dispatch over row widths. The kernels are in
 // kla_conv_kernels.cuh (the operation and its work layout are described
-// there); this unit compiles the any-width kernels, kla_conv_d64.cu and
-// kla_conv_d128.cu the fixed-width ones.
+// there); this unit compiles the any-width kernels, kla_conv_d{16,32,64,128}.cu
+// the fixed-width ones for the scan's head sizes.
 #include "kla_conv_kernels.cuh"
 
 namespace kla {
@@ -45,12 +45,16 @@ size_t conv_partial_bytes(int B, int H, int T, int D, int W, int num_sms) {
 }
 
 template cudaError_t conv_launch_dc<0>(const ConvArgs&, bool, int, cudaStream_t);
+extern template cudaError_t conv_launch_dc<16>(const ConvArgs&, bool, int, cudaStream_t);
+extern template cudaError_t conv_launch_dc<32>(const ConvArgs&, bool, int, cudaStream_t);
 extern template cudaError_t conv_launch_dc<64>(const ConvArgs&, bool, int, cudaStream_t);
 extern template cudaError_t conv_launch_dc<128>(const ConvArgs&, bool, int, cudaStream_t);
 
 namespace {
 cudaError_t conv_dispatch(const ConvArgs& a, bool backward, int num_sms, cudaStream_t s) {
   switch (a.D) {
+    case 16: return conv_launch_dc<16>(a, backward, num_sms, s);
+    case 32: return conv_launch_dc<32>(a, backward, num_sms, s);
     case 64: return conv_launch_dc<64>(a, backward, num_sms, s);
     case 128: return conv_launch_dc<128>(a, backward, num_sms, s);
     default: return conv_launch_dc<0>(a, backward, num_sms, s);

@@ -101,6 +101,8 @@ CASES = [  # B, H, T, D, W
     (2, 2, 77, 64, 3),    # the compile-time widths of 64 and 128 channels
     (1, 2, 45, 128, 8),
     (1, 1, 2, 64, 6),
+    (2, 3, 150, 32, 5),   # the compile-time widths of 16 and 32 channels
+    (3, 1, 61, 16, 2),
 ]
 
 
