@@ -474,7 +474,8 @@ def run_kla(args, world, rank, local):
     sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     peak_tflops = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12
-    flops = FLOPS_PER_ELEMENT_STEP * tokens * w.dk * w.dv
+    element_steps = tokens * w.dk * w.dv
+    flops = FLOPS_PER_ELEMENT_STEP * element_steps
     achieved = flops / (per_launch_ms * 1e-3) / 1e12
     traffic = None
     try:
@@ -504,6 +505,13 @@ def run_kla(args, world, rank, local):
                      "kernel_ms": per_launch_ms,
                      "peak_basis": f"{nsm} SMs x 128 fp32 lanes x 2 flop x {sm_mhz:.0f} MHz (max SM clock)",
                      "flops_per_launch": flops},
+        # The hardware-honest bound of the element-step: max(FP32 lane-ops / 128,
+        # MUFU ops / 16) SM-clocks; 9 lane-ops and 1 reciprocal per element-step
+        # make the MUFU term the larger, 16 element-steps per SM-clock.
+        "hw_bound": {"unit": "element-steps/s", "achieved": element_steps / (per_launch_ms * 1e-3),
+                     "peak": 16 * nsm * sm_mhz * 1e6,
+                     "frac": element_steps / (per_launch_ms * 1e-3) / (16 * nsm * sm_mhz * 1e6),
+                     "basis": "max(9 FP32 lane-ops / 128, 1 MUFU reciprocal / 16) SM-clocks per element-step"},
         "cpu_baseline": {"value": cpu_value, "unit": "tokens/s", **cpu_desc},
         "e2e": {"value": tokens * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": E2E_OVERLAP},
