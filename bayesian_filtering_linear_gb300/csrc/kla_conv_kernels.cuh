@@ -38,6 +38,8 @@
 
 namespace kla {
 
+// Internal linkage on purpose: every translation unit that includes this
+// header compiles only the kernels of the row widths it instantiates.
 namespace {
 
 constexpr int kConvThreads = 256;
