@@ -49,13 +49,13 @@ constexpr int kMaxDevices = 256;
 // rows that the next stage reads before its start.
 constexpr int kConvRows = 4;
 // Shared-memory stages (a stage is TT·D ≈ 4096 elements; stages − 2 are in
-// flight while one is computed). The kernels are bound by the bytes in
-// flight per SM — HBM latency under load is microseconds — so the rings are
-// as deep as two or three blocks per SM allow: forward 64 KB (bf16) or 96 KB
-// (fp32) per block, backward (x and gy rings plus 32 KB of gu) 112 KB (bf16)
-// or 192 KB (fp32).
+// flight while one is computed). Forward: six, 48 KB (bf16) or 96 KB (fp32)
+// per block — in bf16 that leaves four blocks per SM, which measured faster
+// than eight stages at three blocks (27.3 against 28.9 µs per 64-channel
+// headline stream) or ten at two (32.7 µs). Backward: five stages of x and
+// gy plus 32 KB of gu, 112 KB (bf16) or 192 KB (fp32).
 template <typename IO>
-__host__ __device__ constexpr int conv_stages() { return sizeof(IO) == 2 ? 8 : 6; }
+__host__ __device__ constexpr int conv_stages() { return 6; }
 constexpr int kConvBwdStages = 5;
 constexpr int kConvFwdMinStages = 8, kConvBwdMinStages = 32;  // stages per block range at least
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x·log2 e)
