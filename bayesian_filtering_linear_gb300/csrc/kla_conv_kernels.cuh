@@ -19,8 +19,8 @@
 // it through shared-memory stages with cp.async; a thread computes four
 // consecutive tokens × four channels of a stage, the channels as two packed
 // fp32 pairs (fma/mul/add.rn.f32x2), with the exponential and reciprocal of
-// SiLU on the MUFU unit. Both kernels stream from HBM: the bound is the bytes
-// of x, y (and gy, gx).
+// SiLU on the MUFU unit. Their roofline is HBM — the bytes of x and y (and
+// gy, gx) — and they run below it limited by instruction issue.
 //
 // The backward's sums over (b, t) are deterministic: each thread sums its own
 // chunk in token order, a block sums its threads in chunk order through
@@ -51,8 +51,8 @@ constexpr int kConvRows = 4;
 // Shared-memory stages (a stage is TT·D ≈ 4096 elements; stages − 2 are in
 // flight while one is computed). Forward: six, 48 KB (bf16) or 96 KB (fp32)
 // per block — in bf16 that leaves four blocks per SM, which measured faster
-// than eight stages at three blocks (27.3 against 28.9 µs per 64-channel
-// headline stream) or ten at two (32.7 µs). Backward: five stages of x and
+// than eight stages at three blocks (27.3 against 28.9 µs for a B8 H16 T4096
+// stream of 64 bf16 channels) or ten at two (32.7 µs). Backward: five stages of x and
 // gy plus 32 KB of gu, 112 KB (bf16) or 192 KB (fp32).
 template <typename IO>
 __host__ __device__ constexpr int conv_stages() { return 6; }
