@@ -42,9 +42,10 @@
  *    queued and no CUDA call has been made. An asynchronous fault of an
  *    earlier kernel is reported by a later call as KLA_ERR_CUDA.
  *  - Domain (the caller's contract): 0 < a ≤ 1, p̄ ≥ 0, Λ^v ≥ 0, λ0 > 0. The
- *    kernels raise a below 2^-40 to 2^-40 and add 2^-40 to k², which changes
- *    results only below fp32 resolution for |k| ≥ 2^-8; other violations
- *    give NaN/Inf and never a trap.
+ *    kernels raise a below 2^-40 to 2^-40 (a NaN a included) and add 2^-40 to
+ *    k², which changes results only below fp32 resolution for |k| ≥ 2^-8;
+ *    other violations give NaN/Inf in the elements they reach and never a
+ *    trap.
  *  - Entry points are thread-safe; calls on one stream are ordered (for
  *    kla_forward_chunked_noalloc, see its comment on overlapping calls).
  */

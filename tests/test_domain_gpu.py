@@ -6,7 +6,9 @@ only column j ("Technische Samenvatting: Kalman Linear Attention (KLA)",
 Belangrijkste Bijdragen 1: the diagonal structure), so:
 
 * a NaN value v[t, j] reaches only η and y of column j from token t on;
-* a NaN decay a[t, i] reaches row i's λ and η, hence every y_j from t on;
+* a NaN process noise p̄[t, i] reaches row i's λ and η, hence every y_j from
+  t on (a NaN decay a does not: the kernels' floor max(a, 2^-40) takes it to
+  2^-40, as IEEE max returns its non-NaN operand);
 * other heads, and everything before t, are bit for bit the clean run's.
 """
 import math
@@ -45,11 +47,11 @@ def test_nan_value_stays_in_its_column(strategy):
 
 
 @pytest.mark.parametrize("strategy", ["sequential", "chunked"])
-def test_nan_decay_stays_in_its_row(strategy):
+def test_nan_process_noise_stays_in_its_row(strategy):
     x = {n: t.to(DEV) for n, t in make_inputs(1, 2, 96, 16, 16, io="f32", seed=32, random_state=True).items()}
     y0, l0, e0 = run(x, strategy)
-    bad = dict(x, a=x["a"].clone())
-    bad["a"][0, 0, 20, 2] = math.nan
+    bad = dict(x, pbar=x["pbar"].clone())
+    bad["pbar"][0, 0, 20, 2] = math.nan
     y, l, e = run(bad, strategy)
     torch.cuda.synchronize()
     assert torch.equal(y[0, 1], y0[0, 1]) and torch.equal(l[0, 1], l0[0, 1])
