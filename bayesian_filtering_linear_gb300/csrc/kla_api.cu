@@ -48,6 +48,7 @@ kla_status check_options(const kla_options* opt, int dk) {
   if (!valid_gates(opt->gates)) return KLA_ERR_INVALID_ARG;
   if (opt->strategy < KLA_AUTO || opt->strategy > KLA_CHUNKED) return KLA_ERR_INVALID_ARG;
   if (opt->chunk_len < 0 || opt->chunk_len % kChunkAlign != 0) return KLA_ERR_INVALID_ARG;
+  if (opt->coef_pass < KLA_COEF_AUTO || opt->coef_pass > KLA_COEF_ON) return KLA_ERR_INVALID_ARG;
   if (opt->rows_per_lane != 0) {  // must be a geometry the scan kernel is built for
     int rls[2];
     const int nrl = kla::scan_rows_per_lane(dk, rls);
@@ -112,8 +113,16 @@ double pass_cost(long long bh, int dk, int rl, int dv, int io, int cc, int tile,
                              (step_cost + 4.5 / cc) / eff;
 }
 
+// The coefficient pass (kla_coef_pass) under KLA_COEF_AUTO: taken when a
+// head's columns span at least this many blocks (each would build the same
+// per-row coefficients) and its buffer is at most kCoefMaxBytes.
+constexpr int kCoefMinBlocks = 4;
+constexpr size_t kCoefMaxBytes = (size_t)16 << 30;
+
+// allow_coef: the caller can run the coefficient pass (kla_forward's plain
+// readout; not the uncertainty readout or the allocation-free entry point).
 kla_status make_plan(int B, int H, int T, int dk, int dv, int io, const kla_options* opt, int num_sms,
-                     Plan* out) {
+                     Plan* out, bool allow_coef = true) {
   kla_status st = check_shape(B, H, T, dk, dv);
   if (st != KLA_OK) return st;
   if ((st = check_options(opt, dk)) != KLA_OK) return st;
@@ -192,7 +201,14 @@ kla_status make_plan(int B, int H, int T, int dk, int dv, int io, const kla_opti
       p.rows_per_lane = best_c.rl;
     }
   }
-  p.ws_bytes = p.strategy == KLA_CHUNKED ? kla::chunk_workspace_bytes(elems, p.num_chunks) : 0;
+  const int coef = opt ? opt->coef_pass : KLA_COEF_AUTO;
+  if (allow_coef && p.strategy == KLA_SEQUENTIAL && bh > 0 && T > 0 && coef != KLA_COEF_OFF) {
+    const bool split = dv / p.cols_per_block >= kCoefMinBlocks;
+    p.coef_pass = coef == KLA_COEF_ON || (split && kla::coef_workspace_bytes(bh, T, dk) <= kCoefMaxBytes);
+  }
+  p.ws_bytes = p.strategy == KLA_CHUNKED ? kla::chunk_workspace_bytes(elems, p.num_chunks)
+               : p.coef_pass          ? kla::coef_workspace_bytes(bh, T, dk)
+                                      : 0;
   *out = p;
   return KLA_OK;
 }
@@ -244,6 +260,7 @@ void fill_info(const Plan& p, kla_plan_info* out) {
   out->cols_per_block = p.cols_per_block;
   out->workspace_bytes = p.ws_bytes;
   out->rows_per_lane = p.rows_per_lane;
+  out->coef_pass = p.coef_pass;
 }
 
 
@@ -279,7 +296,7 @@ kla_status forward_impl(const void* q, const void* k, const void* v, const void*
   int sms = 0;
   if ((st = device_sms(&sms)) != KLA_OK) return st;
   Plan p{};
-  if ((st = make_plan(B, H, T, dk, dv, io, opt, sms, &p)) != KLA_OK) return st;
+  if ((st = make_plan(B, H, T, dk, dv, io, opt, sms, &p, y_var == nullptr)) != KLA_OK) return st;
   if (p.ws_bytes > 0 && (!workspace || ws_bytes < p.ws_bytes)) return KLA_ERR_WORKSPACE;
   if (workspace && !aligned16(workspace)) return KLA_ERR_MISALIGNED;
 
@@ -302,6 +319,10 @@ kla_status forward_impl(const void* q, const void* k, const void* v, const void*
   const bool var_pass = y_var && !fused;
   if (T == 0) {
     e = kla::launch_init_state(f, s);
+  } else if (p.strategy == KLA_SEQUENTIAL && p.coef_pass) {  // no y_var here (allow_coef above)
+    float* coefs = reinterpret_cast<float*>(workspace);
+    e = kla::launch_coef(f, coefs, s);
+    if (e == cudaSuccess) e = kla::launch_forward(f, p, nullptr, s, nullptr, 0, coefs);
   } else if (p.strategy == KLA_SEQUENTIAL) {
     e = var_pass ? kla::launch_forward(fv, p, nullptr, s, nullptr, 1) : cudaSuccess;
     if (e == cudaSuccess) e = kla::launch_forward(f, p, nullptr, s, nullptr, main_mode);
@@ -545,7 +566,7 @@ kla_status kla_backward(const void* q, const void* k, const void* v, const void*
   if (!aligned16(workspace)) return KLA_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T > 0) {  // forward scan storing its state every 16 tokens (no y)
-    const kla_options seq{KLA_SEQUENTIAL, 0, 0, gates};
+    const kla_options seq{KLA_SEQUENTIAL, 0, 0, gates, KLA_COEF_OFF};
     Plan fp{};
     if ((st = make_plan(B, H, T, dk, dv, io, &seq, sms, &fp)) != KLA_OK) return st;
     kla::ForwardArgs ff{q, k, v, lam_v, a, pbar, lam0, eta0, nullptr, nullptr, nullptr, B, H, T, dk, dv, (int)io,

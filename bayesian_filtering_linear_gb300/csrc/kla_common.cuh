@@ -72,6 +72,8 @@ struct KernelParams {
   float *lamT, *etaT;
   float* ckpt;          // scan MODE 3 only: [T/16 + 1][2][elems] scaled states (P̃, μ)
                         // at every 16-token tile start and at the end
+  const float* coefs;   // scan MODE 4 only: per-row coefficients [B·H][T][5][d_k] of the
+                        // coefficient pass (A, B, 1/a, k/K, q per token and row)
   int T, dv, chunk_len, cc, log2cc;
   int gates;        // kla_gate bits
   long long elems;  // B·H·dk·dv
@@ -88,21 +90,12 @@ struct RawTile {
 };
 
 // Queue 16-byte asynchronous copies of tokens [t0, t0 + tl) of this block's
-// inputs into the raw tile at `dst`.
+// per-column inputs (v, Λ^v) into the raw tile at `dst`.
 // (tid, nthr): this thread's index among the nthr threads sharing the work.
 template <typename IO, int DK, int TC>
-__device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* dst, long long bh, int jb, int t0,
-                                          int tl, int tid, int nthr) {
+__device__ __forceinline__ void stage_cols(const KernelParams& p, unsigned char* dst, long long bh, int jb, int t0,
+                                           int tl, int tid, int nthr) {
   using R = RawTile<IO, DK, TC>;
-  const size_t row_i = (size_t)DK * sizeof(IO);
-  const int chunks_i = (int)(tl * row_i / 16);
-  const size_t base_i = ((size_t)bh * p.T + t0) * row_i;
-#pragma unroll
-  for (int arr = 0; arr < 4; ++arr) {
-    const char* src = (const char*)(arr == 0 ? p.q : arr == 1 ? p.k : arr == 2 ? p.a : p.pbar) + base_i;
-    unsigned char* d = dst + arr * R::row_bytes();
-    for (int c = tid; c < chunks_i; c += nthr) cp_async16(d + (size_t)c * 16, src + (size_t)c * 16);
-  }
   // 16-byte chunks per staged row: cc·sizeof(IO)/16, a power of two (cc is)
   const int lcpr = p.log2cc + (sizeof(IO) == 4 ? 2 : 1) - 4;
   const int chunks_j = tl << lcpr;
@@ -117,6 +110,24 @@ __device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* 
       cp_async16(d + (size_t)c * 16, src + (size_t)row * row_j + (size_t)col * 16);
     }
   }
+}
+
+// The same for all of the tile's inputs: the per-row arrays q, k, a, p̄, then
+// the per-column ones.
+template <typename IO, int DK, int TC>
+__device__ __forceinline__ void stage_raw(const KernelParams& p, unsigned char* dst, long long bh, int jb, int t0,
+                                          int tl, int tid, int nthr) {
+  using R = RawTile<IO, DK, TC>;
+  const size_t row_i = (size_t)DK * sizeof(IO);
+  const int chunks_i = (int)(tl * row_i / 16);
+  const size_t base_i = ((size_t)bh * p.T + t0) * row_i;
+#pragma unroll
+  for (int arr = 0; arr < 4; ++arr) {
+    const char* src = (const char*)(arr == 0 ? p.q : arr == 1 ? p.k : arr == 2 ? p.a : p.pbar) + base_i;
+    unsigned char* d = dst + arr * R::row_bytes();
+    for (int c = tid; c < chunks_i; c += nthr) cp_async16(d + (size_t)c * 16, src + (size_t)c * 16);
+  }
+  stage_cols<IO, DK, TC>(p, dst, bh, jb, t0, tl, tid, nthr);
 }
 
 // Four consecutive I/O values from shared memory, widened to fp32.

@@ -28,6 +28,7 @@ struct Plan {
   int cols_per_block;  // CC: d_v columns per thread block
   int rows_per_lane;   // RL: d_k rows held by one lane of the scan kernel
   int tile;            // TC: tokens staged per shared-memory tile
+  int coef_pass;       // 1: the sequential plan reads per-row coefficients from the coefficient pass
   size_t ws_bytes;
 };
 
@@ -54,7 +55,11 @@ size_t chunk_workspace_bytes(long long elems, int num_chunks);
 // sequential plan only) the scan runs without a readout and stores the
 // backward's checkpoints there instead (mode is then ignored).
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s,
-                           float* ckpt = nullptr, int mode = 0);
+                           float* ckpt = nullptr, int mode = 0, const float* coefs = nullptr);
+// The coefficient pass: per-row coefficients of every token into `coefs`
+// ([B·H][T][5][d_k] fp32, coef_workspace_bytes), read by the scan in mode 4.
+cudaError_t launch_coef(const ForwardArgs& f, float* coefs, cudaStream_t s);
+size_t coef_workspace_bytes(long long bh, int T, int dk);
 // The scan stores its checkpoints every kScanTile tokens.
 constexpr int kScanTile = 16;
 cudaError_t launch_compose(const ForwardArgs& f, const Plan& p, float* maps, cudaStream_t s);

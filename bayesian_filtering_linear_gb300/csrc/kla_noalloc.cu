@@ -93,7 +93,9 @@ kla_status kla_forward_chunked_noalloc(const void* q, const void* k, const void*
                                        const void* a, const void* pbar, const float* lam0, const float* eta0,
                                        void* y, float* lamT, float* etaT, int B, int H, int T, int dk, int dv,
                                        kla_dtype io, int chunk_len, void* stream) {
-  const kla_options opt{KLA_CHUNKED, chunk_len};
+  // no coefficient pass: a short sequence falls back to the sequential plan,
+  // which must then need no workspace either
+  const kla_options opt{KLA_CHUNKED, chunk_len, 0, 0, KLA_COEF_OFF};
   // Shape and option checks first, without any CUDA call.
   kla_plan_info info{};
   kla_status st = kla_plan_for_sms(B, H, T, dk, dv, io, &opt, 1, &info);

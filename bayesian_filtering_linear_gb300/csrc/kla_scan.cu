@@ -57,6 +57,7 @@ cudaError_t scan_dispatch(int io, int dk, int rl, int mode, dim3 grid, int threa
     case 0: return scan_launch_y(io, dk, rl, grid, threads, smem, s, kp);
     case 1: return scan_launch_var(io, dk, rl, grid, threads, smem, s, kp);
     case 2: return scan_launch_y_var(io, dk, rl, grid, threads, smem, s, kp);
+    case 4: return scan_launch_y_pre(io, dk, rl, grid, threads, smem, s, kp);
     default: return scan_launch_state(io, dk, rl, grid, threads, smem, s, kp);
   }
 }
@@ -69,11 +70,13 @@ size_t forward_smem_bytes(int dk, int rl, int io, int cc, int /*tile*/, int mode
 static_assert(kTile == kScanTile, "checkpoints are taken once per tile");
 
 cudaError_t launch_forward(const ForwardArgs& f, const Plan& p, const float* starts, cudaStream_t s, float* ckpt,
-                           int mode) {
+                           int mode, const float* coefs) {
   KernelParams kp = make_params(f, p);
   kp.starts = starts;
   kp.ckpt = ckpt;
+  kp.coefs = coefs;
   if (ckpt) mode = 3;
+  if (coefs) mode = 4;  // y with the coefficient pass's output (one chunk)
   const dim3 grid((unsigned)((long long)f.B * f.H), (unsigned)(f.dv / p.cols_per_block), (unsigned)p.num_chunks);
   const int threads = 32 * (p.cols_per_block / warp_cols(f.dk, p.rows_per_lane) + kProducerWarps);
   const size_t smem = forward_smem_bytes(f.dk, p.rows_per_lane, f.io, p.cols_per_block, p.tile, mode);

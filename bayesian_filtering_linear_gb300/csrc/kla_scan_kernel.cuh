@@ -91,6 +91,30 @@ struct ScanLayout {
   __host__ __device__ size_t total() const { return kprev(2); }
 };
 
+// Per-row coefficients of one token for four consecutive rows, from the
+// row's inputs k, a, p̄ (pre-activations when GATED) and K of the token
+// before (1 at a chunk start): A = K_t a/K_{t-1}, B = K_t p̄/a, 1/a, k/K_t,
+// K_t, and 1/K_t. The producers and the coefficient pass both call this, so
+// the two paths give bit-identical coefficients.
+template <bool GATED>
+__device__ __forceinline__ void row_coef4(const float (&kv)[4], const float (&av)[4], const float (&pv)[4],
+                                          const float (&kpv)[4], int gates, float (&A)[4], float (&B)[4],
+                                          float (&AI)[4], float (&KI)[4], float (&Kt)[4], float (&rKo)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float at = fmaxf(GATED ? gate_a(av[u], gates) : av[u], kAMin);
+    const float pbu = GATED ? gate_pbar(pv[u], av[u], gates) : pv[u];
+    Kt[u] = fmaf(kv[u], kv[u], kK2Floor);
+    const float aK = at * Kt[u];
+    const float r = rcp_approx(aK * kpv[u]);  // 1 / (a K_t K_{t-1})
+    AI[u] = (Kt[u] * kpv[u]) * r;             // 1/a
+    A[u] = aK * (aK * r);                     // K_t a / K_{t-1}
+    B[u] = (Kt[u] * pbu) * AI[u];             // K_t p̄ / a
+    rKo[u] = at * kpv[u] * r;                 // 1 / K_t
+    KI[u] = kv[u] * rKo[u];                   // k / K_t
+  }
+}
+
 // Per-(t, i) row coefficients of a staged tile, four rows per thread:
 // coef[t][0..4][i] = (A, B, 1/a, k/K, q); MODE 1 (variance readout only) has
 // q²/K in place of q, MODE 2 (both readouts) adds q²/K as coef[t][5][i].
@@ -119,21 +143,10 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
     const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
     const float pv[4] = {p4.x, p4.y, p4.z, p4.w}, kpv[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
     const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
-    float A[4], B[4], AI[4], KI[4], Kt[4], QV[4];
+    float A[4], B[4], AI[4], KI[4], Kt[4], rK[4], QV[4];
+    row_coef4<GATED>(kv, av, pv, kpv, gates, A, B, AI, KI, Kt, rK);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float at = fmaxf(GATED ? gate_a(av[u], gates) : av[u], kAMin);
-      const float pbu = GATED ? gate_pbar(pv[u], av[u], gates) : pv[u];
-      Kt[u] = fmaf(kv[u], kv[u], kK2Floor);
-      const float aK = at * Kt[u];
-      const float r = rcp_approx(aK * kpv[u]);  // 1 / (a K_t K_{t-1})
-      AI[u] = (Kt[u] * kpv[u]) * r;             // 1/a
-      A[u] = aK * (aK * r);                     // K_t a / K_{t-1}
-      B[u] = (Kt[u] * pbu) * AI[u];             // K_t p̄ / a
-      const float rK = at * kpv[u] * r;         // 1 / K_t
-      KI[u] = kv[u] * rK;                       // k / K_t
-      QV[u] = qv[u] * qv[u] * rK;               // q²/K_t (variance readout)
-    }
+    for (int u = 0; u < 4; ++u) QV[u] = qv[u] * qv[u] * rK[u];  // q²/K_t (variance readout)
     constexpr int NC = MODE == 2 ? 6 : 5;
     float* ct = coef + t * NC * DK + i;
     *reinterpret_cast<float4*>(ct + 0 * DK) = make_float4(A[0], A[1], A[2], A[3]);
@@ -146,6 +159,49 @@ __device__ __forceinline__ void row_coefficients(const unsigned char* raw, float
       *reinterpret_cast<float4*>(ct + 4 * DK) = q4;
     if (MODE == 2) *reinterpret_cast<float4*>(ct + 5 * DK) = make_float4(QV[0], QV[1], QV[2], QV[3]);
     if (t == tl - 1) *reinterpret_cast<float4*>(kp_nxt + i) = make_float4(Kt[0], Kt[1], Kt[2], Kt[3]);
+  }
+}
+
+// The coefficient pass (scan MODE 4 reads its output): the per-row
+// coefficients (A, B, 1/a, k/K, q) of every token of every head into
+// coefs[B·H][T][5][d_k], each (t, i) once, however many column blocks of the
+// head read them afterwards. K of the token before is 1 at t = 0. A block
+// covers kCoefTokens tokens of one head (grid.x) for heads blockIdx.y,
+// blockIdx.y + gridDim.y, ...; a thread handles four consecutive rows of a
+// token, so loads and stores are 16-byte (fp32) or 8-byte (bf16) per thread
+// and consecutive threads touch consecutive addresses.
+constexpr int kCoefTokens = 64;
+template <typename IO, int DK, bool GATED>
+__global__ void __launch_bounds__(256) kla_coef_kernel(const KernelParams p, float* coefs, long long bh_count) {
+  constexpr int R4 = DK / 4;
+  const int t0 = blockIdx.x * kCoefTokens;
+  const int tl = min(kCoefTokens, p.T - t0);
+  for (long long bh = blockIdx.y; bh < bh_count; bh += gridDim.y) {
+    const size_t row0 = (size_t)bh * p.T;
+    for (int g = threadIdx.x; g < tl * R4; g += blockDim.x) {
+      const int tt = g / R4, i = 4 * (g % R4), t = t0 + tt;
+      const size_t o = (row0 + t) * DK + i;
+      const float4 k4 = load4<IO>(reinterpret_cast<const IO*>(p.k) + o);
+      const float4 a4 = load4<IO>(reinterpret_cast<const IO*>(p.a) + o);
+      const float4 p4 = load4<IO>(reinterpret_cast<const IO*>(p.pbar) + o);
+      const float4 q4 = load4<IO>(reinterpret_cast<const IO*>(p.q) + o);
+      float4 kp4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+      if (t > 0) {
+        const float4 km = load4<IO>(reinterpret_cast<const IO*>(p.k) + o - DK);
+        kp4 = make_float4(fmaf(km.x, km.x, kK2Floor), fmaf(km.y, km.y, kK2Floor), fmaf(km.z, km.z, kK2Floor),
+                          fmaf(km.w, km.w, kK2Floor));
+      }
+      const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, av[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float pv[4] = {p4.x, p4.y, p4.z, p4.w}, kpv[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
+      float A[4], B[4], AI[4], KI[4], Kt[4], rK[4];
+      row_coef4<GATED>(kv, av, pv, kpv, p.gates, A, B, AI, KI, Kt, rK);
+      float* ct = coefs + (row0 + t) * (5 * DK) + i;
+      *reinterpret_cast<float4*>(ct + 0 * DK) = make_float4(A[0], A[1], A[2], A[3]);
+      *reinterpret_cast<float4*>(ct + 1 * DK) = make_float4(B[0], B[1], B[2], B[3]);
+      *reinterpret_cast<float4*>(ct + 2 * DK) = make_float4(AI[0], AI[1], AI[2], AI[3]);
+      *reinterpret_cast<float4*>(ct + 3 * DK) = make_float4(KI[0], KI[1], KI[2], KI[3]);
+      *reinterpret_cast<float4*>(ct + 4 * DK) = q4;
+    }
   }
 }
 
@@ -178,13 +234,16 @@ __device__ __forceinline__ void store_y(const float* ypart, IO* yout, int dv, in
 // MODE 0: y. MODE 1: the variance readout y_var[t, j] = Σ_i q_i² P_t[i, j]
 // instead of y (the mean recursion is skipped; y points at y_var). MODE 2:
 // both, y into p.y and y_var into p.y_var. MODE 3: no readout; the state is
-// stored into p.ckpt for the backward pass.
+// stored into p.ckpt for the backward pass. MODE 4: y, as MODE 0, with the
+// per-row coefficients copied from the coefficient pass's output p.coefs
+// instead of built by the producers (one chunk, the sequential plan).
 template <typename IO, int DK, int RL, int TC, int MODE = 0>
 __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps, 1) kla_scan_kernel(const KernelParams p) {
   using G = Geo<DK, RL>;
   constexpr int NPR = RL / 2;  // row pairs per lane
   constexpr bool VAR = MODE == 1;
   constexpr bool CKPT = MODE == 3;
+  constexpr bool PRE = MODE == 4;
   constexpr int NC = MODE == 2 ? 6 : 5, NOUT = MODE == 2 ? 2 : 1;
   extern __shared__ __align__(16) unsigned char smem[];
   const ScanLayout<IO, DK, TC, G::NP, NC, NOUT> L(p.cc);
@@ -219,6 +278,73 @@ __global__ void __launch_bounds__(kMaxThreads + 32 * kProducerWarps, 1) kla_scan
   if (warp >= ncons) {
     // ================= producer warps =================
     const int ptid = tid - 32 * ncons, pn = 32 * kProducerWarps;
+    if constexpr (PRE) {
+      // The same hand-off with the row coefficients copied, not built: tile
+      // m's coefficients (tl·5·d_k contiguous floats) go straight into
+      // coef[m % 2] once the scan is done with that buffer, while the store
+      // of y of the tile before covers the copy's latency; only the
+      // per-column terms are built here.
+      auto fetch_coef = [&](int m) {
+        const float* src = p.coefs + ((size_t)bh * p.T + t_begin + m * TC) * (5 * DK);
+        float* dst = reinterpret_cast<float*>(smem + L.coef(m & 1));
+        const int chunks = tile_len(m) * (5 * DK / 4);
+        for (int c = ptid; c < chunks; c += pn) cp_async16(dst + 4 * c, src + 4 * c);
+      };
+      auto build_cols = [&](auto gated, int m) {
+        column_terms<IO, DK, TC, decltype(gated)::value>(smem + L.raw(m & 1), reinterpret_cast<float4*>(smem + L.pj(m & 1)),
+                                                         p.cc, tile_len(m), ptid, pn, p.gates);
+      };
+      auto cols = [&](int m) {
+        if (p.gates) build_cols(std::true_type{}, m);
+        else build_cols(std::false_type{}, m);
+      };
+      // K of the chunk's last token, for the final state (read by the scan
+      // warps after the last tile, so after many FULL barriers)
+      if (p.lamT && ntiles > 0) {
+        float* klast = reinterpret_cast<float*>(smem + L.kprev(ntiles & 1));
+        const IO* kl = reinterpret_cast<const IO*>(p.k) + ((size_t)bh * p.T + t_end - 1) * DK;
+        for (int i = ptid; i < DK; i += pn) {
+          const float kv = to_f32<IO>(kl[i]);
+          klast[i] = fmaf(kv, kv, kK2Floor);
+        }
+      }
+      stage_cols<IO, DK, TC>(p, smem + L.raw(0), bh, jb, t_begin, tile_len(0), ptid, pn);
+      fetch_coef(0);
+      cp_async_commit();
+      if (ntiles > 1) {
+        stage_cols<IO, DK, TC>(p, smem + L.raw(1), bh, jb, t_begin + TC, tile_len(1), ptid, pn);
+        fetch_coef(1);
+      }
+      cp_async_commit();
+      cp_async_wait<1>();
+      named_sync(kBarProducers, pn);  // tile 0's columns and coefficients visible to all producers
+      cols(0);
+      named_arrive(kBarFull0, nall);
+      if (ntiles > 1) {
+        cp_async_wait<0>();
+        named_sync(kBarProducers, pn);
+        cols(1);
+        named_arrive(kBarFull0 + 1, nall);
+      }
+      for (int n = 0; n < ntiles; ++n) {
+        const int b = n & 1;
+        if (n + 2 < ntiles) stage_cols<IO, DK, TC>(p, smem + L.raw(b), bh, jb, t_begin + (n + 2) * TC, tile_len(n + 2), ptid, pn);
+        cp_async_commit();
+        named_sync(kBarEmpty0 + b, nall);  // the scan of tile n is done with coef/pj[b] and ypart[b]
+        if (n + 2 < ntiles) fetch_coef(n + 2);
+        cp_async_commit();
+        if (p.y)
+          store_y<IO, G::NP, TC, L.TCP>(reinterpret_cast<const float*>(smem + L.ypart(b)),
+                                        ybase + (size_t)(t_begin + n * TC) * p.dv, p.dv, p.cc, p.log2cc, tile_len(n), ptid, pn);
+        if (n + 2 < ntiles) {
+          cp_async_wait<0>();
+          named_sync(kBarProducers, pn);
+          cols(n + 2);
+          named_arrive(kBarFull0 + b, nall);
+        }
+      }
+      return;
+    }
     float* kp0 = reinterpret_cast<float*>(smem + L.kprev(0));
     for (int i = ptid; i < DK; i += pn) kp0[i] = 1.0f;
     // coefficients of tile m into buffer m % 2; the gate activations are a
@@ -518,6 +644,8 @@ cudaError_t scan_launch_var(int io, int dk, int rl, dim3 grid, int threads, size
 cudaError_t scan_launch_y_var(int io, int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
                               const KernelParams& kp);
 cudaError_t scan_launch_state(int io, int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
+                              const KernelParams& kp);
+cudaError_t scan_launch_y_pre(int io, int dk, int rl, dim3 grid, int threads, size_t smem, cudaStream_t s,
                               const KernelParams& kp);
 
 }  // namespace kla

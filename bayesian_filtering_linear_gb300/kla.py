@@ -31,7 +31,7 @@ EXPORTS = ("kla_plan", "kla_plan_for_sms", "kla_forward_workspace_size", "kla_fo
 
 class Options(ctypes.Structure):
     _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("rows_per_lane", ctypes.c_int),
-                ("gates", ctypes.c_int)]
+                ("gates", ctypes.c_int), ("coef_pass", ctypes.c_int)]
 
 
 class BackwardPlanInfo(ctypes.Structure):
@@ -42,7 +42,7 @@ class BackwardPlanInfo(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [("strategy", ctypes.c_int), ("chunk_len", ctypes.c_int), ("num_chunks", ctypes.c_int),
                 ("cols_per_block", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
-                ("rows_per_lane", ctypes.c_int)]
+                ("rows_per_lane", ctypes.c_int), ("coef_pass", ctypes.c_int)]
 
 
 def load_library(path: str = LIB_PATH):
@@ -113,18 +113,25 @@ def status_string(status: int) -> str:
 GATE_LAMV_SOFTPLUS, GATE_A_SIGMOID, GATE_PBAR_SOFTPLUS, GATE_PBAR_OU = 1, 2, 4, 8
 
 
-def options(strategy: str | int = "auto", chunk_len: int = 0, rows_per_lane: int = 0, gates: int = 0) -> Options:
+# kla_coef_pass values
+_COEF_PASS = {"auto": 0, "off": 1, "on": 2}
+
+
+def options(strategy: str | int = "auto", chunk_len: int = 0, rows_per_lane: int = 0, gates: int = 0,
+            coef_pass: str | int = "auto") -> Options:
     s = _STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
-    return Options(s, int(chunk_len), int(rows_per_lane), int(gates))
+    c = _COEF_PASS[coef_pass] if isinstance(coef_pass, str) else int(coef_pass)
+    return Options(s, int(chunk_len), int(rows_per_lane), int(gates), c)
 
 
 def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strategy: str | int = "auto",
-         chunk_len: int = 0, num_sms: int | None = None, rows_per_lane: int = 0) -> dict:
+         chunk_len: int = 0, num_sms: int | None = None, rows_per_lane: int = 0,
+         coef_pass: str | int = "auto") -> dict:
     """The launch plan kla_forward uses (for the current device, or for a
     device with ``num_sms`` SMs without touching CUDA)."""
     io_code = {"f32": F32, "bf16": BF16}.get(io, io)
     info = PlanInfo()
-    opt = options(strategy, chunk_len, rows_per_lane)
+    opt = options(strategy, chunk_len, rows_per_lane, coef_pass=coef_pass)
     if num_sms is None:
         st = LIB.kla_plan(B, H, T, dk, dv, io_code, ctypes.byref(opt), ctypes.byref(info))
     else:
@@ -133,7 +140,7 @@ def plan(B: int, H: int, T: int, dk: int, dv: int, io: str | int = "bf16", strat
     return {"strategy": {SEQUENTIAL: "sequential", CHUNKED: "chunked"}[info.strategy],
             "chunk_len": info.chunk_len, "num_chunks": info.num_chunks,
             "cols_per_block": info.cols_per_block, "workspace_bytes": int(info.workspace_bytes),
-            "rows_per_lane": info.rows_per_lane}
+            "rows_per_lane": info.rows_per_lane, "coef_pass": bool(info.coef_pass)}
 
 
 def backward_plan(B: int, H: int, T: int, dk: int, dv: int, num_sms: int | None = None) -> dict:
@@ -172,12 +179,13 @@ def _need(t, name, dtype, shape, device):
 def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None, etaT=None,
             strategy: str | int = "auto", chunk_len: int = 0, workspace=None, stream=None,
             final_state: bool = True, rows_per_lane: int = 0, uncertainty: bool = False, y_var=None,
-            gates: int = 0):
+            gates: int = 0, coef_pass: str | int = "auto"):
     """Whole-sequence KLA scan. Returns ``(y, lamT, etaT)`` (the last two are
     None when ``final_state`` is False and none were given); with
     ``uncertainty`` (or a ``y_var`` buffer) also the variance readout
     ``y_var[t, j] = Σ_i q_i² / λ_{t,i,j}`` as a fourth element. ``gates``: kla_gate
-    bits (GATE_*), the corresponding inputs being pre-activations."""
+    bits (GATE_*), the corresponding inputs being pre-activations.
+    ``coef_pass``: "auto", "off" or "on" (kla_coef_pass; results do not depend on it)."""
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -200,7 +208,7 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
     if final_state and lamT is None:
         lamT = torch.empty(st_shape, dtype=torch.float32, device=dev)
         etaT = torch.empty(st_shape, dtype=torch.float32, device=dev)
-    opt = options(strategy, chunk_len, rows_per_lane, gates)
+    opt = options(strategy, chunk_len, rows_per_lane, gates, coef_pass)
     with torch.cuda.device(dev):
         if workspace is None:
             info = PlanInfo()

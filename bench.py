@@ -419,7 +419,7 @@ def run_kla(args, world, rank, local):
     if args.pass_ in ("conv", "conv_backward"):
         return run_conv(args, world, rank, local, w, stream, backward=args.pass_ == "conv_backward")
 
-    fwd_opt = {"strategy": args.strategy, "chunk_len": args.chunk_len}
+    fwd_opt = {"strategy": args.strategy, "chunk_len": args.chunk_len, "coef_pass": args.coef_pass}
     plan = kla.plan(w.B, w.H, w.T, w.dk, w.dv, w.io, **fwd_opt)
     ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev) if plan["workspace_bytes"] else None
     y = torch.empty((w.B, w.H, w.T, w.dv), dtype=x["q"].dtype, device=dev)
@@ -485,7 +485,7 @@ def run_kla(args, world, rank, local):
     except (KeyError, OSError, ValueError):
         pass
     cpu_value, cpu_desc = cpu_oracle_sample(wname, os.cpu_count() or 1)
-    launches_per_step = 1 if plan["strategy"] == "sequential" else 3
+    launches_per_step = (2 if plan["coef_pass"] else 1) if plan["strategy"] == "sequential" else 3
     l2_note = (f"inputs ({in_bytes / 1e6:.0f} MB) fit in L2: {L2_FLUSH_BYTES >> 20} MB written between steps, "
                "step time from per-launch events" if flush else
                f"inputs ({in_bytes / 1e6:.0f} MB) larger than L2; no flush")
@@ -497,11 +497,12 @@ def run_kla(args, world, rank, local):
                    "B": w.B, "H": w.H,
                    "T": w.T, "dk": w.dk, "dv": w.dv, "io": w.io, "strategy": plan["strategy"],
                    "chunk_len": plan["chunk_len"], "cols_per_block": plan["cols_per_block"],
-                   "rows_per_lane": plan["rows_per_lane"],
+                   "rows_per_lane": plan["rows_per_lane"], "coef_pass": plan["coef_pass"],
                    "l2": l2_note, "parallelism": f"{world} independent batches"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": achieved / peak_tflops, "traffic": traffic,
-                     "kernel": "kla_scan_kernel" if plan["strategy"] == "sequential" else "whole chunked pass",
+                     "kernel": ("whole pass: kla_coef_kernel + kla_scan_kernel" if plan["coef_pass"] else
+                                "kla_scan_kernel") if plan["strategy"] == "sequential" else "whole chunked pass",
                      "kernel_ms": per_launch_ms,
                      "peak_basis": f"{nsm} SMs x 128 fp32 lanes x 2 flop x {sm_mhz:.0f} MHz (max SM clock)",
                      "flops_per_launch": flops},
@@ -884,6 +885,8 @@ def main(argv=None):
                     help="force the forward's strategy (default: the planner's choice)")
     ap.add_argument("--chunk-len", dest="chunk_len", type=int, default=0,
                     help="tokens per chunk with --strategy chunked (0: the planner's choice)")
+    ap.add_argument("--coef-pass", dest="coef_pass", choices=("auto", "off", "on"), default="auto",
+                    help="the sequential plan's coefficient pass (kla_coef_pass; default: the planner's choice)")
     args = ap.parse_args(argv)
     world, rank, local = dist_info()
     if world > 1:

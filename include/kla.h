@@ -94,6 +94,20 @@ typedef enum kla_gate {
   KLA_GATE_PBAR_OU = 8
 } kla_gate;
 
+/* The coefficient pass of the sequential plan. The scan's per-row
+ * coefficients of a token (from k, a, p̄, q and k of the token before) serve
+ * every column of the head. When a head's columns are split over several
+ * thread blocks, each block would build them again; with the pass, one
+ * kernel writes them once per (token, row) into the workspace
+ * (B·H·T·5·d_k fp32) and the scan blocks copy them. Results are bit for bit
+ * those without the pass. kla_forward only: the chunked plan, the
+ * uncertainty readout and the other entry points do not use it. */
+typedef enum kla_coef_pass {
+  KLA_COEF_AUTO = 0, /* when a head's columns span 4 or more blocks and the workspace is at most 16 GiB */
+  KLA_COEF_OFF = 1,
+  KLA_COEF_ON = 2    /* whenever the plan is sequential */
+} kla_coef_pass;
+
 typedef struct kla_options {
   int strategy;      /* kla_strategy */
   int chunk_len;     /* tokens per chunk for KLA_CHUNKED; 0 = automatic; multiple of 32 */
@@ -101,6 +115,7 @@ typedef struct kla_options {
                         another value is INVALID_ARG. Results do not depend on it. */
   int gates;         /* kla_gate bits (0 = inputs are a, p̄, Λ^v themselves); unknown bits or both
                         p̄ bits are INVALID_ARG */
+  int coef_pass;     /* kla_coef_pass; another value is INVALID_ARG. Results do not depend on it. */
 } kla_options;
 
 /* The launch plan kla_forward would use for this shape on the current device. */
@@ -111,6 +126,8 @@ typedef struct kla_plan_info {
   int cols_per_block;     /* d_v columns handled by one thread block          */
   size_t workspace_bytes; /* device workspace kla_forward needs (0 if none)   */
   int rows_per_lane;      /* d_k rows one lane of the scan kernel holds (4, 8) */
+  int coef_pass;          /* 1: kla_forward runs the coefficient pass (its buffer is part of
+                             workspace_bytes); 0: it does not */
 } kla_plan_info;
 
 /* Plan for the current CUDA device. Errors: INVALID_ARG (out NULL, negative
@@ -135,8 +152,11 @@ size_t kla_forward_workspace_size(int B, int H, int T, int dk, int dv, const kla
  *   lamT, etaT [B,H,dk,dv] fp32 final state (may be NULL; may alias lam0 /
  *     eta0 exactly for an in-place update; partial overlap is not allowed).
  *   workspace / ws_bytes: device scratch of at least
- *     kla_forward_workspace_size() bytes (may be NULL when that is 0).
- *   opt: NULL means KLA_AUTO with an automatic chunk length. */
+ *     kla_forward_workspace_size() bytes (may be NULL when that is 0): the
+ *     chunked plan's chunk maps, or the sequential plan's coefficient pass
+ *     (kla_coef_pass); the sequential plan without the pass needs none.
+ *   opt: NULL means KLA_AUTO with an automatic chunk length and
+ *     KLA_COEF_AUTO. */
 kla_status kla_forward(const void* q, const void* k, const void* v, const void* lam_v,
                        const void* a, const void* pbar, const float* lam0, const float* eta0,
                        void* y, float* lamT, float* etaT,
@@ -155,7 +175,9 @@ kla_status kla_forward(const void* q, const void* k, const void* v, const void* 
  *   reduction over d_k). Where that kernel's shared memory would not fit
  *   (d_k = 128 with 32-column blocks) the library instead
  *   runs a separate pass without the mean before the main pass, so in-place
- *   λ0/η0 → λ_T/η_T updates stay correct either way. */
+ *   λ0/η0 → λ_T/η_T updates stay correct either way. The coefficient pass
+ *   (kla_coef_pass) is not used here, so the workspace this needs is at most
+ *   kla_forward_workspace_size(). */
 kla_status kla_forward_uncertainty(const void* q, const void* k, const void* v, const void* lam_v,
                                    const void* a, const void* pbar, const float* lam0, const float* eta0,
                                    void* y, void* y_var, float* lamT, float* etaT,

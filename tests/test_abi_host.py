@@ -86,6 +86,8 @@ def test_state_pointers_must_come_in_pairs_and_not_overlap():
 
 def test_bad_io_and_options():
     assert fwd(io=7) == kla.ERR_INVALID_ARG
+    for c in (-1, 3):
+        assert fwd(opt=ctypes.byref(kla.Options(kla.AUTO, 0, 0, 0, c))) == kla.ERR_INVALID_ARG
     assert fwd(opt=ctypes.byref(kla.Options(9, 0))) == kla.ERR_INVALID_ARG
     assert fwd(opt=ctypes.byref(kla.Options(kla.CHUNKED, 48))) == kla.ERR_INVALID_ARG
     assert fwd(opt=ctypes.byref(kla.Options(kla.CHUNKED, -32))) == kla.ERR_INVALID_ARG
@@ -126,6 +128,38 @@ def test_planner_headline_shape_is_sequential_on_152_sms():
     assert 64 % p["cols_per_block"] == 0
 
 
+def test_planner_coefficient_pass():
+    """kla_coef_pass: automatic when a head's columns span four or more
+    blocks (the medium and long workloads on 152 SMs), never for one block
+    per head (the headline) or on the chunked plan; its buffer is
+    B·H·T·5·d_k fp32 and is the plan's whole workspace."""
+    coef_bytes = lambda B, H, T, dk: B * H * T * 5 * dk * 4
+    med = kla.plan(4, 8, 2048, 64, 64, "f32", num_sms=152)
+    assert med["strategy"] == "sequential" and 64 // med["cols_per_block"] >= 4
+    assert med["coef_pass"] and med["workspace_bytes"] == coef_bytes(4, 8, 2048, 64)
+    long_ = kla.plan(1, 16, 65536, 128, 128, "bf16", num_sms=152)
+    assert long_["strategy"] == "sequential" and long_["coef_pass"]
+    assert long_["workspace_bytes"] == coef_bytes(1, 16, 65536, 128)
+    head = kla.plan(8, 16, 4096, 64, 64, "bf16", num_sms=152)
+    assert head["cols_per_block"] == 64 and not head["coef_pass"] and head["workspace_bytes"] == 0
+    # forced on / off; the geometry does not depend on it
+    on = kla.plan(8, 16, 4096, 64, 64, "bf16", coef_pass="on", num_sms=152)
+    assert on["coef_pass"] and on["workspace_bytes"] == coef_bytes(8, 16, 4096, 64)
+    assert {k: v for k, v in on.items() if k not in ("coef_pass", "workspace_bytes")} == \
+        {k: v for k, v in head.items() if k not in ("coef_pass", "workspace_bytes")}
+    off = kla.plan(4, 8, 2048, 64, 64, "f32", coef_pass="off", num_sms=152)
+    assert not off["coef_pass"] and off["workspace_bytes"] == 0 and off["cols_per_block"] == med["cols_per_block"]
+    # the chunked plan never takes it, even when asked to
+    ch = kla.plan(1, 2, 16384, 64, 64, "bf16", strategy="chunked", coef_pass="on", num_sms=152)
+    assert ch["strategy"] == "chunked" and not ch["coef_pass"]
+    # empty sequences and batches need nothing
+    assert kla.plan(4, 8, 0, 64, 64, "f32", coef_pass="on", num_sms=152)["workspace_bytes"] == 0
+    assert kla.plan(0, 8, 64, 64, 64, "f32", coef_pass="on", num_sms=152)["workspace_bytes"] == 0
+    # above 16 GiB the automatic choice leaves it out
+    big = kla.plan(1, 16, 1 << 21, 128, 128, "bf16", strategy="sequential", num_sms=152)
+    assert coef_bytes(1, 16, 1 << 21, 128) > 16 << 30 and not big["coef_pass"] and big["workspace_bytes"] == 0
+
+
 def test_planner_low_parallelism_goes_chunked_and_sizes_workspace():
     p = kla.plan(1, 2, 16384, 64, 64, "bf16", num_sms=152)
     assert p["strategy"] == "chunked"
@@ -135,8 +169,8 @@ def test_planner_low_parallelism_goes_chunked_and_sizes_workspace():
 
 
 def test_planner_forced_strategies_and_chunk_len():
-    seq = kla.plan(1, 2, 16384, 64, 64, "f32", strategy="sequential", num_sms=152)
-    assert seq["strategy"] == "sequential" and seq["workspace_bytes"] == 0
+    seq = kla.plan(1, 2, 16384, 64, 64, "f32", strategy="sequential", coef_pass="off", num_sms=152)
+    assert seq["strategy"] == "sequential" and seq["workspace_bytes"] == 0 and not seq["coef_pass"]
     ch = kla.plan(8, 16, 4096, 64, 64, "bf16", strategy="chunked", chunk_len=1024, num_sms=152)
     assert ch["strategy"] == "chunked" and ch["chunk_len"] == 1024 and ch["num_chunks"] == 4
     # a chunk as long as the sequence leaves nothing to parallelise: sequential
