@@ -32,7 +32,7 @@
 //     several blocks) adds the per-row partial sums of the blocks.
 //
 // Layout of a block: (head, column block of cc columns, all d_k rows). A lane
-// owns one row and CPL = 8 (or, for few heads, 4) consecutive columns (fp32x2
+// owns one row and CPL = 8 (or, for few heads, 4 or 2) consecutive columns (fp32x2
 // pairs), so every
 // per-row sum (dq, dk, da, dp̄) is first a sum inside the lane; a warp covers
 // RW = min(32, d_k) rows and 32/RW column groups; per-column sums (dv, dΛ^v)
@@ -50,7 +50,7 @@ namespace kla {
 namespace {
 
 constexpr int kChunk = 16;  // tokens per checkpoint interval and per staged tile
-constexpr int kCpl = 8;     // columns per lane (4 when a block of 8 would have few warps)
+constexpr int kCpl = 8;     // columns per lane (4 or 2 when a block of 8 would have few warps)
 constexpr int kSub = 4;     // tokens per reverse sub-chunk (states kept in shared memory)
 static_assert(kChunk == kScanTile, "the forward scan checkpoints once per tile");
 
@@ -104,6 +104,19 @@ struct BwdSmem {
                             (size_t)kSub * 2 * cpl * threads + (size_t)kChunk * (4 * dk + 3 * cc));
   }
 };
+
+// UG consecutive column pairs (fp32x2) from 8·UG-byte aligned memory: one
+// 128-bit load for two pairs, one 64-bit load for one.
+template <int UG>
+__device__ __forceinline__ void ld_pairs(const float* src, f2 (&out)[UG]) {
+  if constexpr (UG == 2) {
+    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src);
+    out[0] = v.x;
+    out[1] = v.y;
+  } else {
+    out[0] = *reinterpret_cast<const unsigned long long*>(src);
+  }
+}
 
 template <typename IO>
 __device__ __forceinline__ float ld(const void* base, size_t idx) {
@@ -218,7 +231,8 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane, int& fi
 template <typename IO, int DK, int CPL>
 __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
   using G = BwdGeo<DK, CPL>;
-  constexpr int NP = CPL / 2;  // column pairs per lane
+  constexpr int NP = CPL / 2;            // column pairs per lane
+  constexpr int UG = NP >= 2 ? 2 : 1;    // column pairs per shared- or global-memory load
   extern __shared__ __align__(16) float bwd_smem[];
   const BwdSmem s(bwd_smem, DK, p.cc, CPL);
   const long long bh = blockIdx.x;
@@ -230,11 +244,15 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
 
   auto load_pairs = [&](const float* src, f2 (&P)[NP], f2 (&M)[NP]) {
 #pragma unroll
-    for (int u = 0; u < NP; u += 2) {
-      const ulonglong2 p4 = *reinterpret_cast<const ulonglong2*>(src + ln.e0 + 2 * u);
-      const ulonglong2 m4 = *reinterpret_cast<const ulonglong2*>(src + p.elems + ln.e0 + 2 * u);
-      P[u] = p4.x; P[u + 1] = p4.y;
-      M[u] = m4.x; M[u + 1] = m4.y;
+    for (int u = 0; u < NP; u += UG) {
+      f2 pp[UG], mm[UG];
+      ld_pairs<UG>(src + ln.e0 + 2 * u, pp);
+      ld_pairs<UG>(src + p.elems + ln.e0 + 2 * u, mm);
+#pragma unroll
+      for (int x = 0; x < UG; ++x) {
+        P[u + x] = pp[x];
+        M[u + x] = mm[x];
+      }
     }
   };
   // one forward token (staged token t) on the lane's column pairs
@@ -243,12 +261,12 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
     const f2 a1 = f2_make(at, at), a2 = f2_make(at * at, at * at), pb = f2_make(s.p[t * DK + i], s.p[t * DK + i]);
     const f2 k1 = f2_make(kt, kt), k2 = f2_make(kt * kt, kt * kt);
 #pragma unroll
-    for (int u = 0; u < NP; u += 2) {
-      const ulonglong2 L4 = *reinterpret_cast<const ulonglong2*>(s.L + t * p.cc + jl + 2 * u);
-      const ulonglong2 lv4 = *reinterpret_cast<const ulonglong2*>(s.Lv + t * p.cc + jl + 2 * u);
-      const f2 Ls[2] = {L4.x, L4.y}, Lvs[2] = {lv4.x, lv4.y};
+    for (int u = 0; u < NP; u += UG) {
+      f2 Ls[UG], Lvs[UG];
+      ld_pairs<UG>(s.L + t * p.cc + jl + 2 * u, Ls);
+      ld_pairs<UG>(s.Lv + t * p.cc + jl + 2 * u, Lvs);
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
+      for (int x = 0; x < UG; ++x) {
         const f2 Pp = f2_fma(a2, P[u + x], pb);
         const f2 w = f2_rcp(f2_fma(f2_mul(k2, Ls[x]), Pp, one2));
         const f2 b = f2_mul(k1, Lvs[x]);
@@ -356,13 +374,13 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
         f2 rq = zero, rda1 = zero, rda2 = zero, rdp = zero, rdk1n = zero, rdk2 = zero;
         float cv[2 * CPL];  // per column: k²c̄, then k·b̄
 #pragma unroll
-        for (int u = 0; u < NP; u += 2) {
-          const ulonglong2 L4 = *reinterpret_cast<const ulonglong2*>(s.L + t * p.cc + jl + 2 * u);
-          const ulonglong2 lv4 = *reinterpret_cast<const ulonglong2*>(s.Lv + t * p.cc + jl + 2 * u);
-          const ulonglong2 g4 = *reinterpret_cast<const ulonglong2*>(s.dy + t * p.cc + jl + 2 * u);
-          const f2 Ls[2] = {L4.x, L4.y}, Lvs[2] = {lv4.x, lv4.y}, gs[2] = {g4.x, g4.y};
+        for (int u = 0; u < NP; u += UG) {
+          f2 Ls[UG], Lvs[UG], gs[UG];
+          ld_pairs<UG>(s.L + t * p.cc + jl + 2 * u, Ls);
+          ld_pairs<UG>(s.Lv + t * p.cc + jl + 2 * u, Lvs);
+          ld_pairs<UG>(s.dy + t * p.cc + jl + 2 * u, gs);
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
+          for (int x = 0; x < UG; ++x) {
             const int uu2 = u + x;
             const f2 P0 = Ps(r, uu2), M0 = Ms(r, uu2);
             const f2 Pp = f2_fma(a2, P0, pb);
@@ -502,6 +520,10 @@ cudaError_t launch_bwd_io(int dk, int cpl, const BwdParams& bp, dim3 grid, int t
     case 32 * 16 + 4: return launch_bwd_typed<IO, 32, 4>(bp, grid, threads, smem, s);
     case 64 * 16 + 4: return launch_bwd_typed<IO, 64, 4>(bp, grid, threads, smem, s);
     case 128 * 16 + 4: return launch_bwd_typed<IO, 128, 4>(bp, grid, threads, smem, s);
+    case 16 * 16 + 2: return launch_bwd_typed<IO, 16, 2>(bp, grid, threads, smem, s);
+    case 32 * 16 + 2: return launch_bwd_typed<IO, 32, 2>(bp, grid, threads, smem, s);
+    case 64 * 16 + 2: return launch_bwd_typed<IO, 64, 2>(bp, grid, threads, smem, s);
+    case 128 * 16 + 2: return launch_bwd_typed<IO, 128, 2>(bp, grid, threads, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -539,13 +561,15 @@ BwdPlan backward_plan(long long bh, int T, int dk, int dv, int num_sms) {
     const long long r = std::max(1LL, std::min(std::min(per_sm, by_smem), std::min(by_threads, by_regs)));
     return r * (b.threads / 32);
   };
-  // Eight columns per lane amortise the per-row work best; four columns
-  // double the warps of a block, which pays when eight would leave the SMs
-  // with few warps to hide latency with (few heads).
+  // Eight columns per lane amortise the per-row work best; four (then two)
+  // columns double the warps of a block, which pays when eight would leave
+  // the SMs with few warps to hide latency with (few heads).
   BwdPlan b = geometry(kCpl);
-  if (resident_warps(b) < kMaxWarps) {
-    const BwdPlan b4 = geometry(kCpl / 2);
-    if (resident_warps(b4) > resident_warps(b)) b = b4;
+  for (int cpl = kCpl / 2; cpl >= 2 && resident_warps(b) < kMaxWarps; cpl /= 2) {
+    const BwdPlan n = geometry(cpl);
+    // (a staged column row must be at least 16 bytes in bf16: 8 columns)
+    if (n.cc < 8 || resident_warps(n) <= resident_warps(b)) break;
+    b = n;
   }
   b.ncb = dv / b.cc;
   b.nchunks = (T + kChunk - 1) / kChunk;

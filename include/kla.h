@@ -292,7 +292,7 @@ size_t kla_backward_workspace_size(int B, int H, int T, int dk, int dv);
 /* Launch geometry kla_backward uses. */
 typedef struct kla_backward_plan_info {
   int cols_per_block;     /* d_v columns of one block of the reverse kernel   */
-  int cols_per_lane;      /* 8, or 4 when eight would leave SMs with few warps */
+  int cols_per_lane;      /* 8, or 4 or 2 when eight would leave SMs with few warps */
   int threads;            /* threads per block                                 */
   int column_blocks;      /* d_v / cols_per_block                              */
   size_t workspace_bytes; /* what kla_backward_workspace_size returns          */

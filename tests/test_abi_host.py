@@ -245,20 +245,28 @@ def test_backward_without_a_device_reports_cuda_error():
 
 def test_backward_plan_geometry_on_a_152_sm_device():
     """Eight columns per lane when the blocks fill the SMs with warps (many
-    heads), four when eight would leave few warps per SM (few heads); the
-    workspace is the 16-token checkpoints plus, with split columns, the fp32
-    per-row partial sums."""
+    heads), four or two when eight would leave few warps per SM (few heads);
+    the workspace is the 16-token checkpoints plus, with split columns, the
+    fp32 per-row partial sums."""
     bp = lambda *shape, sms=152: kla.backward_plan(*shape, num_sms=sms)
     head = bp(8, 16, 4096, 64, 64)
     assert (head["cols_per_lane"], head["cols_per_block"], head["threads"], head["column_blocks"]) == (8, 64, 512, 1)
     assert head["workspace_bytes"] == (4096 // 16 + 1) * 2 * 128 * 64 * 64 * 4
     med = bp(4, 8, 2048, 64, 64)
-    assert (med["cols_per_lane"], med["cols_per_block"], med["threads"], med["column_blocks"]) == (4, 16, 256, 4)
+    assert (med["cols_per_lane"], med["cols_per_block"], med["threads"], med["column_blocks"]) == (2, 16, 512, 4)
     assert med["workspace_bytes"] == (2048 // 16 + 1) * 2 * 32 * 64 * 64 * 4 + 4 * 32 * 2048 * 64 * 4
     assert bp(1, 16, 65536, 128, 128)["cols_per_lane"] == 4
-    # the shapes the GPU parity tests use for four columns per lane
-    for shape in ((8, 8, 24, 16, 64), (8, 8, 19, 32, 32), (4, 4, 40, 64, 64), (1, 16, 21, 128, 128)):
-        assert bp(*shape)["cols_per_lane"] == 4, shape
+    # the GPU parity shapes of tests/test_backward_gpu.py: each head size with two and four columns per lane
+    for shape, cpl in (((8, 8, 24, 16, 64), 2), ((8, 8, 19, 32, 32), 2), ((4, 4, 40, 64, 64), 2),
+                       ((3, 16, 18, 128, 16), 2), ((8, 16, 20, 16, 128), 4), ((3, 16, 22, 32, 128), 4),
+                       ((3, 16, 25, 64, 64), 4), ((1, 16, 21, 128, 128), 4)):
+        assert bp(*shape)["cols_per_lane"] == cpl, shape
+    # no block narrower than 8 columns (a staged bf16 column row is then at least 16 bytes)
+    for sms in (152, 132, 16):
+        for dk in (16, 32, 64, 128):
+            for dv in (16, 32, 64, 128):
+                for bh in (1, 2, 3, 5, 8, 13, 32, 64, 128, 1024):
+                    assert bp(1, bh, 40, dk, dv, sms=sms)["cols_per_block"] >= 8
     assert bp(1, 1, 40, 16, 16)["cols_per_lane"] == 8
     for shape in ((8, 16, 4096, 64, 64), (4, 8, 2048, 64, 64), (3, 5, 77, 32, 128)):
         p = bp(*shape)

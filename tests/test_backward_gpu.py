@@ -92,11 +92,17 @@ SHAPES = [
     (1, 1, 8, 16, 16, "f32"),
     (1, 1, 9, 32, 16, "f32"),
     (1, 2, 46, 64, 32, "f32"),
-    # enough heads that the planner gives the reverse kernel four columns per
-    # lane on a 152-SM device (checked on the host in test_abi_host.py)
+    # head counts for which the planner gives the reverse kernel two or four
+    # columns per lane on a 152-SM device, every head size with each (checked
+    # on the host in test_abi_host.py): two columns
     (8, 8, 24, 16, 64, "f32"),
     (8, 8, 19, 32, 32, "bf16"),
     (4, 4, 40, 64, 64, "f32"),
+    (3, 16, 18, 128, 16, "bf16"),
+    # four columns
+    (8, 16, 20, 16, 128, "f32"),
+    (3, 16, 22, 32, 128, "bf16"),
+    (3, 16, 25, 64, 64, "f32"),
     (1, 16, 21, 128, 128, "bf16"),
 ]
 
