@@ -50,7 +50,10 @@
 // do nothing but the recurrence; the producers' work overlaps it, and their
 // raw-tile loads have a whole tile of scanning to land. The per-row coefficients
 // (A, B, 1/a, k/K, q) are computed once per (t, i) and serve all CC columns;
-// the per-column terms (Λ^v, Λ^v v) once per (t, j) for all d_k rows.
+// the per-column terms (Λ^v, Λ^v v) once per (t, j) for all d_k rows. When a
+// head's columns span several blocks, the coefficient pass (kla_coef_kernel)
+// computes the per-row coefficients once for all of them and the producers
+// (MODE 4) copy each tile's coefficients instead of building them.
 // ---------------------------------------------------------------------------
 #pragma once
 
