@@ -208,7 +208,9 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
     if final_state and lamT is None:
         lamT = torch.empty(st_shape, dtype=torch.float32, device=dev)
         etaT = torch.empty(st_shape, dtype=torch.float32, device=dev)
-    opt = options(strategy, chunk_len, rows_per_lane, gates, coef_pass)
+    # the uncertainty readout never runs the coefficient pass: size its workspace without it
+    want_var = uncertainty or y_var is not None
+    opt = options(strategy, chunk_len, rows_per_lane, gates, "off" if want_var else coef_pass)
     with torch.cuda.device(dev):
         if workspace is None:
             info = PlanInfo()
@@ -216,7 +218,7 @@ def forward(q, k, v, lam_v, a, pbar, lam0=None, eta0=None, *, y=None, lamT=None,
             nbytes = int(info.workspace_bytes)
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-        if uncertainty or y_var is not None:
+        if want_var:
             if y_var is None:
                 y_var = torch.empty((B, H, T, dv), dtype=dt, device=dev)
             else:

@@ -8,6 +8,8 @@ in-place state updates — and match the oracle ("Technische Samenvatting:
 Kalman Linear Attention (KLA)", Methodologie §1–§2) where the planner takes it
 by itself.
 """
+import ctypes
+
 import pytest
 import torch
 
@@ -88,8 +90,21 @@ def test_uncertainty_readout_ignores_the_pass():
     x = to_dev(make_inputs(1, 2, 64, 64, 64, io="f32", seed=514, random_state=True))
     a = gpu_forward(x, coef_pass="off", uncertainty=True)
     b = gpu_forward(x, coef_pass="on", uncertainty=True)
+    # through the C ABI directly: asked for, the pass is still not run, so no workspace is needed
+    y, yv = torch.empty_like(a[0]), torch.empty_like(a[3])
+    lT, eT = torch.empty_like(a[1]), torch.empty_like(a[2])
+    opt = kla.options(coef_pass="on")
+    st = kla.LIB.kla_forward_uncertainty(*(ctypes.c_void_p(x[n].data_ptr()) for n in
+                                           ("q", "k", "v", "lam_v", "a", "pbar", "lam0", "eta0")),
+                                         ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(yv.data_ptr()),
+                                         ctypes.c_void_p(lT.data_ptr()), ctypes.c_void_p(eT.data_ptr()),
+                                         1, 2, 64, 64, 64, kla.F32, None, 0, ctypes.byref(opt),
+                                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
+    assert st == kla.OK
     for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    for u, v in zip(a, (y, lT, eT, yv)):
         assert torch.equal(u, v)
 
 
