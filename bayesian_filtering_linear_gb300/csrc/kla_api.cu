@@ -114,9 +114,14 @@ double pass_cost(long long bh, int dk, int rl, int dv, int io, int cc, int tile,
 }
 
 // The coefficient pass (kla_coef_pass) under KLA_COEF_AUTO: taken when a
-// head's columns span at least this many blocks (each would build the same
-// per-row coefficients) and its buffer is at most kCoefMaxBytes.
+// head's columns span at least kCoefMinBlocks blocks (each would build the
+// same per-row coefficients) of at most kCoefMaxCols columns (a block's
+// per-row work is shared by its columns, so it weighs more in narrow
+// blocks), and its buffer is at most kCoefMaxBytes. Measured on GB300: 4 or
+// 8 blocks of 16 columns 10-12% faster with the pass; 4 blocks of 32 columns
+// 1% slower, 2 blocks of 32 columns 8% slower, one block of 64 14% slower.
 constexpr int kCoefMinBlocks = 4;
+constexpr int kCoefMaxCols = 16;
 constexpr size_t kCoefMaxBytes = (size_t)16 << 30;
 
 // allow_coef: the caller can run the coefficient pass (kla_forward's plain
@@ -203,7 +208,7 @@ kla_status make_plan(int B, int H, int T, int dk, int dv, int io, const kla_opti
   }
   const int coef = opt ? opt->coef_pass : KLA_COEF_AUTO;
   if (allow_coef && p.strategy == KLA_SEQUENTIAL && bh > 0 && T > 0 && coef != KLA_COEF_OFF) {
-    const bool split = dv / p.cols_per_block >= kCoefMinBlocks;
+    const bool split = dv / p.cols_per_block >= kCoefMinBlocks && p.cols_per_block <= kCoefMaxCols;
     p.coef_pass = coef == KLA_COEF_ON || (split && kla::coef_workspace_bytes(bh, T, dk) <= kCoefMaxBytes);
   }
   p.ws_bytes = p.strategy == KLA_CHUNKED ? kla::chunk_workspace_bytes(elems, p.num_chunks)

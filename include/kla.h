@@ -103,7 +103,8 @@ typedef enum kla_gate {
  * those without the pass. kla_forward only: the chunked plan, the
  * uncertainty readout and the other entry points do not use it. */
 typedef enum kla_coef_pass {
-  KLA_COEF_AUTO = 0, /* when a head's columns span 4 or more blocks and the workspace is at most 16 GiB */
+  KLA_COEF_AUTO = 0, /* when a head's columns span 4 or more blocks of at most 16 columns and the
+                        workspace is at most 16 GiB */
   KLA_COEF_OFF = 1,
   KLA_COEF_ON = 2    /* whenever the plan is sequential */
 } kla_coef_pass;

@@ -130,9 +130,9 @@ def test_planner_headline_shape_is_sequential_on_152_sms():
 
 def test_planner_coefficient_pass():
     """kla_coef_pass: automatic when a head's columns span four or more
-    blocks (the medium and long workloads on 152 SMs), never for one block
-    per head (the headline) or on the chunked plan; its buffer is
-    B·H·T·5·d_k fp32 and is the plan's whole workspace."""
+    blocks of at most 16 columns (the medium and long workloads on 152 SMs),
+    never for one block per head (the headline) or on the chunked plan; its
+    buffer is B·H·T·5·d_k fp32 and is the plan's whole workspace."""
     coef_bytes = lambda B, H, T, dk: B * H * T * 5 * dk * 4
     med = kla.plan(4, 8, 2048, 64, 64, "f32", num_sms=152)
     assert med["strategy"] == "sequential" and 64 // med["cols_per_block"] >= 4
@@ -142,6 +142,10 @@ def test_planner_coefficient_pass():
     assert long_["workspace_bytes"] == coef_bytes(1, 16, 65536, 128)
     head = kla.plan(8, 16, 4096, 64, 64, "bf16", num_sms=152)
     assert head["cols_per_block"] == 64 and not head["coef_pass"] and head["workspace_bytes"] == 0
+    # four blocks of 32 columns, or two of 32: the per-row work weighs too little there
+    for shape in ((8, 8, 2048, 128, 128, "f32"), (4, 16, 4096, 64, 64, "bf16")):
+        p = kla.plan(*shape, num_sms=152)
+        assert p["cols_per_block"] == 32 and not p["coef_pass"] and p["workspace_bytes"] == 0, (shape, p)
     # forced on / off; the geometry does not depend on it
     on = kla.plan(8, 16, 4096, 64, 64, "bf16", coef_pass="on", num_sms=152)
     assert on["coef_pass"] and on["workspace_bytes"] == coef_bytes(8, 16, 4096, 64)
