@@ -100,8 +100,10 @@ typedef enum kla_gate {
  * thread blocks, each block would build them again; with the pass, one
  * kernel writes them once per (token, row) into the workspace
  * (B·H·T·5·d_k fp32) and the scan blocks copy them. Results are bit for bit
- * those without the pass. kla_forward only: the chunked plan, the
- * uncertainty readout and the other entry points do not use it. */
+ * those without the pass: it changes how kla_forward runs, not what it
+ * computes (Methodologie §1–§2 of the summary cited above). kla_forward
+ * only: the chunked plan, the uncertainty readout and the other entry points
+ * do not use it. */
 typedef enum kla_coef_pass {
   KLA_COEF_AUTO = 0, /* when a head's columns span 4 or more blocks of at most 16 columns and the
                         workspace is at most 16 GiB */
