@@ -345,6 +345,28 @@ E2E_OVERLAP = ("every step copies its own inputs in from pinned host memory and 
                "buffer sets the copies run on their own streams and overlap the neighbouring steps' compute")
 
 
+def packed_inputs(tensors: dict, device, nbuf: int):
+    """One pinned host byte buffer holding `tensors` back to back (each at a
+    16-byte aligned offset), `nbuf` device byte buffers of the same layout,
+    and per buffer the tensors as views into it, so that a step's inputs move
+    in one host-to-device copy. Returns (host, device buffers, views, bytes)."""
+    import torch
+    offs, total = {}, 0
+    for n, t in tensors.items():
+        offs[n] = total
+        total += -(-t.numel() * t.element_size() // 16) * 16
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for n, t in tensors.items():
+        raw = t.detach().contiguous().reshape(-1).cpu().view(torch.uint8)
+        host[offs[n]:offs[n] + raw.numel()].copy_(raw)
+    flats = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(nbuf)]
+
+    def views(flat):
+        return {n: flat[offs[n]:offs[n] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for n, t in tensors.items()}
+    return host, flats, [views(f) for f in flats], total
+
+
 def pipelined_e2e(copy_in, compute, copy_out, args, world, stream, nbuf=E2E_BUFFERS) -> float:
     """Mean ms of an end-to-end step, slowest rank, with `nbuf` sets of device
     buffers: step i copies its inputs into set i % nbuf on one stream,
@@ -445,17 +467,14 @@ def run_kla(args, world, rank, local):
 
     # ---- end to end through host buffers: H2D of the inputs, the call, D2H of
     # the outputs, every step, inside the timed region ------------------------
-    host = {n: x[n].cpu().pin_memory() for n in names}
     nb = E2E_BUFFERS
-    devb = [{n: torch.empty_like(x[n]) for n in names} for _ in range(nb)]
+    host, flat, devb, h2d = packed_inputs({n: x[n] for n in names}, dev, nb)
     outs = [(torch.empty_like(y), torch.empty_like(lamT), torch.empty_like(etaT)) for _ in range(nb)]
     outs_h = [tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in o) for o in outs]
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0])
 
-    def copy_in(b, s):
-        for n in names:
-            devb[b][n].copy_(host[n], non_blocking=True)
+    def copy_in(b, s):  # the step's eight inputs, packed: one copy
+        flat[b].copy_(host, non_blocking=True)
 
     def compute(b, s):
         d, (yb, lb, eb) = devb[b], outs[b]
@@ -658,20 +677,15 @@ def run_kla_backward(args, world, rank, local, w, x, stream):
     tokens = w.B * w.H * w.T
     value = tokens * world / (ms_per_step * 1e-3)
 
-    host = {n: x[n].cpu().pin_memory() for n in names}
-    host_up = {"gy": gy.cpu().pin_memory(), "gl": gl.cpu().pin_memory(), "ge": ge.cpu().pin_memory()}
     nb = E2E_BUFFERS
-    devb = [{n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in list(host.items()) + list(host_up.items())}
-            for _ in range(nb)]
+    host, flat, devb, h2d = packed_inputs(dict({n: x[n] for n in names}, gy=gy, gl=gl, ge=ge), dev, nb)
     sample = kla.backward(*(x[n] for n in names), gy=gy, glamT=gl, getaT=ge, workspace=ws, stream=stream)
     outs_h = [{n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in sample.items()} for _ in range(nb)]
-    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_up.values()))
     d2h = sum(t.numel() * t.element_size() for t in outs_h[0].values())
     results = [None] * nb
 
     def copy_in(b, s):
-        for n, t in list(host.items()) + list(host_up.items()):
-            devb[b][n].copy_(t, non_blocking=True)
+        flat[b].copy_(host, non_blocking=True)  # inputs and upstream gradients, packed: one copy
 
     def compute(b, s):  # the gradients are allocated on `s` (the current stream here)
         d = devb[b]
