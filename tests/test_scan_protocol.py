@@ -16,6 +16,10 @@ every tile count and many random interleavings, that
 
 Planted protocol mistakes (a dropped barrier, a buffer reused one step early)
 must each be caught, so the checker itself is pinned.
+
+The same checks cover the kernel's MODE 4, whose producers copy each tile's
+per-row coefficients (the coefficient pass's output) into coef[b] with
+cp.async once the scan has released that buffer, instead of building them.
 """
 import random
 
@@ -37,7 +41,7 @@ def producer_ops(ntiles, p, mutant=None):
     def build(m):
         b = m % 2
         ops.append(("acc", [("r", f"raw{b}", None), ("r", f"kprev{b}", None),
-                            ("w", f"coef{b}", p), ("w", f"kprev{b ^ 1}", p)]))
+                            ("w", f"coef{b}", p), ("w", f"pj{b}", p), ("w", f"kprev{b ^ 1}", p)]))
 
     stage(0)
     ops.append(("commit",))
@@ -78,6 +82,58 @@ def producer_ops(ntiles, p, mutant=None):
     return ops
 
 
+def producer_ops_pre(ntiles, p, mutant=None):
+    """MODE 4: the producers stage only the per-column inputs (raw[b]) and
+    copy the tile's coefficients straight into coef[b]; K of the last token
+    (kprev[ntiles % 2]) is written once at the start."""
+    ops = []
+
+    def stage_cols(n):
+        ops.append(("stage", f"raw{n % 2}", p))
+
+    def fetch(n):  # cp.async of tile n's coefficients into coef[n % 2]
+        ops.append(("stage", f"coef{n % 2}", p))
+
+    def cols(m):
+        ops.append(("acc", [("r", f"raw{m % 2}", None), ("w", f"pj{m % 2}", p)]))
+
+    ops.append(("acc", [("w", f"kprev{ntiles % 2}", p)]))
+    stage_cols(0)
+    fetch(0)
+    ops.append(("commit",))
+    if ntiles > 1:
+        stage_cols(1)
+        fetch(1)
+    ops.append(("commit",))
+    ops.append(("wait", 1))
+    ops.append(("sync", PROD))
+    cols(0)
+    ops.append(("arrive", FULL[0]))
+    if ntiles > 1:
+        ops.append(("wait", 0))
+        ops.append(("sync", PROD))
+        cols(1)
+        ops.append(("arrive", FULL[1]))
+    for n in range(ntiles):
+        b = n % 2
+        if n + 2 < ntiles:
+            stage_cols(n + 2)
+        ops.append(("commit",))
+        if n + 2 < ntiles and mutant == "fetch_before_empty":
+            fetch(n + 2)
+        ops.append(("sync", EMPTY[b]))
+        if n + 2 < ntiles and mutant != "fetch_before_empty":
+            fetch(n + 2)
+        ops.append(("commit",))
+        ops.append(("acc", [("r", f"ypart{b}", None), ("w", "y", p)]))  # store_y(n)
+        if n + 2 < ntiles:
+            ops.append(("wait", 0))
+            ops.append(("sync", PROD))
+            cols(n + 2)
+            ops.append(("arrive", FULL[b]))
+    return ops
+
+
 def scanner_ops(ntiles, c, mutant=None):
     ops = []
     for n in range(ntiles):
@@ -88,7 +144,7 @@ def scanner_ops(ntiles, c, mutant=None):
             ops.append(("acc", [("r", f"coef{b}", None), ("w", f"ypart{b}", c)]))
             continue
         ops.append(("sync", FULL[b]))
-        ops.append(("acc", [("r", f"coef{b}", None), ("w", f"ypart{b}", c)]))
+        ops.append(("acc", [("r", f"coef{b}", None), ("r", f"pj{b}", None), ("w", f"ypart{b}", c)]))
         ops.append(("arrive", EMPTY[b]))
     ops.append(("acc", [("r", f"kprev{ntiles % 2}", None)]))  # final state reads K of the last token
     return ops
@@ -98,11 +154,11 @@ class Race(Exception):
     pass
 
 
-def run(ntiles, n_prod, n_scan, seed, mutant=None):
-    """Simulate one interleaving. Returns True when every warp finished;
-    raises Race on an unordered conflicting access."""
+def run(ntiles, n_prod, n_scan, seed, mutant=None, pre=False):
+    """Simulate one interleaving (pre: the MODE 4 producers). Returns True
+    when every warp finished; raises Race on an unordered conflicting access."""
     rnd = random.Random(seed)
-    progs = [producer_ops(ntiles, p, mutant) for p in range(n_prod)]
+    progs = [(producer_ops_pre if pre else producer_ops)(ntiles, p, mutant) for p in range(n_prod)]
     progs += [scanner_ops(ntiles, n_prod + c, mutant) for c in range(n_scan)]
     nw = len(progs)
     count = {FULL[0]: nw, FULL[1]: nw, EMPTY[0]: nw, EMPTY[1]: nw, PROD: n_prod}
@@ -190,9 +246,23 @@ def run(ntiles, n_prod, n_scan, seed, mutant=None):
 
 
 @pytest.mark.parametrize("ntiles", range(1, 8))
-def test_protocol_has_no_deadlock_and_no_race(ntiles):
+@pytest.mark.parametrize("pre", [False, True], ids=["build", "copy"])
+def test_protocol_has_no_deadlock_and_no_race(ntiles, pre):
     for seed in range(150):
-        assert run(ntiles, n_prod=2, n_scan=3, seed=seed), f"deadlock at {ntiles} tiles, seed {seed}"
+        assert run(ntiles, n_prod=2, n_scan=3, seed=seed, pre=pre), f"deadlock at {ntiles} tiles, seed {seed}"
+
+
+def test_copy_mode_fetching_before_the_scan_released_the_buffer_is_caught():
+    """The copy of tile n+2's coefficients issued before the EMPTY wait of
+    tile n would overwrite coef[b] while the scan still reads it."""
+    caught = False
+    for seed in range(300):
+        try:
+            run(5, n_prod=2, n_scan=3, seed=seed, mutant="fetch_before_empty", pre=True)
+        except Race:
+            caught = True
+            break
+    assert caught
 
 
 @pytest.mark.parametrize("mutant", ["no_producer_barrier", "stage_after_empty", "arrive_before_scan",
