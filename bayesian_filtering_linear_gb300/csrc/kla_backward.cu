@@ -76,21 +76,19 @@ struct BwdGeo {
   static constexpr int NWR = DK / RW;           // warps along rows
 };
 
-// Shared memory of one block (fp32): staged per-row inputs q, k, a, p̄
-// [kChunk][DK] and per-column inputs v, Λ^v, Λ^v·v, dy [kChunk][cc], the
+// Shared memory of one block (fp32): staged per-row inputs (a, k, p̄, q)
+// interleaved per (token, row) [kChunk][DK][4] (one 128-bit load gives a
+// lane its row's four) and per-column inputs v, Λ^v, Λ^v·v, dy [kChunk][cc], the
 // per-token accumulators of the row sums [kChunk][4][DK] and column sums
 // [kChunk][2][cc], and each thread's states before the tokens of the current
 // sub-chunk, [kSub][2][cpl/2][threads] fp32x2 (thread-fastest, so a warp's
 // accesses are contiguous).
 struct BwdSmem {
-  float *q, *k, *a, *p, *v, *L, *Lv, *dy, *racc, *cacc, *st;
+  float *rw, *v, *L, *Lv, *dy, *racc, *cacc, *st;
   unsigned char* raw;  // the next chunk's inputs as loaded (I/O dtype), filled by cp.async
   __device__ BwdSmem(float* base, int dk, int cc, int cpl) {
-    q = base;
-    k = q + kChunk * dk;
-    a = k + kChunk * dk;
-    p = a + kChunk * dk;
-    v = p + kChunk * dk;
+    rw = base;
+    v = rw + 4 * kChunk * dk;
     L = v + kChunk * cc;
     Lv = L + kChunk * cc;
     dy = Lv + kChunk * cc;
@@ -157,11 +155,10 @@ __device__ void convert_raw(const BwdParams& p, const BwdSmem& s, int tl) {
   const IO *rq = r, *rk = r + kChunk * p.dk, *ra = rk + kChunk * p.dk, *rp = ra + kChunk * p.dk;
   const IO *rv = rp + kChunk * p.dk, *rL = rv + kChunk * p.cc, *rg = rL + kChunk * p.cc;
   for (int x = threadIdx.x; x < tl * p.dk; x += nthr) {
-    s.q[x] = to_f32<IO>(rq[x]);
-    s.k[x] = to_f32<IO>(rk[x]);
     const float xa = to_f32<IO>(ra[x]);
-    s.a[x] = gate_a(xa, p.gates);
-    s.p[x] = gate_pbar(to_f32<IO>(rp[x]), xa, p.gates);
+    *reinterpret_cast<float4*>(s.rw + 4 * x) =
+        make_float4(gate_a(xa, p.gates), to_f32<IO>(rk[x]), gate_pbar(to_f32<IO>(rp[x]), xa, p.gates),
+                    to_f32<IO>(rq[x]));
   }
   for (int x = threadIdx.x; x < tl * p.cc; x += nthr) {
     s.v[x] = to_f32<IO>(rv[x]);
@@ -257,8 +254,9 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
   };
   // one forward token (staged token t) on the lane's column pairs
   auto fwd = [&](int t, f2 (&P)[NP], f2 (&M)[NP]) {
-    const float at = s.a[t * DK + i], kt = s.k[t * DK + i];
-    const f2 a1 = f2_make(at, at), a2 = f2_make(at * at, at * at), pb = f2_make(s.p[t * DK + i], s.p[t * DK + i]);
+    const float4 r4 = *reinterpret_cast<const float4*>(s.rw + 4 * (t * DK + i));  // (a, k, p̄, q)
+    const float at = r4.x, kt = r4.y;
+    const f2 a1 = f2_make(at, at), a2 = f2_make(at * at, at * at), pb = f2_make(r4.z, r4.z);
     const f2 k1 = f2_make(kt, kt), k2 = f2_make(kt * kt, kt * kt);
 #pragma unroll
     for (int u = 0; u < NP; u += UG) {
@@ -366,7 +364,8 @@ __global__ void __launch_bounds__(512, 1) kla_bwd_kernel(const BwdParams p) {
       for (int r = kSub - 1; r >= 0; --r) {
         const int t = ts + r;
         if (t >= tl) continue;
-        const float at = s.a[t * DK + i], kt = s.k[t * DK + i], qt = s.q[t * DK + i], pt = s.p[t * DK + i];
+        const float4 r4 = *reinterpret_cast<const float4*>(s.rw + 4 * (t * DK + i));  // (a, k, p̄, q)
+        const float at = r4.x, kt = r4.y, pt = r4.z, qt = r4.w;
         const f2 a1 = f2_make(at, at), a2 = f2_make(at * at, at * at), pb = f2_make(pt, pt);
         const f2 k1 = f2_make(kt, kt), k2 = f2_make(kt * kt, kt * kt), q1 = f2_make(qt, qt);
         const f2 nk2 = f2_make(-kt * kt, -kt * kt);
